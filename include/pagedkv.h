@@ -1,0 +1,245 @@
+/*
+ * pagedkv.h -- C ABI of libpagedkv.so: single-token decode attention over a
+ * paged KV cache, for NVIDIA GB300 (sm_103a).
+ *
+ * The problem (sources by page title and section):
+ *  - "CS336 · 第 10 课" (inference lecture guide), KV-cache section: at each
+ *    decode step the new token's K/V are appended to the cache and its query
+ *    attends over every cached key, a = softmax(q K^T / sqrt(d_h)), y = a V.
+ *  - "推理优化与 AI Infra" (tiniestgpt notes), section 2: the cache is a pool
+ *    of physical blocks k_cache[block][slot][head][dim] reached through
+ *    block_table[seq][i]; section 5: int8 KV with per_token or per_head
+ *    scales, dequantised after the gather; section 8: static step buffers
+ *    (block_table, seq_lens, slot ids) and a host-side integer bound on the
+ *    KV length so that no device value is read on the host.
+ *  - "实验五：Gemma4 端到端推理优化" (Lab5-Gemma4): sections 滑动窗口注意力
+ *    (window [i-w, i]), 分组查询注意力 (query heads share KV heads), the
+ *    model overview (W_K = W_V on global layers: K and V one tensor), and
+ *    Flash Attention (online softmax with running max/sum, blocks outside
+ *    the window skipped, a separate narrow-query decode kernel).
+ *
+ * Conventions for every call:
+ *  - All pointers are DEVICE pointers unless stated; the caller allocates and
+ *    owns every buffer.  The library allocates no device memory and keeps no
+ *    state except a thread-local error string, an error word in device
+ *    memory (pkv_device_status) and per-device launch attributes.
+ *  - Work is enqueued asynchronously on `stream` (a cudaStream_t; NULL = the
+ *    legacy default stream).  No call synchronises or reads device data on
+ *    the host, so the calls may be captured in a CUDA graph.
+ *  - Return value: 0 (PKV_OK) on success; a negative PKV_E_* code when an
+ *    argument is rejected on the host (nothing is launched; the message is in
+ *    pkv_last_error()); a positive cudaError_t when a launch fails.
+ *  - Errors the host cannot see (a block id outside the pool, a length
+ *    beyond the block table or beyond max_seq_len, a slot outside the pool)
+ *    are detected in the kernels: the offending keys or tokens are skipped
+ *    and a bit is set in the device error word, read with
+ *    pkv_device_status() after the stream has been synchronised.
+ */
+#ifndef PAGEDKV_H
+#define PAGEDKV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define PKV_API __attribute__((visibility("default")))
+#else
+#define PKV_API
+#endif
+
+/* element type of the pool */
+#define PKV_BF16 0
+#define PKV_INT8 1
+/* int8 scale granularity (tiniestgpt notes, section 5: per_token / per_head) */
+#define PKV_SCALE_NONE 0
+#define PKV_SCALE_PER_TOKEN 1
+#define PKV_SCALE_PER_HEAD 2
+/* output element type */
+#define PKV_OUT_BF16 0
+#define PKV_OUT_F32 1
+/* split_tokens value asking the library to choose the split length */
+#define PKV_SPLIT_AUTO (-1)
+
+/* host-side status codes */
+#define PKV_OK 0
+#define PKV_E_NULL (-1)        /* a required pointer is NULL */
+#define PKV_E_SHAPE (-2)       /* inconsistent sizes (e.g. H_q % H_kv != 0) */
+#define PKV_E_UNSUPPORTED (-3) /* head_dim / block_size / dtype not built */
+#define PKV_E_WORKSPACE (-4)   /* workspace missing or too small */
+#define PKV_E_ALIGN (-5)       /* a pointer violates its alignment rule */
+#define PKV_E_ARG (-6)         /* any other invalid argument */
+#define PKV_E_DRIVER (-7)      /* tensor-map encoding / device query failed */
+
+/* device error word bits (pkv_device_status) */
+#define PKV_DEV_BAD_BLOCK 1u    /* block_table entry outside [0, num_blocks) */
+#define PKV_DEV_LEN_TABLE 2u    /* seq_len > max_blocks_per_seq * block_size */
+#define PKV_DEV_BAD_SLOT 4u     /* slot_mapping entry >= num_blocks * block_size */
+#define PKV_DEV_TIMEOUT 8u      /* a pipeline wait ran past its limit */
+#define PKV_DEV_LEN_BOUND 16u   /* seq_len > max_seq_len given on the host */
+
+/*
+ * One layer's KV pool (tiniestgpt notes, section 2; one pool per layer).
+ *   k, v:  [num_blocks][block_size][num_kv_heads][head_dim], elements bf16 or
+ *          int8 (dtype).  16-byte aligned.  v == NULL or v == k means K and V
+ *          are one tensor (Lab5-Gemma4 model overview: W_K = W_V on global
+ *          layers); it is then read once per key.
+ *   k_scale, v_scale: fp32 scale tables of an int8 pool.
+ *          PKV_SCALE_PER_TOKEN: [num_blocks * block_size], indexed by slot,
+ *          written by paged_kv_append, 16-byte aligned;
+ *          PKV_SCALE_PER_HEAD:  [num_kv_heads], set by the caller (static).
+ *          Unused (may be NULL) for bf16 pools; v_scale unused when K == V.
+ *   block_size must be 16; head_dim must be 64, 128 or 256.
+ */
+typedef struct pkv_pool {
+    void *k;
+    void *v;
+    float *k_scale;
+    float *v_scale;
+    int32_t num_blocks;
+    int32_t block_size;
+    int32_t num_kv_heads;
+    int32_t head_dim;
+    int32_t dtype;      /* PKV_BF16 | PKV_INT8 */
+    int32_t scale_mode; /* PKV_SCALE_* (PKV_SCALE_NONE only for bf16) */
+} pkv_pool;
+
+/*
+ * paged_kv_append -- write each new token's K and V into its slot.
+ * (CS336 lecture 10, KV-cache section: "append new K/V"; tiniestgpt notes,
+ * sections 2 and 8: slot ids; section 5: int8 quantisation with
+ * scale = max|x|/127, x_q = round(x/scale) from the CS336 guide's int8
+ * section.)
+ *   k, v:          [num_tokens][num_kv_heads][head_dim] bf16, 16-byte
+ *                  aligned; v ignored (may be NULL) when the pool has K == V.
+ *   slot_mapping:  [num_tokens] int64, 8-byte aligned; token t goes to block
+ *                  slot / block_size, offset slot % block_size; a negative
+ *                  slot is padding and is skipped.
+ *   bf16 pool: bit copy.  int8 per token: scale = max|x| / 127 over the
+ *   token's num_kv_heads*head_dim values (fp32, IEEE division), stored at
+ *   scale[slot]; q = clamp(round_half_even(x / scale), -127, 127); a zero
+ *   scale stores zeros.  int8 per head: the same rounding with the caller's
+ *   static scale[h].  K and V are quantised separately.
+ *   Tokens that map to the same slot race (the last writer is unspecified).
+ */
+PKV_API int paged_kv_append(const void *k, const void *v, const int64_t *slot_mapping,
+                            int32_t num_tokens, const pkv_pool *pool, void *stream);
+
+/*
+ * paged_decode_split_tokens -- the split length paged_decode_attention uses
+ * for split_tokens (resolves PKV_SPLIT_AUTO from the batch shape and the
+ * current device's SM count).  Returns 0 for a single pass, a positive
+ * multiple of block_size, or a negative PKV_E_* code.
+ */
+PKV_API int32_t paged_decode_split_tokens(int32_t batch, int32_t num_q_heads,
+                                          int32_t num_kv_heads, int32_t block_size,
+                                          int32_t max_seq_len, int32_t window,
+                                          int32_t split_tokens);
+
+/*
+ * paged_decode_num_splits -- the most key splits a sequence of length at
+ * most max_seq_len can have for a resolved split length (>= 1).
+ */
+PKV_API int32_t paged_decode_num_splits(int32_t block_size, int32_t max_seq_len, int32_t window,
+                                        int32_t split_tokens);
+
+/*
+ * paged_decode_workspace_bytes -- device scratch paged_decode_attention needs
+ * for these sizes (0 when it runs as a single pass).  Layout: partial
+ * log-sum-exp [batch][num_q_heads][num_splits] fp32, then (256-byte
+ * aligned) partial outputs [batch][num_q_heads][num_splits][head_dim] fp32.
+ */
+PKV_API size_t paged_decode_workspace_bytes(int32_t batch, int32_t num_q_heads,
+                                            int32_t num_kv_heads, int32_t head_dim,
+                                            int32_t block_size, int32_t max_seq_len,
+                                            int32_t window, int32_t split_tokens);
+
+/*
+ * paged_decode_attention -- one decode step of one layer: for every sequence
+ * b and query head h,
+ *     out[b][h] = softmax_j(softmax_scale * <q[b][h], K_b[j]>) V_b[j]
+ * over the keys j in [lo, pos], pos = seq_lens[b] - 1,
+ * lo = window > 0 ? max(0, pos - window) : 0 (Lab5-Gemma4 sliding-window
+ * section: position i sees [i-w, i]; window 0 = global causal layer).
+ * K_b[j] is row j % block_size of physical block
+ * block_table[b][j / block_size], kv head h / (num_q_heads / num_kv_heads)
+ * (consecutive query heads share a KV head).  int8 values are dequantised
+ * after the gather.  Online softmax in fp32 (Lab5-Gemma4, Flash Attention
+ * section): scores are never written to memory.  Blocks outside [lo, pos]
+ * are never read.
+ *   q:            [batch][num_q_heads][head_dim] bf16, 16-byte aligned.
+ *   block_table:  [batch][max_blocks_per_seq] int32.
+ *   seq_lens:     [batch] int32, length including the token appended this
+ *                 step; 0 gives a zero output row.
+ *   max_seq_len:  host upper bound on every seq_lens[b] (tiniestgpt notes,
+ *                 section 8); it sizes the grid.
+ *   split_tokens: 0 = single pass; > 0 = split each key range into pieces
+ *                 of this many keys (multiple of block_size) and merge them
+ *                 with a log-sum-exp combine; PKV_SPLIT_AUTO = library's
+ *                 choice.
+ *   workspace:    device scratch of paged_decode_workspace_bytes(...) bytes,
+ *                 256-byte aligned (NULL allowed when that is 0).
+ *   out:          [batch][num_q_heads][head_dim], bf16 (out_dtype
+ *                 PKV_OUT_BF16) or fp32 (PKV_OUT_F32), 16-byte aligned.
+ */
+PKV_API int paged_decode_attention(const void *q, const pkv_pool *pool, const int32_t *block_table,
+                                   int32_t max_blocks_per_seq, const int32_t *seq_lens,
+                                   int32_t batch, int32_t num_q_heads, int32_t max_seq_len,
+                                   int32_t window, float softmax_scale, int32_t split_tokens,
+                                   void *workspace, size_t workspace_bytes, void *out,
+                                   int32_t out_dtype, void *stream);
+
+/*
+ * paged_decode_split_partial -- the first step of the split-KV path: every
+ * (sequence, query head, split s) attends over keys
+ * [lo + s*split_tokens', ...) where split_tokens' counts from the block
+ * holding lo (splits are block-aligned: split s covers logical blocks
+ * lo/bs + s*split_tokens/bs ... of the sequence, clipped to [lo, pos]).
+ * For a sequence whose range has a single split the final output row is
+ * written to `out` directly; otherwise partial_lse[b][h][s] (natural log of
+ * the sum of exp(score)) and partial_o[b][h][s][:] (the split's normalised
+ * output) are written.  split_tokens must be a positive multiple of
+ * block_size; num_splits >= paged_decode_num_splits(...).
+ */
+PKV_API int paged_decode_split_partial(const void *q, const pkv_pool *pool,
+                                       const int32_t *block_table, int32_t max_blocks_per_seq,
+                                       const int32_t *seq_lens, int32_t batch,
+                                       int32_t num_q_heads, int32_t max_seq_len, int32_t window,
+                                       float softmax_scale, int32_t split_tokens,
+                                       float *partial_lse, float *partial_o, int32_t num_splits,
+                                       void *out, int32_t out_dtype, void *stream);
+
+/*
+ * paged_decode_lse_combine -- the second step: for each sequence with more
+ * than one split and each query head,
+ *     L = log sum_s exp(lse_s),   out = sum_s exp(lse_s - L) o_s
+ * (the online-softmax merge of Lab5-Gemma4's Flash Attention section applied
+ * to whole splits).  Sequences with one split are left untouched.  The
+ * split count of each sequence is recomputed from seq_lens, window,
+ * block_size and split_tokens exactly as paged_decode_split_partial does.
+ */
+PKV_API int paged_decode_lse_combine(const float *partial_lse, const float *partial_o,
+                                     const int32_t *seq_lens, int32_t batch, int32_t num_q_heads,
+                                     int32_t head_dim, int32_t block_size, int32_t window,
+                                     int32_t split_tokens, int32_t num_splits, void *out,
+                                     int32_t out_dtype, void *stream);
+
+/* Message of the last host-side error on this thread ("" if none). */
+PKV_API const char *pkv_last_error(void);
+
+/*
+ * pkv_device_status -- the device error word (PKV_DEV_* bits) of the
+ * current device, optionally clearing it.  This call synchronises the
+ * device; call it after the stream's work has finished.  Returns a
+ * negative PKV_E_* code if the device cannot be queried.
+ */
+PKV_API int pkv_device_status(int32_t clear);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PAGEDKV_H */

@@ -1,0 +1,267 @@
+"""ctypes binding of libpagedkv.so (include/pagedkv.h).
+
+Argument marshalling only: tensors become device pointers, the current torch
+stream becomes the cudaStream_t, and status codes become exceptions.  Every
+step of the computation runs in the library's kernels; nothing here computes
+attention, and there is no CPU fallback -- if the library is missing or a
+tensor is not on a CUDA device, the call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+from dataclasses import dataclass
+from typing import Optional
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libpagedkv.so")
+HEADER = os.path.join(os.path.dirname(HERE), "include", "pagedkv.h")
+
+PKV_BF16, PKV_INT8 = 0, 1
+SCALE_NONE, SCALE_PER_TOKEN, SCALE_PER_HEAD = 0, 1, 2
+OUT_BF16, OUT_F32 = 0, 1
+SPLIT_AUTO = -1
+
+_lib = None
+
+
+class PkvPoolC(ctypes.Structure):
+    """Mirror of ``pkv_pool`` in include/pagedkv.h."""
+    _fields_ = [
+        ("k", ctypes.c_void_p),
+        ("v", ctypes.c_void_p),
+        ("k_scale", ctypes.c_void_p),
+        ("v_scale", ctypes.c_void_p),
+        ("num_blocks", ctypes.c_int32),
+        ("block_size", ctypes.c_int32),
+        ("num_kv_heads", ctypes.c_int32),
+        ("head_dim", ctypes.c_int32),
+        ("dtype", ctypes.c_int32),
+        ("scale_mode", ctypes.c_int32),
+    ]
+
+
+def library_path() -> str:
+    return LIB_PATH
+
+
+def load_library():
+    """Load libpagedkv.so (built by ``__graft_entry__.build()``); raise if absent."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError(f"{LIB_PATH} is missing: build it with __graft_entry__.build() "
+                           "(there is no fallback implementation)")
+    lib = ctypes.CDLL(LIB_PATH)
+    p, i32, f32, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_float, ctypes.c_size_t
+    lib.paged_kv_append.argtypes = [p, p, p, i32, p, p]
+    lib.paged_kv_append.restype = ctypes.c_int
+    lib.paged_decode_split_tokens.argtypes = [i32] * 7
+    lib.paged_decode_split_tokens.restype = i32
+    lib.paged_decode_num_splits.argtypes = [i32] * 4
+    lib.paged_decode_num_splits.restype = i32
+    lib.paged_decode_workspace_bytes.argtypes = [i32] * 8
+    lib.paged_decode_workspace_bytes.restype = sz
+    lib.paged_decode_attention.argtypes = [p, p, p, i32, p, i32, i32, i32, i32, f32, i32, p, sz,
+                                           p, i32, p]
+    lib.paged_decode_attention.restype = ctypes.c_int
+    lib.paged_decode_split_partial.argtypes = [p, p, p, i32, p, i32, i32, i32, i32, f32, i32, p,
+                                               p, i32, p, i32, p]
+    lib.paged_decode_split_partial.restype = ctypes.c_int
+    lib.paged_decode_lse_combine.argtypes = [p, p, p, i32, i32, i32, i32, i32, i32, i32, p, i32,
+                                             p]
+    lib.paged_decode_lse_combine.restype = ctypes.c_int
+    lib.pkv_last_error.argtypes = []
+    lib.pkv_last_error.restype = ctypes.c_char_p
+    lib.pkv_device_status.argtypes = [i32]
+    lib.pkv_device_status.restype = ctypes.c_int
+    _lib = lib
+    return lib
+
+
+def exported_symbols():
+    """Names of the functions include/pagedkv.h declares with PKV_API."""
+    with open(HEADER) as f:
+        text = f.read()
+    return re.findall(r"PKV_API\s+[\w\s\*]+?\b(\w+)\s*\(", text)
+
+
+class PagedKVError(RuntimeError):
+    pass
+
+
+def _check(rc: int, what: str):
+    if rc != 0:
+        msg = load_library().pkv_last_error().decode(errors="replace")
+        raise PagedKVError(f"{what} failed ({rc}): {msg}")
+
+
+def _dev_ptr(t, name):
+    import torch
+    if t is None:
+        return None
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise PagedKVError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise PagedKVError(f"{name} must be contiguous")
+    return t.data_ptr()
+
+
+def _stream(stream):
+    import torch
+    if stream is None:
+        return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    if isinstance(stream, torch.cuda.Stream):
+        return ctypes.c_void_p(stream.cuda_stream)
+    return ctypes.c_void_p(int(stream))
+
+
+@dataclass
+class PagedKVPool:
+    """One layer's KV pool as torch device tensors.
+
+    k, v: [num_blocks, block_size, num_kv_heads, head_dim], bf16 or int8;
+    v None means K and V are one tensor.  int8 pools carry fp32 scale tables
+    (per token: [num_blocks * block_size]; per head: [num_kv_heads]).
+    """
+    k: "object"
+    v: Optional[object] = None
+    k_scale: Optional[object] = None
+    v_scale: Optional[object] = None
+    scale_mode: int = SCALE_NONE
+
+    @property
+    def dtype(self) -> int:
+        import torch
+        return PKV_INT8 if self.k.dtype == torch.int8 else PKV_BF16
+
+    @property
+    def num_blocks(self) -> int:
+        return int(self.k.shape[0])
+
+    @property
+    def block_size(self) -> int:
+        return int(self.k.shape[1])
+
+    @property
+    def num_kv_heads(self) -> int:
+        return int(self.k.shape[2])
+
+    @property
+    def head_dim(self) -> int:
+        return int(self.k.shape[3])
+
+    def c_struct(self) -> PkvPoolC:
+        import torch
+        if self.k.dim() != 4:
+            raise PagedKVError("pool k must be [num_blocks, block_size, num_kv_heads, head_dim]")
+        if self.k.dtype not in (torch.bfloat16, torch.int8):
+            raise PagedKVError("pool dtype must be bfloat16 or int8")
+        if self.v is not None and (self.v.shape != self.k.shape or self.v.dtype != self.k.dtype):
+            raise PagedKVError("pool v must match k")
+        for s in (self.k_scale, self.v_scale):
+            if s is not None and s.dtype != torch.float32:
+                raise PagedKVError("scale tables must be float32")
+        return PkvPoolC(_dev_ptr(self.k, "pool.k"), _dev_ptr(self.v, "pool.v"),
+                        _dev_ptr(self.k_scale, "pool.k_scale"), _dev_ptr(self.v_scale, "pool.v_scale"),
+                        self.num_blocks, self.block_size, self.num_kv_heads, self.head_dim,
+                        self.dtype, int(self.scale_mode))
+
+
+def paged_kv_append(k, v, slot_mapping, pool: PagedKVPool, stream=None) -> None:
+    """Write the new tokens' K/V ([T, H_kv, D] bf16) into slots ``slot_mapping``
+    ([T] int64) of ``pool``, quantising to int8 if the pool is int8."""
+    lib = load_library()
+    pc = pool.c_struct()
+    n = int(slot_mapping.shape[0])
+    _check(lib.paged_kv_append(_dev_ptr(k, "k"), _dev_ptr(v, "v"), _dev_ptr(slot_mapping, "slot_mapping"),
+                               n, ctypes.byref(pc), _stream(stream)), "paged_kv_append")
+
+
+def paged_decode_split_tokens(batch, num_q_heads, num_kv_heads, max_seq_len, window,
+                              split_tokens=SPLIT_AUTO, block_size=16) -> int:
+    st = load_library().paged_decode_split_tokens(batch, num_q_heads, num_kv_heads, block_size,
+                                                  max_seq_len, window, split_tokens)
+    if st < 0:
+        _check(st, "paged_decode_split_tokens")
+    return st
+
+
+def paged_decode_num_splits(max_seq_len, window, split_tokens, block_size=16) -> int:
+    return int(load_library().paged_decode_num_splits(block_size, max_seq_len, window, split_tokens))
+
+
+def paged_decode_workspace_bytes(batch, num_q_heads, num_kv_heads, head_dim, max_seq_len, window,
+                                 split_tokens=SPLIT_AUTO, block_size=16) -> int:
+    return int(load_library().paged_decode_workspace_bytes(batch, num_q_heads, num_kv_heads,
+                                                           head_dim, block_size, max_seq_len,
+                                                           window, split_tokens))
+
+
+def paged_decode_attention(q, pool: PagedKVPool, block_table, seq_lens, window: int,
+                           softmax_scale: float, out, max_seq_len: int,
+                           split_tokens: int = SPLIT_AUTO, workspace=None, stream=None):
+    """Decode attention of q [B, H_q, D] (bf16) over ``pool`` into ``out``
+    ([B, H_q, D], bf16 or fp32).  ``max_seq_len`` is the host-side bound on
+    seq_lens.  ``workspace``: a uint8 CUDA tensor of at least
+    paged_decode_workspace_bytes(...) bytes (allocated through torch if None)."""
+    import torch
+    lib = load_library()
+    pc = pool.c_struct()
+    B, Hq, D = (int(x) for x in q.shape)
+    need = lib.paged_decode_workspace_bytes(B, Hq, pool.num_kv_heads, D, pool.block_size,
+                                            max_seq_len, window, split_tokens)
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    ws_ptr = _dev_ptr(workspace, "workspace") if workspace is not None else None
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    out_dtype = OUT_F32 if out.dtype == torch.float32 else OUT_BF16
+    _check(lib.paged_decode_attention(_dev_ptr(q, "q"), ctypes.byref(pc), _dev_ptr(block_table, "block_table"),
+                                      int(block_table.shape[1]), _dev_ptr(seq_lens, "seq_lens"), B, Hq,
+                                      int(max_seq_len), int(window), float(softmax_scale),
+                                      int(split_tokens), ws_ptr, ws_bytes, _dev_ptr(out, "out"),
+                                      out_dtype, _stream(stream)), "paged_decode_attention")
+    return out
+
+
+def paged_decode_split_partial(q, pool: PagedKVPool, block_table, seq_lens, window: int,
+                               softmax_scale: float, split_tokens: int, partial_lse, partial_o,
+                               out, max_seq_len: int, stream=None):
+    """Split-KV step 1: partial_lse [B, H_q, S] and partial_o [B, H_q, S, D]
+    (fp32) for multi-split sequences; final rows of single-split ones in out."""
+    import torch
+    lib = load_library()
+    pc = pool.c_struct()
+    B, Hq, D = (int(x) for x in q.shape)
+    ns = int(partial_lse.shape[2])
+    out_dtype = OUT_F32 if out.dtype == torch.float32 else OUT_BF16
+    _check(lib.paged_decode_split_partial(_dev_ptr(q, "q"), ctypes.byref(pc), _dev_ptr(block_table, "block_table"),
+                                          int(block_table.shape[1]), _dev_ptr(seq_lens, "seq_lens"), B, Hq,
+                                          int(max_seq_len), int(window), float(softmax_scale),
+                                          int(split_tokens), _dev_ptr(partial_lse, "partial_lse"),
+                                          _dev_ptr(partial_o, "partial_o"), ns, _dev_ptr(out, "out"),
+                                          out_dtype, _stream(stream)), "paged_decode_split_partial")
+
+
+def paged_decode_lse_combine(partial_lse, partial_o, seq_lens, window: int, split_tokens: int, out,
+                             block_size: int = 16, stream=None):
+    """Split-KV step 2: merge the partials of multi-split sequences into out."""
+    import torch
+    lib = load_library()
+    B, Hq, ns = (int(x) for x in partial_lse.shape)
+    D = int(partial_o.shape[3])
+    out_dtype = OUT_F32 if out.dtype == torch.float32 else OUT_BF16
+    _check(lib.paged_decode_lse_combine(_dev_ptr(partial_lse, "partial_lse"), _dev_ptr(partial_o, "partial_o"),
+                                        _dev_ptr(seq_lens, "seq_lens"), B, Hq, D, block_size, int(window),
+                                        int(split_tokens), ns, _dev_ptr(out, "out"), out_dtype,
+                                        _stream(stream)), "paged_decode_lse_combine")
+
+
+def device_status(clear: bool = True) -> int:
+    """Device error word (PKV_DEV_* bits); synchronises the device."""
+    rc = load_library().pkv_device_status(1 if clear else 0)
+    if rc < 0:
+        _check(rc, "pkv_device_status")
+    return rc
