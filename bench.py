@@ -1,0 +1,507 @@
+#!/usr/bin/env python3
+"""Benchmark one decode step of a paged-KV attention layer on GB300.
+
+A step is the whole hot path over one batch: append the batch's new K/V
+token (one per sequence) into the paged pool, then decode attention for
+every sequence (split-KV partial kernel + log-sum-exp combine when the split
+length is > 0, a single pass otherwise).  Default workload: the Gemma4-12B
+sliding-window layer (batch 64, lengths uniform in [512, 8192], H_q=16,
+H_kv=8, head_dim=256, window 1024, bf16 KV, 16-token blocks, pool 1.25x the
+needed blocks, shuffled).  Inputs are seeded synthetic data resident in HBM.
+
+value = algorithmic bytes of the step (KV rows in each window read once, Q,
+output, appended rows) / device time per step, in GB/s.
+Prints one JSON line (rank 0).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+"""
+from __future__ import annotations
+
+import argparse
+import datetime as _dt
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from paged_kv_decode_03_gb300 import bytes_model, synth  # noqa: E402
+
+METRIC = "decode-attn achieved HBM GB/s (% of ~8 TB/s) and seq·layer decode steps/sec"
+NOMINAL_HBM_GBS = 8000.0
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=3000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--config", default="c2", choices=sorted(synth.CONFIGS))
+    ap.add_argument("--cpu-seconds", type=float, default=8.0,
+                    help="CPU time budget of the oracle baseline sample")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args()
+
+
+# ------------------------------------------------------------------ helpers
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def csrc_sha() -> str:
+    h = hashlib.sha256()
+    base = os.path.join(ROOT, "paged_kv_decode_03_gb300", "csrc")
+    for name in sorted(os.listdir(base)):
+        with open(os.path.join(base, name), "rb") as f:
+            h.update(name.encode())
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(config: str):
+    """DRAM bytes per launch of the decode kernel from the committed ncu
+    summary, if it was taken on the current kernel sources."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        e = d.get(config)
+        if e and e.get("csrc_sha") == csrc_sha():
+            return e.get("bytes_per_launch")
+    except Exception:
+        pass
+    return None
+
+
+def workload_desc(spec) -> str:
+    lens = spec.lens
+    if lens[0] == "uniform":
+        ls = f"lens U[{lens[1]},{lens[2]}]"
+    elif lens[0] == "const":
+        ls = f"lens {lens[1]}"
+    elif lens[0] == "lognormal":
+        ls = f"lens lognormal(median {lens[1]}, sigma {lens[2]}) clipped [{lens[3]},{lens[4]}]"
+    else:
+        ls = f"lens {list(lens[1])}"
+    kv = {"bf16": "bf16 KV", "int8_token": "int8 KV per-token scales",
+          "int8_head": "int8 KV per-head scales"}[spec.kv]
+    return (f"{spec.name}: B={spec.batch}, H_q={spec.num_q_heads}, H_kv={spec.num_kv_heads}, "
+            f"D={spec.head_dim}, window={spec.window or 'none (global)'}, {kv}"
+            f"{', K=V one tensor' if spec.alias else ''}, block {spec.block_size}, {ls}")
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples during a region."""
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100", "-i", str(index)], stdout=subprocess.PIPE,
+                stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self, t0: float, t1: float):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out = ""
+        rows = []
+        for line in out.splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                ts = _dt.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                rows.append((ts, float(parts[1]), float(parts[2]), parts[5:9]))
+            except ValueError:
+                continue
+        inside = [r for r in rows if t0 - 0.05 <= r[0] <= t1 + 0.05]
+        window = "timed"
+        if not inside:
+            inside, window = rows, "whole run (timed region shorter than the sample period)"
+        if not inside:
+            return None
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in inside for i, v in enumerate(r[3]) if v == "Active"})
+        return {"sm_mhz": statistics.median(r[1] for r in inside),
+                "sm_max_mhz": max(r[2] for r in inside), "reasons": reasons,
+                "samples": len(inside), "window": window}
+
+
+# ------------------------------------------------------------- our arm
+def run_ours(args, rank, world, local_rank):
+    import torch
+    import paged_kv_decode_03_gb300 as pkv
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    pkv.load_library()
+    spec = synth.CONFIGS[args.config]
+    w = synth.make_workload(spec)
+    B, Hq, D = w.q.shape
+    P = spec.block_size
+
+    def dbits(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(dev)
+
+    def dnum(a):
+        return torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+
+    shape = (w.layout.num_blocks, P, spec.num_kv_heads, D)
+    if spec.kv == "bf16":
+        k_pool = torch.full(shape, int(np.int16(synth.BF16_NAN.view(np.int16))), dtype=torch.int16,
+                            device=dev).view(torch.bfloat16)
+    else:
+        k_pool = torch.full(shape, int(synth.INT8_POISON), dtype=torch.int8, device=dev)
+    v_pool = None if spec.alias else k_pool.clone()
+    ks = vs = None
+    mode = pkv.SCALE_NONE
+    if spec.kv == "int8_token":
+        mode = pkv.SCALE_PER_TOKEN
+        ks = torch.full((w.layout.num_blocks * P,), float("nan"), device=dev)
+        vs = None if spec.alias else ks.clone()
+    elif spec.kv == "int8_head":
+        mode = pkv.SCALE_PER_HEAD
+        ks = dnum(w.k_head_scale)
+        vs = None if spec.alias else dnum(w.v_head_scale)
+    pool = pkv.PagedKVPool(k=k_pool, v=v_pool, k_scale=ks, v_scale=vs, scale_mode=mode)
+    T = len(w.hist_slots)
+    for s in range(0, T, 1 << 16):
+        e = min(T, s + (1 << 16))
+        pkv.paged_kv_append(dbits(w.hist_k[s:e]), None if w.hist_v is None else dbits(w.hist_v[s:e]),
+                            dnum(w.hist_slots[s:e]), pool)
+    q = dbits(w.q)
+    bt = dnum(w.block_table)
+    sl = dnum(w.seq_lens)
+    k_new = dbits(w.new_k)
+    v_new = None if w.new_v is None else dbits(w.new_v)
+    slots = dnum(w.new_slots)
+    out = torch.empty((B, Hq, D), dtype=torch.bfloat16, device=dev)
+    max_len = int(w.seq_lens.max())
+    scale = float(np.float32(spec.softmax_scale))
+    st = pkv.paged_decode_split_tokens(B, Hq, spec.num_kv_heads, max_len, spec.window,
+                                       spec.split_tokens or pkv.SPLIT_AUTO)
+    ns = pkv.paged_decode_num_splits(max_len, spec.window, st) if st > 0 else 1
+    ws_bytes = pkv.paged_decode_workspace_bytes(B, Hq, spec.num_kv_heads, D, max_len,
+                                                spec.window, st)
+    ws = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device=dev)
+    lse = torch.empty((B, Hq, ns), dtype=torch.float32, device=dev)
+    po = torch.empty((B, Hq, ns, D), dtype=torch.float32, device=dev)
+    torch.cuda.synchronize()
+    pkv.device_status(clear=True)
+
+    def step(ev=None):
+        if ev is not None:
+            ev[0].record()
+        pkv.paged_kv_append(k_new, v_new, slots, pool)
+        if ev is not None:
+            ev[1].record()
+        if st > 0:
+            pkv.paged_decode_split_partial(q, pool, bt, sl, spec.window, scale, st, lse, po, out,
+                                           max_len)
+            if ev is not None:
+                ev[2].record()
+            pkv.paged_decode_lse_combine(lse, po, sl, spec.window, st, out)
+        else:
+            pkv.paged_decode_attention(q, pool, bt, sl, spec.window, scale, out, max_len,
+                                       split_tokens=0)
+            if ev is not None:
+                ev[2].record()
+        if ev is not None:
+            ev[3].record()
+
+    launches_per_step = 1 + (2 if st > 0 else 1)
+    dbytes = bytes_model.decode_bytes(spec, w.seq_lens, w.block_table)
+    abytes = bytes_model.append_bytes(spec, int((w.new_slots >= 0).sum()))
+    step_bytes = dbytes["kv"] + dbytes["q"] + dbytes["out"] + abytes
+    decode_kernel_bytes = dbytes["kv"] + dbytes["q"] + (dbytes["out"] if st == 0 else 0)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    sampler = ClockSampler(local_rank) if rank == 0 else None
+    time.sleep(0.25 if sampler else 0)
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    t0 = time.time()
+    start.record()
+    for i in range(args.steps):
+        step(evs[i])
+    end.record()
+    torch.cuda.synchronize()
+    t1 = time.time()
+    if world > 1:
+        torch.distributed.barrier()
+    clocks = sampler.stop(t0, t1) if sampler else None
+    elapsed_ms = start.elapsed_time(end)
+    if world > 1:
+        tm = torch.tensor([elapsed_ms], device=dev)
+        torch.distributed.all_reduce(tm, op=torch.distributed.ReduceOp.MAX)
+        elapsed_ms = float(tm.item())
+    status = pkv.device_status(clear=True)
+    app_us = statistics.mean(e[0].elapsed_time(e[1]) for e in evs) * 1e3
+    dec_us = statistics.mean(e[1].elapsed_time(e[2]) for e in evs) * 1e3
+    cmb_us = statistics.mean(e[2].elapsed_time(e[3]) for e in evs) * 1e3
+    ms_per_step = elapsed_ms / args.steps
+    value = world * step_bytes / (ms_per_step * 1e-3) / 1e9
+
+    # ---- end to end through the C ABI with host buffers
+    e2e = None
+    if not args.no_e2e:
+        pin = {}
+
+        def pinned_bits(a):
+            t = torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16)
+            return t.pin_memory()
+
+        pin["q"] = pinned_bits(w.q)
+        pin["k"] = pinned_bits(w.new_k)
+        pin["v"] = None if w.new_v is None else pinned_bits(w.new_v)
+        pin["slots"] = torch.from_numpy(w.new_slots).pin_memory()
+        pin["bt"] = torch.from_numpy(w.block_table).pin_memory()
+        pin["sl"] = torch.from_numpy(w.seq_lens).pin_memory()
+        out_h = torch.empty((B, Hq, D), dtype=torch.bfloat16).pin_memory()
+        h2d = sum(t.numel() * t.element_size() for t in pin.values() if t is not None)
+        d2h = out_h.numel() * out_h.element_size()
+
+        def e2e_step():
+            q.copy_(pin["q"], non_blocking=True)
+            k_new.copy_(pin["k"], non_blocking=True)
+            if v_new is not None:
+                v_new.copy_(pin["v"], non_blocking=True)
+            slots.copy_(pin["slots"], non_blocking=True)
+            bt.copy_(pin["bt"], non_blocking=True)
+            sl.copy_(pin["sl"], non_blocking=True)
+            pkv.paged_kv_append(k_new, v_new, slots, pool)
+            pkv.paged_decode_attention(q, pool, bt, sl, spec.window, scale, out, max_len,
+                                       split_tokens=st, workspace=ws)
+            out_h.copy_(out, non_blocking=True)
+
+        for _ in range(max(3, args.warmup)):
+            e2e_step()
+        torch.cuda.synchronize()
+        if world > 1:
+            torch.distributed.barrier()
+        s2 = torch.cuda.Event(enable_timing=True)
+        e2 = torch.cuda.Event(enable_timing=True)
+        s2.record()
+        for _ in range(args.steps):
+            e2e_step()
+        e2.record()
+        torch.cuda.synchronize()
+        e2e_ms = s2.elapsed_time(e2)
+        if world > 1:
+            tm = torch.tensor([e2e_ms], device=dev)
+            torch.distributed.all_reduce(tm, op=torch.distributed.ReduceOp.MAX)
+            e2e_ms = float(tm.item())
+        e2e = {"value": world * step_bytes / (e2e_ms / args.steps * 1e-3) / 1e9, "unit": "GB/s",
+               "ms_per_step": e2e_ms / args.steps, "h2d_bytes_per_step": int(h2d),
+               "d2h_bytes_per_step": int(d2h),
+               "api": "paged_kv_append + paged_decode_attention (C ABI), pinned host buffers"}
+
+    if rank != 0:
+        return None
+    peak, peak_kind = peaks()
+    achieved = decode_kernel_bytes / (dec_us * 1e-6) / 1e9
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(spec, w, step_bytes, args.cpu_seconds)
+    line = {
+        "metric": METRIC,
+        "value": round(value, 2),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_per_step, 6),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16" if spec.kv == "bf16" else "int8 KV / bf16 q",
+        "data": "synthetic (seeded N(0,1) bf16 K/V/q; shuffled physical blocks)",
+        "config": {
+            "workload": workload_desc(spec),
+            "batch": B, "num_q_heads": Hq, "num_kv_heads": spec.num_kv_heads, "head_dim": D,
+            "window": spec.window, "block_size": P, "num_blocks": w.layout.num_blocks,
+            "split_tokens": st, "num_splits": ns,
+            "step": "append 1 token/seq + decode (split partial + combine)" if st > 0
+                    else "append 1 token/seq + single-pass decode",
+            "l2": f"inputs larger than L2 ({dbytes['kv'] / 1e6:.0f} MB of KV read per step vs 129 MB L2); no flush",
+            "parallelism": f"replicas: one independent batch per GPU x{world}",
+        },
+        "pct_of_nominal_8tbs": round(100 * value / world / NOMINAL_HBM_GBS, 2),
+        "pct_of_measured_peak": round(100 * value / world / peak, 2),
+        "seq_layer_steps_per_s": round(world * B / (ms_per_step * 1e-3), 1),
+        "bytes_per_step": {"kv": dbytes["kv"], "q": dbytes["q"], "out": dbytes["out"],
+                           "append": abytes, "total": step_bytes},
+        "kernels_us": {"append": round(app_us, 3), "decode": round(dec_us, 3),
+                       "combine": round(cmb_us, 3)},
+        "roofline": {"bound": "hbm", "kernel": "decode_kernel (split partial)" if st > 0 else "decode_kernel",
+                     "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "peak_source": peak_kind,
+                     "algorithmic_bytes_per_launch": decode_kernel_bytes,
+                     "traffic": recorded_traffic(args.config)},
+        "gpu_launches": launches_per_step * args.steps,
+        "device_error_word": status,
+        "clocks": clocks,
+    }
+    if e2e is not None:
+        line["e2e"] = {k: (round(v, 4) if isinstance(v, float) else v) for k, v in e2e.items()}
+    if cpu is not None:
+        line["cpu_baseline"] = cpu
+    return line
+
+
+# --------------------------------------------------------- CPU baseline
+def cores_used():
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count()
+
+
+def oracle_setup(spec, w):
+    import oracle
+    k, v, ks, vs = synth.empty_pool_arrays(spec, w.layout)
+    mode = {"bf16": oracle.SCALE_NONE, "int8_token": oracle.SCALE_PER_TOKEN,
+            "int8_head": oracle.SCALE_PER_HEAD}[spec.kv]
+    if spec.kv == "int8_head":
+        ks = w.k_head_scale.copy()
+        vs = None if spec.alias else w.v_head_scale.copy()
+    pool = oracle.OraclePool(k=k, v=v, k_scale=ks, v_scale=vs, scale_mode=mode)
+    if len(w.hist_slots):
+        oracle.append(w.hist_k, w.hist_v, w.hist_slots, pool)
+    return pool
+
+
+def cpu_baseline(spec, w, step_bytes, budget_s):
+    """The oracle as it stands, on the host cores, over repetitions of the
+    full step (append the new tokens + decode every row) for about
+    ``budget_s`` seconds."""
+    import oracle
+    pool = oracle_setup(spec, w)
+    threads = oracle.max_threads()
+    reps, t = 0, 0.0
+    while reps == 0 or t < budget_s:
+        t0 = time.perf_counter()
+        oracle.append(w.new_k, w.new_v, w.new_slots, pool)
+        oracle.decode(w.q, pool, w.block_table, w.seq_lens, spec.num_q_heads, spec.window,
+                      np.float32(spec.softmax_scale))
+        t += time.perf_counter() - t0
+        reps += 1
+    return {"value": round(step_bytes * reps / t / 1e9, 4), "unit": "GB/s", "cores": threads,
+            "kind": "oracle", "seconds": round(t, 2),
+            "sample": f"{reps} full step(s) of {spec.name} (append {spec.batch} tokens + "
+                      f"decode {spec.batch}x{spec.num_q_heads} rows), fp64 C oracle, "
+                      f"{threads} OpenMP threads"}
+
+
+def run_reference(args, rank):
+    """The oracle timed as the reference arm: each step a bounded sample of
+    the workload (whole sequences, all heads), sized so that warmup + steps
+    take about two minutes."""
+    if rank != 0:
+        return None
+    import oracle
+    spec = synth.CONFIGS[args.config]
+    w = synth.make_workload(spec)
+    pool = oracle_setup(spec, w)
+    threads = oracle.max_threads()
+    B, Hq, _ = w.q.shape
+    order = np.argsort(-w.seq_lens)  # deterministic sample: longest first
+
+    def sample_step(nseq):
+        idx = np.sort(order[:nseq])
+        rows = np.array([(b, h) for b in idx for h in range(Hq)], np.int32)
+        oracle.append(w.new_k[idx], None if w.new_v is None else w.new_v[idx], w.new_slots[idx], pool)
+        oracle.decode(w.q, pool, w.block_table, w.seq_lens, Hq, spec.window,
+                      np.float32(spec.softmax_scale), rows=rows)
+        return idx
+
+    t0 = time.perf_counter()
+    sample_step(1)
+    t_one = max(time.perf_counter() - t0, 1e-4)
+    budget = 120.0 / max(1, args.steps + args.warmup)
+    nseq = int(max(1, min(B, budget // t_one)))
+    for _ in range(max(3, args.warmup)):
+        sample_step(nseq)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        idx = sample_step(nseq)
+    dt = (time.perf_counter() - t0) / args.steps
+    dbytes = bytes_model.decode_bytes(spec, w.seq_lens[idx], w.block_table[idx])
+    abytes = bytes_model.append_bytes(spec, len(idx))
+    sbytes = dbytes["kv"] + dbytes["q"] + dbytes["out"] + abytes
+    value = sbytes / dt / 1e9
+    sample = (f"{len(idx)} of {B} sequences of {spec.name} per step (longest first), all "
+              f"{Hq} heads: append + decode, fp64 C oracle")
+    return {
+        "metric": METRIC, "impl": "reference", "value": round(value, 4), "unit": "GB/s",
+        "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(dt * 1e3, 3), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)",
+        "config": {"workload": workload_desc(spec), "batch": B,
+                   "parallelism": "host cores (OpenMP)"},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": threads,
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    args = parse_args()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        line = run_reference(args, rank)
+        if line is not None:
+            print(json.dumps(line), flush=True)
+        return 0
+    if world > 1:
+        import torch
+        torch.cuda.set_device(local_rank)
+        torch.distributed.init_process_group("nccl")
+    line = run_ours(args, rank, world, local_rank)
+    if line is not None:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,497 @@
+// pkv_abi.cu -- the extern "C" entry points declared in include/pagedkv.h:
+// argument validation on the host, TMA tensor-map encoding, split-length
+// resolution and kernel launches.  No device memory is allocated here.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <cstdarg>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+#include <string>
+
+#include "pkv_device.cuh"
+#include "pkv_internal.h"
+
+namespace pkv {
+
+// Device error word (PKV_DEV_* bits), one per device that loads the
+// library.  Kernels receive its address as a parameter.
+static __device__ unsigned int g_error_word = 0;
+
+// Address of g_error_word on the current device (looked up once per device).
+static unsigned int *error_word_ptr()
+{
+    static std::mutex mu;
+    static unsigned int *ptrs[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
+        return nullptr;
+    std::lock_guard<std::mutex> lock(mu);
+    if (!ptrs[dev]) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_error_word) != cudaSuccess)
+            return nullptr;
+        ptrs[dev] = static_cast<unsigned int *>(p);
+    }
+    return ptrs[dev];
+}
+
+static thread_local std::string t_last_error;
+
+static int fail(int code, const char *fmt, ...)
+{
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof buf, fmt, ap);
+    va_end(ap);
+    t_last_error = buf;
+    return code;
+}
+
+static int cuda_fail(cudaError_t e, const char *what)
+{
+    t_last_error = std::string(what) + ": " + cudaGetErrorString(e);
+    return static_cast<int>(e);
+}
+
+static bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// ---------------------------------------------------------- tensor maps
+static PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
+{
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        cudaDriverEntryPointQueryResult q;
+        void *f = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+    });
+    return fn;
+}
+
+// Tensor map over a pool [num_blocks*block_size][H_kv][D] (innermost first:
+// D, H_kv, rows); box = {chunk elements, 1 head, block_size rows}.
+static int encode_pool_map(CUtensorMap *map, void *base, const pkv_pool &pool)
+{
+    auto fn = encode_fn();
+    if (!fn)
+        return fail(PKV_E_DRIVER, "cuTensorMapEncodeTiled is unavailable");
+    const int es = pool.dtype == PKV_INT8 ? 1 : 2;
+    const int che = pool.head_dim * es > 256 ? 256 / es : pool.head_dim;
+    cuuint64_t dims[3] = {(cuuint64_t)pool.head_dim, (cuuint64_t)pool.num_kv_heads,
+                          (cuuint64_t)pool.num_blocks * (cuuint64_t)pool.block_size};
+    cuuint64_t strides[2] = {(cuuint64_t)pool.head_dim * es,
+                             (cuuint64_t)pool.num_kv_heads * pool.head_dim * es};
+    cuuint32_t box[3] = {(cuuint32_t)che, 1u, (cuuint32_t)pool.block_size};
+    cuuint32_t estr[3] = {1u, 1u, 1u};
+    CUresult r = fn(map, es == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8,
+                    3, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                    CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS)
+        return fail(PKV_E_DRIVER, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+    return PKV_OK;
+}
+
+// ---------------------------------------------------------- validation
+static int check_pool(const pkv_pool *pool)
+{
+    if (!pool)
+        return fail(PKV_E_NULL, "pool is NULL");
+    if (!pool->k)
+        return fail(PKV_E_NULL, "pool->k is NULL");
+    if (pool->block_size != kBlock)
+        return fail(PKV_E_UNSUPPORTED, "block_size %d not supported (16 only)", pool->block_size);
+    if (pool->head_dim != 64 && pool->head_dim != 128 && pool->head_dim != 256)
+        return fail(PKV_E_UNSUPPORTED, "head_dim %d not supported (64, 128, 256)", pool->head_dim);
+    if (pool->num_kv_heads <= 0 || pool->num_blocks <= 0)
+        return fail(PKV_E_SHAPE, "num_kv_heads and num_blocks must be positive");
+    if ((int64_t)pool->num_blocks * pool->block_size > INT32_MAX)
+        return fail(PKV_E_SHAPE, "pool has more than 2^31 slots");
+    if (pool->dtype != PKV_BF16 && pool->dtype != PKV_INT8)
+        return fail(PKV_E_UNSUPPORTED, "dtype %d", pool->dtype);
+    if (!aligned(pool->k, 16) || (pool->v && !aligned(pool->v, 16)))
+        return fail(PKV_E_ALIGN, "pool k/v must be 16-byte aligned");
+    const bool alias = pool->v == nullptr || pool->v == pool->k;
+    if (pool->dtype == PKV_BF16) {
+        if (pool->scale_mode != PKV_SCALE_NONE)
+            return fail(PKV_E_ARG, "bf16 pools take no scales");
+    } else {
+        if (pool->scale_mode != PKV_SCALE_PER_TOKEN && pool->scale_mode != PKV_SCALE_PER_HEAD)
+            return fail(PKV_E_ARG, "int8 pools need per-token or per-head scales");
+        if (!pool->k_scale || (!alias && !pool->v_scale))
+            return fail(PKV_E_NULL, "int8 pool scale table is NULL");
+        if (pool->scale_mode == PKV_SCALE_PER_TOKEN &&
+            (!aligned(pool->k_scale, 16) || (!alias && !aligned(pool->v_scale, 16))))
+            return fail(PKV_E_ALIGN, "per-token scale tables must be 16-byte aligned");
+        if (!aligned(pool->k_scale, 4) || (!alias && !aligned(pool->v_scale, 4)))
+            return fail(PKV_E_ALIGN, "scale tables must be 4-byte aligned");
+    }
+    return PKV_OK;
+}
+
+static int sm_count()
+{
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess)
+        return -1;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return -1;
+    return n;
+}
+
+static int stages_per_warp()
+{
+    static int v = [] {
+        const char *e = getenv("PKV_STAGES_PER_WARP");
+        int s = e ? atoi(e) : 2;
+        return s < 1 ? 1 : (s > 4 ? 4 : s);
+    }();
+    return v;
+}
+
+// Most paged blocks the key range of a length-<=L sequence can touch.
+static int64_t max_range_blocks(int P, int64_t L, int window)
+{
+    if (L <= 0)
+        return 0;
+    const int64_t keys = window > 0 ? (L < window + 1 ? L : (int64_t)window + 1) : L;
+    const int64_t whole = (L + P - 1) / P;
+    const int64_t span = (keys + P - 2) / P + 1;
+    return whole < span ? whole : span;
+}
+
+}  // namespace pkv
+
+using namespace pkv;
+
+extern "C" {
+
+PKV_API const char *pkv_last_error(void) { return t_last_error.c_str(); }
+
+PKV_API int pkv_device_status(int32_t clear)
+{
+    unsigned int w = 0;
+    cudaError_t e = cudaMemcpyFromSymbol(&w, g_error_word, sizeof w);
+    if (e != cudaSuccess)
+        return fail(PKV_E_DRIVER, "reading the device error word: %s", cudaGetErrorString(e));
+    if (clear) {
+        unsigned int z = 0;
+        e = cudaMemcpyToSymbol(g_error_word, &z, sizeof z);
+        if (e != cudaSuccess)
+            return fail(PKV_E_DRIVER, "clearing the device error word: %s", cudaGetErrorString(e));
+    }
+    return static_cast<int>(w);
+}
+
+PKV_API int paged_kv_append(const void *k, const void *v, const int64_t *slot_mapping,
+                            int32_t num_tokens, const pkv_pool *pool, void *stream)
+{
+    t_last_error.clear();
+    if (int rc = check_pool(pool))
+        return rc;
+    if (num_tokens < 0)
+        return fail(PKV_E_ARG, "num_tokens < 0");
+    if (num_tokens == 0)
+        return PKV_OK;
+    const bool alias = pool->v == nullptr || pool->v == pool->k;
+    if (!k || !slot_mapping || (!alias && !v))
+        return fail(PKV_E_NULL, "k, v or slot_mapping is NULL");
+    if (!aligned(k, 16) || (!alias && !aligned(v, 16)) || !aligned(slot_mapping, 8))
+        return fail(PKV_E_ALIGN, "k/v must be 16-byte and slot_mapping 8-byte aligned");
+    AppendParams p{};
+    p.k = static_cast<const uint16_t *>(k);
+    p.v = static_cast<const uint16_t *>(alias ? k : v);
+    p.slot_mapping = slot_mapping;
+    p.pool_k = pool->k;
+    p.pool_v = alias ? pool->k : pool->v;
+    p.k_scale = pool->k_scale;
+    p.v_scale = alias ? pool->k_scale : pool->v_scale;
+    p.num_tokens = num_tokens;
+    p.row = pool->num_kv_heads * pool->head_dim;
+    p.head_dim = pool->head_dim;
+    p.num_slots = (int64_t)pool->num_blocks * pool->block_size;
+    p.scale_mode = pool->scale_mode;
+    p.alias = alias;
+    p.err = error_word_ptr();
+    if (!p.err)
+        return fail(PKV_E_DRIVER, "cannot resolve the device error word");
+    cudaError_t e = launch_append(p, pool->dtype == PKV_INT8, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess)
+        return cuda_fail(e, "append launch");
+    return PKV_OK;
+}
+
+PKV_API int32_t paged_decode_num_splits(int32_t block_size, int32_t max_seq_len, int32_t window,
+                                        int32_t split_tokens)
+{
+    if (block_size <= 0 || split_tokens <= 0 || split_tokens % block_size)
+        return 1;
+    const int64_t nblk = max_range_blocks(block_size, max_seq_len, window);
+    const int64_t sb = split_tokens / block_size;
+    const int64_t ns = (nblk + sb - 1) / sb;
+    return ns < 1 ? 1 : static_cast<int32_t>(ns);
+}
+
+PKV_API int32_t paged_decode_split_tokens(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads,
+                                          int32_t block_size, int32_t max_seq_len, int32_t window,
+                                          int32_t split_tokens)
+{
+    if (block_size <= 0 || num_kv_heads <= 0 || num_q_heads <= 0 || batch < 0)
+        return fail(PKV_E_ARG, "bad sizes");
+    if (split_tokens >= 0) {
+        if (split_tokens % block_size)
+            return fail(PKV_E_ARG, "split_tokens %d is not a multiple of block_size", split_tokens);
+        return split_tokens;
+    }
+    if (split_tokens != PKV_SPLIT_AUTO)
+        return fail(PKV_E_ARG, "split_tokens %d", split_tokens);
+    // Auto: enough CTAs for about four per SM, splits of at least 8 blocks.
+    const int sms = sm_count();
+    if (sms <= 0)
+        return fail(PKV_E_DRIVER, "cannot query the SM count");
+    const int group = num_q_heads / num_kv_heads;
+    const int gt = decode_group_tile(group);
+    const int64_t units = (int64_t)batch * num_kv_heads * ((group + gt - 1) / gt);
+    const int64_t nblk = max_range_blocks(block_size, max_seq_len, window);
+    if (units <= 0 || nblk <= 8)
+        return 0;
+    int64_t want = (4LL * sms + units - 1) / units;
+    const int64_t cap = nblk / 8;
+    if (want > cap)
+        want = cap;
+    if (want <= 1)
+        return 0;
+    const int64_t sb = (nblk + want - 1) / want;
+    return static_cast<int32_t>(sb * block_size);
+}
+
+PKV_API size_t paged_decode_workspace_bytes(int32_t batch, int32_t num_q_heads,
+                                            int32_t num_kv_heads, int32_t head_dim,
+                                            int32_t block_size, int32_t max_seq_len,
+                                            int32_t window, int32_t split_tokens)
+{
+    const int32_t st = paged_decode_split_tokens(batch, num_q_heads, num_kv_heads, block_size,
+                                                 max_seq_len, window, split_tokens);
+    if (st <= 0)
+        return 0;
+    const size_t ns = paged_decode_num_splits(block_size, max_seq_len, window, st);
+    const size_t rows = (size_t)batch * num_q_heads * ns;
+    const size_t lse = (rows * sizeof(float) + 255) / 256 * 256;
+    return lse + rows * head_dim * sizeof(float);
+}
+
+static int check_decode_args(const void *q, const pkv_pool *pool, const int32_t *block_table,
+                             int32_t max_blocks_per_seq, const int32_t *seq_lens, int32_t batch,
+                             int32_t num_q_heads, int32_t max_seq_len, int32_t window, void *out,
+                             int32_t out_dtype)
+{
+    if (int rc = check_pool(pool))
+        return rc;
+    if (batch < 0 || num_q_heads <= 0 || max_blocks_per_seq <= 0 || max_seq_len < 0)
+        return fail(PKV_E_SHAPE, "batch, num_q_heads, max_blocks_per_seq or max_seq_len invalid");
+    if (num_q_heads % pool->num_kv_heads)
+        return fail(PKV_E_SHAPE, "num_q_heads %d is not a multiple of num_kv_heads %d",
+                    num_q_heads, pool->num_kv_heads);
+    if (batch > 65535)
+        return fail(PKV_E_UNSUPPORTED, "batch > 65535");
+    if (window < 0)
+        return fail(PKV_E_ARG, "window < 0");
+    if ((int64_t)max_seq_len > (int64_t)max_blocks_per_seq * pool->block_size)
+        return fail(PKV_E_SHAPE, "max_seq_len exceeds max_blocks_per_seq * block_size");
+    if (out_dtype != PKV_OUT_BF16 && out_dtype != PKV_OUT_F32)
+        return fail(PKV_E_ARG, "out_dtype %d", out_dtype);
+    if (!q || !block_table || !seq_lens || !out)
+        return fail(PKV_E_NULL, "q, block_table, seq_lens or out is NULL");
+    if (!aligned(q, 16) || !aligned(out, 16) || !aligned(block_table, 4) || !aligned(seq_lens, 4))
+        return fail(PKV_E_ALIGN, "q/out must be 16-byte aligned");
+    return PKV_OK;
+}
+
+static int run_decode(const void *q, const pkv_pool *pool, const int32_t *block_table,
+                      int32_t max_blocks_per_seq, const int32_t *seq_lens, int32_t batch,
+                      int32_t num_q_heads, int32_t max_seq_len, int32_t window,
+                      float softmax_scale, int32_t split_tokens, float *part_lse, float *part_o,
+                      int32_t num_splits, void *out, int32_t out_dtype, cudaStream_t s)
+{
+    const bool alias = pool->v == nullptr || pool->v == pool->k;
+    CUtensorMap tmk, tmv;
+    if (int rc = encode_pool_map(&tmk, pool->k, *pool))
+        return rc;
+    if (alias)
+        tmv = tmk;
+    else if (int rc = encode_pool_map(&tmv, pool->v, *pool))
+        return rc;
+    const int group = num_q_heads / pool->num_kv_heads;
+    const int gt = decode_group_tile(group);
+    DecodeParams p{};
+    p.q = static_cast<const uint16_t *>(q);
+    p.block_table = block_table;
+    p.seq_lens = seq_lens;
+    p.k_scale = pool->k_scale;
+    p.v_scale = alias ? pool->k_scale : pool->v_scale;
+    p.part_lse = part_lse;
+    p.part_o = part_o;
+    p.out = out;
+    p.max_blocks = max_blocks_per_seq;
+    p.scale_mode = pool->scale_mode;
+    p.batch = batch;
+    p.num_q_heads = num_q_heads;
+    p.num_kv_heads = pool->num_kv_heads;
+    p.group = group;
+    p.head_chunks = (group + gt - 1) / gt;
+    p.num_blocks = pool->num_blocks;
+    p.window = window;
+    p.max_seq_len = max_seq_len;
+    p.split_blocks = split_tokens > 0 ? split_tokens / pool->block_size : 0;
+    p.num_splits = split_tokens > 0 ? num_splits : 1;
+    p.alias = alias;
+    p.out_f32 = out_dtype == PKV_OUT_F32;
+    p.num_stages = 4 * stages_per_warp();
+    p.qk_scale_log2 = softmax_scale * LOG2E;
+    p.err = error_word_ptr();
+    if (!p.err)
+        return fail(PKV_E_DRIVER, "cannot resolve the device error word");
+    if ((int64_t)p.num_kv_heads * p.head_chunks > 65535)
+        return fail(PKV_E_UNSUPPORTED, "too many kv heads");
+    cudaError_t e = launch_decode(p, tmk, tmv, pool->head_dim, pool->dtype == PKV_INT8, gt, s);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "decode launch");
+    return PKV_OK;
+}
+
+PKV_API int paged_decode_split_partial(const void *q, const pkv_pool *pool,
+                                       const int32_t *block_table, int32_t max_blocks_per_seq,
+                                       const int32_t *seq_lens, int32_t batch, int32_t num_q_heads,
+                                       int32_t max_seq_len, int32_t window, float softmax_scale,
+                                       int32_t split_tokens, float *partial_lse, float *partial_o,
+                                       int32_t num_splits, void *out, int32_t out_dtype,
+                                       void *stream)
+{
+    t_last_error.clear();
+    if (int rc = check_decode_args(q, pool, block_table, max_blocks_per_seq, seq_lens, batch,
+                                   num_q_heads, max_seq_len, window, out, out_dtype))
+        return rc;
+    if (split_tokens <= 0 || split_tokens % pool->block_size)
+        return fail(PKV_E_ARG, "split_tokens must be a positive multiple of block_size");
+    const int32_t need = paged_decode_num_splits(pool->block_size, max_seq_len, window, split_tokens);
+    if (num_splits < need)
+        return fail(PKV_E_WORKSPACE, "num_splits %d < %d needed", num_splits, need);
+    if (num_splits > 1024)
+        return fail(PKV_E_UNSUPPORTED, "more than 1024 splits");
+    if (!partial_lse || !partial_o)
+        return fail(PKV_E_NULL, "partial buffers are NULL");
+    if (!aligned(partial_lse, 4) || !aligned(partial_o, 16))
+        return fail(PKV_E_ALIGN, "partial_o must be 16-byte aligned");
+    if (batch == 0)
+        return PKV_OK;
+    return run_decode(q, pool, block_table, max_blocks_per_seq, seq_lens, batch, num_q_heads,
+                      max_seq_len, window, softmax_scale, split_tokens, partial_lse, partial_o,
+                      num_splits, out, out_dtype, static_cast<cudaStream_t>(stream));
+}
+
+PKV_API int paged_decode_lse_combine(const float *partial_lse, const float *partial_o,
+                                     const int32_t *seq_lens, int32_t batch, int32_t num_q_heads,
+                                     int32_t head_dim, int32_t block_size, int32_t window,
+                                     int32_t split_tokens, int32_t num_splits, void *out,
+                                     int32_t out_dtype, void *stream)
+{
+    t_last_error.clear();
+    if (!partial_lse || !partial_o || !seq_lens || !out)
+        return fail(PKV_E_NULL, "NULL argument");
+    if (block_size != kBlock)
+        return fail(PKV_E_UNSUPPORTED, "block_size %d", block_size);
+    if (batch < 0 || num_q_heads <= 0 || head_dim <= 0 || num_splits <= 0 || num_splits > 1024 ||
+        batch > 65535)
+        return fail(PKV_E_SHAPE, "bad sizes");
+    if (split_tokens <= 0 || split_tokens % block_size)
+        return fail(PKV_E_ARG, "split_tokens must be a positive multiple of block_size");
+    if (window < 0 || (out_dtype != PKV_OUT_BF16 && out_dtype != PKV_OUT_F32))
+        return fail(PKV_E_ARG, "window or out_dtype");
+    if (batch == 0)
+        return PKV_OK;
+    CombineParams p{};
+    p.part_lse = partial_lse;
+    p.part_o = partial_o;
+    p.seq_lens = seq_lens;
+    p.out = out;
+    p.batch = batch;
+    p.num_q_heads = num_q_heads;
+    p.head_dim = head_dim;
+    p.window = window;
+    p.split_blocks = split_tokens / block_size;
+    p.num_splits = num_splits;
+    p.out_f32 = out_dtype == PKV_OUT_F32;
+    cudaError_t e = launch_combine(p, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess)
+        return cuda_fail(e, "combine launch");
+    return PKV_OK;
+}
+
+PKV_API int paged_decode_attention(const void *q, const pkv_pool *pool, const int32_t *block_table,
+                                   int32_t max_blocks_per_seq, const int32_t *seq_lens,
+                                   int32_t batch, int32_t num_q_heads, int32_t max_seq_len,
+                                   int32_t window, float softmax_scale, int32_t split_tokens,
+                                   void *workspace, size_t workspace_bytes, void *out,
+                                   int32_t out_dtype, void *stream)
+{
+    t_last_error.clear();
+    if (int rc = check_decode_args(q, pool, block_table, max_blocks_per_seq, seq_lens, batch,
+                                   num_q_heads, max_seq_len, window, out, out_dtype))
+        return rc;
+    const int32_t st = paged_decode_split_tokens(batch, num_q_heads, pool->num_kv_heads,
+                                                 pool->block_size, max_seq_len, window,
+                                                 split_tokens);
+    if (st < 0)
+        return st;
+    if (batch == 0)
+        return PKV_OK;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (st == 0)
+        return run_decode(q, pool, block_table, max_blocks_per_seq, seq_lens, batch, num_q_heads,
+                          max_seq_len, window, softmax_scale, 0, nullptr, nullptr, 1, out,
+                          out_dtype, s);
+    const int32_t ns = paged_decode_num_splits(pool->block_size, max_seq_len, window, st);
+    if (ns > 1024)
+        return fail(PKV_E_UNSUPPORTED, "more than 1024 splits; use a longer split_tokens");
+    const size_t need = paged_decode_workspace_bytes(batch, num_q_heads, pool->num_kv_heads,
+                                                     pool->head_dim, pool->block_size,
+                                                     max_seq_len, window, st);
+    if (!workspace || workspace_bytes < need)
+        return fail(PKV_E_WORKSPACE, "workspace of %zu bytes needed, %zu given", need,
+                    workspace_bytes);
+    if (!aligned(workspace, 256))
+        return fail(PKV_E_ALIGN, "workspace must be 256-byte aligned");
+    const size_t rows = (size_t)batch * num_q_heads * ns;
+    float *lse = static_cast<float *>(workspace);
+    float *po = reinterpret_cast<float *>(static_cast<char *>(workspace) +
+                                          (rows * sizeof(float) + 255) / 256 * 256);
+    if (int rc = run_decode(q, pool, block_table, max_blocks_per_seq, seq_lens, batch, num_q_heads,
+                            max_seq_len, window, softmax_scale, st, lse, po, ns, out, out_dtype, s))
+        return rc;
+    CombineParams c{};
+    c.part_lse = lse;
+    c.part_o = po;
+    c.seq_lens = seq_lens;
+    c.out = out;
+    c.batch = batch;
+    c.num_q_heads = num_q_heads;
+    c.head_dim = pool->head_dim;
+    c.window = window;
+    c.split_blocks = st / pool->block_size;
+    c.num_splits = ns;
+    c.out_f32 = out_dtype == PKV_OUT_F32;
+    cudaError_t e = launch_combine(c, s);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "combine launch");
+    return PKV_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,132 @@
+// pkv_append.cu -- write the step's new K/V rows into their pool slots,
+// copying bf16 or quantising to int8.
+//
+// Sources (page title, section): "CS336 · 第 10 课", KV-cache section (each
+// decode step appends the new token's K/V) and int8 section
+// (scale = max|x| / 127, x_q = round(x / scale)); "推理优化与 AI Infra",
+// section 2 (pool [block][slot][head][dim]), section 5 (per_token or
+// per_head scales) and section 8 (slot ids as a static step buffer).
+//
+// One CTA per token.  The token's row for all kv heads is contiguous in the
+// pool ([slot][H_kv][D] with slot = block * 16 + offset), so the write is a
+// straight vectorised copy.  Quantisation follows the fp32 formula exactly:
+// IEEE division for the scale and for every element (no reciprocal),
+// round-half-to-even, saturation to [-127, 127], zero scale -> zero codes.
+#include <cuda_bf16.h>
+
+#include "pkv_device.cuh"
+#include "pkv_internal.h"
+
+namespace pkv {
+
+constexpr int APPEND_THREADS = 128;
+
+__device__ __forceinline__ int8_t quantize_one(float x, float scale)
+{
+    if (scale == 0.f)
+        return 0;
+    int r = __float2int_rn(__fdiv_rn(x, scale));
+    r = max(-127, min(127, r));
+    return static_cast<int8_t>(r);
+}
+
+__device__ __forceinline__ void unpack8(const uint4 w, float *f)
+{
+    f[0] = bf16lo(w.x); f[1] = bf16hi(w.x); f[2] = bf16lo(w.y); f[3] = bf16hi(w.y);
+    f[4] = bf16lo(w.z); f[5] = bf16hi(w.z); f[6] = bf16lo(w.w); f[7] = bf16hi(w.w);
+}
+
+__device__ __forceinline__ uint2 pack8(const int8_t *q)
+{
+    uint2 r;
+    r.x = (uint32_t)(uint8_t)q[0] | ((uint32_t)(uint8_t)q[1] << 8) |
+          ((uint32_t)(uint8_t)q[2] << 16) | ((uint32_t)(uint8_t)q[3] << 24);
+    r.y = (uint32_t)(uint8_t)q[4] | ((uint32_t)(uint8_t)q[5] << 8) |
+          ((uint32_t)(uint8_t)q[6] << 16) | ((uint32_t)(uint8_t)q[7] << 24);
+    return r;
+}
+
+// Block-wide max of non-negative values; every thread gets the result.
+__device__ __forceinline__ float block_max(float v, float *red)
+{
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1)
+        v = fmaxf(v, __shfl_xor_sync(FULL_MASK, v, off));
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (lane == 0)
+        red[warp] = v;
+    __syncthreads();
+    float r = 0.f;
+    for (int w = 0; w < (int)(blockDim.x >> 5); ++w)
+        r = fmaxf(r, red[w]);
+    __syncthreads();
+    return r;
+}
+
+template <bool INT8>
+__global__ void __launch_bounds__(APPEND_THREADS) append_kernel(const AppendParams p)
+{
+    __shared__ float red[APPEND_THREADS / 32];
+    const int t = blockIdx.x;
+    const int64_t slot = p.slot_mapping[t];
+    if (slot < 0)
+        return;
+    if (slot >= p.num_slots) {
+        if (threadIdx.x == 0)
+            record_error(p.err, PKV_DEV_BAD_SLOT);
+        return;
+    }
+    const int nvec = p.row / 8;  // 8 elements per vector
+    for (int which = 0; which < (p.alias ? 1 : 2); ++which) {
+        const uint4 *src =
+            reinterpret_cast<const uint4 *>((which ? p.v : p.k) + static_cast<int64_t>(t) * p.row);
+        if constexpr (!INT8) {
+            uint4 *dst = reinterpret_cast<uint4 *>(static_cast<uint16_t *>(which ? p.pool_v : p.pool_k) +
+                                                   slot * p.row);
+            for (int i = threadIdx.x; i < nvec; i += blockDim.x)
+                dst[i] = src[i];
+        } else {
+            uint2 *dst = reinterpret_cast<uint2 *>(static_cast<int8_t *>(which ? p.pool_v : p.pool_k) +
+                                                   slot * p.row);
+            float *tbl = which ? p.v_scale : p.k_scale;
+            float scale = 0.f;
+            if (p.scale_mode == PKV_SCALE_PER_TOKEN) {
+                float amax = 0.f;
+                for (int i = threadIdx.x; i < nvec; i += blockDim.x) {
+                    float f[8];
+                    unpack8(src[i], f);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e)
+                        amax = fmaxf(amax, fabsf(f[e]));
+                }
+                amax = block_max(amax, red);
+                scale = __fdiv_rn(amax, 127.f);
+                if (threadIdx.x == 0)
+                    tbl[slot] = scale;
+            }
+            for (int i = threadIdx.x; i < nvec; i += blockDim.x) {
+                float f[8];
+                unpack8(src[i], f);
+                const float s = p.scale_mode == PKV_SCALE_PER_TOKEN ? scale : tbl[(i * 8) / p.head_dim];
+                int8_t q[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e)
+                    q[e] = quantize_one(f[e], s);
+                dst[i] = pack8(q);
+            }
+        }
+    }
+}
+
+cudaError_t launch_append(const AppendParams &p, int int8, cudaStream_t s)
+{
+    if (p.num_tokens <= 0)
+        return cudaSuccess;
+    if (int8)
+        append_kernel<true><<<p.num_tokens, APPEND_THREADS, 0, s>>>(p);
+    else
+        append_kernel<false><<<p.num_tokens, APPEND_THREADS, 0, s>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace pkv

@@ -1,0 +1,85 @@
+// pkv_internal.h -- host-side interface between the C-ABI layer and the
+// kernel launchers.  Not installed; not part of the public ABI.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "pagedkv.h"
+
+namespace pkv {
+
+constexpr int kBlock = 16;  // tokens per paged block (block_size)
+
+// Parameters of the decode kernels (passed by value to the kernel).
+struct DecodeParams {
+    const uint16_t *q;        // [B][H_q][D] bf16 bits
+    const int32_t *block_table;
+    const int32_t *seq_lens;
+    const float *k_scale;
+    const float *v_scale;
+    float *part_lse;          // [B][H_q][num_splits]
+    float *part_o;            // [B][H_q][num_splits][D]
+    void *out;                // [B][H_q][D]
+    int32_t max_blocks;       // block_table row length
+    int32_t scale_mode;
+    int32_t batch;
+    int32_t num_q_heads;
+    int32_t num_kv_heads;
+    int32_t group;            // H_q / H_kv
+    int32_t head_chunks;      // CTAs per kv head along the query group
+    int32_t num_blocks;       // pool blocks
+    int32_t window;
+    int32_t max_seq_len;
+    int32_t split_blocks;     // paged blocks per split; 0 = single pass
+    int32_t num_splits;       // grid extent along splits
+    int32_t alias;            // K and V are one tensor
+    int32_t out_f32;
+    int32_t num_stages;       // smem ring depth
+    float qk_scale_log2;      // softmax_scale * log2(e)
+    unsigned int *err;        // device error word
+};
+
+struct AppendParams {
+    const uint16_t *k;
+    const uint16_t *v;
+    const int64_t *slot_mapping;
+    void *pool_k;
+    void *pool_v;
+    float *k_scale;
+    float *v_scale;
+    int32_t num_tokens;
+    int32_t row;              // num_kv_heads * head_dim
+    int32_t head_dim;
+    int64_t num_slots;
+    int32_t scale_mode;
+    int32_t alias;
+    unsigned int *err;
+};
+
+struct CombineParams {
+    const float *part_lse;
+    const float *part_o;
+    const int32_t *seq_lens;
+    void *out;
+    int32_t batch;
+    int32_t num_q_heads;
+    int32_t head_dim;
+    int32_t window;
+    int32_t split_blocks;
+    int32_t num_splits;
+    int32_t out_f32;
+};
+
+// CUDA-core decode kernel family (TMA-fed smem ring, one CTA per
+// (split, kv head, head chunk, sequence)).
+int decode_group_tile(int group);  // query heads per CTA for a GQA group
+size_t decode_smem_bytes(int head_dim, int int8, int alias, int per_token, int group_tile,
+                         int num_stages);
+cudaError_t launch_decode(const DecodeParams &p, const CUtensorMap &tmk, const CUtensorMap &tmv,
+                          int head_dim, int int8, int group_tile, cudaStream_t s);
+cudaError_t launch_combine(const CombineParams &p, cudaStream_t s);
+cudaError_t launch_append(const AppendParams &p, int int8, cudaStream_t s);
+
+}  // namespace pkv

@@ -1,0 +1,282 @@
+"""GPU parity: the CUDA path through the C ABI against the CPU oracle on the
+same seeded inputs.  Append/quantise must be bit-exact; attention must match
+within max |err| <= 2e-2 on bf16 outputs and a normwise per-row relative
+error <= 1e-4 on fp32 outputs."""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+
+import oracle  # noqa: E402
+import paged_kv_decode_03_gb300 as pkv  # noqa: E402
+from paged_kv_decode_03_gb300 import synth  # noqa: E402
+from tests import _util  # noqa: E402
+
+pytestmark = pytest.mark.gpu
+
+BF16_TOL = 2e-2
+F32_REL_TOL = 1e-4
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _device():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    pkv.load_library()
+    pkv.device_status(clear=True)
+    yield
+    torch.cuda.synchronize()
+
+
+from tests import _gpu  # noqa: E402
+
+
+def _check_pool_bits(gpu_pool, ora_pool):
+    k, v, ks, vs = _gpu.pool_to_host(gpu_pool)
+    assert np.array_equal(k, ora_pool.k), "K pool differs from the oracle's append"
+    if ora_pool.v is not None:
+        assert np.array_equal(v, ora_pool.v), "V pool differs from the oracle's append"
+    if ora_pool.scale_mode == oracle.SCALE_PER_TOKEN:
+        assert np.array_equal(ks.view(np.uint32), ora_pool.k_scale.view(np.uint32))
+        if ora_pool.v_scale is not None:
+            assert np.array_equal(vs.view(np.uint32), ora_pool.v_scale.view(np.uint32))
+
+
+def _run_case(spec, splits=(0, pkv.SPLIT_AUTO), out_modes=(False, True), check_pool=True):
+    w = synth.make_workload(spec)
+    gp = _gpu.device_pool(w)
+    _gpu.append_all(w, gp)
+    op = _util.oracle_pool(w)
+    torch.cuda.synchronize()
+    if check_pool:
+        _check_pool_bits(gp, op)
+    ref = _util.oracle_decode(w, op)
+    step = _gpu.DeviceStep(w)
+    for st in splits:
+        for f32 in out_modes:
+            got = _gpu.out_to_f64(step.decode(gp, split_tokens=st, out_f32=f32))
+            torch.cuda.synchronize()
+            if f32:
+                err = _gpu.max_row_rel_err(got, ref)
+                assert err <= F32_REL_TOL, (spec.name, st, "f32", err)
+            else:
+                err = _gpu.max_abs_err(got, ref)
+                assert err <= BF16_TOL, (spec.name, st, "bf16", err)
+    assert pkv.device_status(clear=True) == 0
+    return w, gp, op, ref
+
+
+def test_c1_tiny_global():
+    _run_case(synth.C1, splits=(0, 16, 32, pkv.SPLIT_AUTO))
+
+
+def test_c2_sliding_small():
+    spec = synth.shrink(synth.C2, batch=8, lens=("uniform", 1, 3000))
+    _run_case(spec, splits=(0, 256, 1024, pkv.SPLIT_AUTO))
+
+
+def test_c3_global_kv_shared_small():
+    spec = synth.shrink(synth.C3, batch=4, lens=("uniform", 1, 5000))
+    _run_case(spec, splits=(0, 1024, pkv.SPLIT_AUTO))
+
+
+def test_c4_int8_per_token_small():
+    spec = synth.shrink(synth.C4, batch=4, lens=("const", 300))
+    _run_case(spec, splits=(0, 64, pkv.SPLIT_AUTO))
+
+
+def test_c5_step_small():
+    """Six layers (5 sliding int8 per-head + 1 global bf16) over one ragged
+    layout with shared prefix blocks: append one token per sequence, then
+    decode, layer by layer."""
+    s = synth.shrink(synth.C5_SLIDING, batch=24, lens=("lognormal", 300.0, 1.0, 1, 4000),
+                     shared_prefix_seqs=6)
+    g = synth.shrink(synth.C5_GLOBAL, batch=24, lens=("lognormal", 300.0, 1.0, 1, 4000),
+                     shared_prefix_seqs=6)
+    layers = synth.make_step(s, g)
+    for w in layers:
+        gp = _gpu.device_pool(w)
+        _gpu.append_all(w, gp)
+        op = _util.oracle_pool(w)
+        torch.cuda.synchronize()
+        _check_pool_bits(gp, op)
+        ref = _util.oracle_decode(w, op)
+        got = _gpu.out_to_f64(_gpu.DeviceStep(w).decode(gp))
+        assert _gpu.max_abs_err(got, ref) <= BF16_TOL
+    assert pkv.device_status(clear=True) == 0
+
+
+@pytest.mark.parametrize("D", [64, 128, 256])
+@pytest.mark.parametrize("kv", ["bf16", "int8_token", "int8_head"])
+@pytest.mark.parametrize("hq,hkv", [(2, 2), (6, 2), (8, 2), (16, 1)])
+def test_edge_shapes(D, kv, hq, hkv):
+    """Ragged lengths at block edges (0, 1, 15, 16, 17, 33, ...), GQA group
+    sizes 1, 3, 4, 16, every head_dim, every KV format."""
+    spec = synth.Spec(f"edge_{D}_{kv}_{hq}_{hkv}", batch=9, num_q_heads=hq, num_kv_heads=hkv,
+                      head_dim=D, lens=("fixed", (0, 1, 15, 16, 17, 33, 64, 100, 257)), kv=kv,
+                      seed=77 + D + hq)
+    _run_case(spec, splits=(0, 16, 48, pkv.SPLIT_AUTO))
+
+
+@pytest.mark.parametrize("window", [1, 15, 16, 17, 100, 5000])
+def test_window_edges(window):
+    spec = synth.Spec(f"win_{window}", batch=7, num_q_heads=4, num_kv_heads=2, head_dim=128,
+                      lens=("fixed", (1, 2, 16, 17, 18, 130, 700)), window=window, seed=91)
+    _run_case(spec, splits=(0, 32, pkv.SPLIT_AUTO))
+
+
+def test_int8_kv_alias_per_token():
+    spec = synth.Spec("alias_int8", batch=5, num_q_heads=8, num_kv_heads=1, head_dim=256,
+                      lens=("fixed", (1, 40, 200, 333, 17)), kv="int8_token", alias=True, seed=5)
+    _run_case(spec, splits=(0, 64))
+
+
+def test_split_partial_matches_oracle_partials():
+    """paged_decode_split_partial writes, per split, the log-sum-exp and the
+    normalised output of that split's keys."""
+    spec = synth.shrink(synth.C2, batch=6, num_q_heads=4, num_kv_heads=2, head_dim=128,
+                        lens=("fixed", (5, 300, 1100, 1500, 2000, 64)), window=1024)
+    w = synth.make_workload(spec)
+    gp = _gpu.device_pool(w)
+    _gpu.append_all(w, gp)
+    op = _util.oracle_pool(w)
+    step = _gpu.DeviceStep(w)
+    split = 256
+    ns = pkv.paged_decode_num_splits(step.max_seq_len, spec.window, split)
+    B, Hq, D = w.q.shape
+    lse = torch.full((B, Hq, ns), float("nan"), device="cuda")
+    po = torch.full((B, Hq, ns, D), float("nan"), device="cuda")
+    out = torch.zeros((B, Hq, D), dtype=torch.float32, device="cuda")
+    pkv.paged_decode_split_partial(step.q, gp, step.block_table, step.seq_lens, spec.window,
+                                   np.float32(spec.softmax_scale), split, lse, po, out,
+                                   step.max_seq_len)
+    torch.cuda.synchronize()
+    lse_h, po_h, out_h = lse.cpu().numpy(), po.cpu().numpy(), out.cpu().numpy()
+    full = _util.oracle_decode(w, op)
+    for b in range(B):
+        L = int(w.seq_lens[b])
+        pos = L - 1
+        lo = max(0, pos - spec.window)
+        nblk = pos // 16 - lo // 16 + 1
+        nsb = -(-nblk // (split // 16))
+        if nsb == 1:
+            assert _gpu.max_row_rel_err(out_h[b].astype(np.float64), full[b]) <= F32_REL_TOL
+            continue
+        for s in range(nsb):
+            kb = (lo // 16 + s * (split // 16)) * 16
+            ke = kb + split
+            ol, oo = oracle.partial(w.q, op, w.block_table, w.seq_lens, Hq, spec.window,
+                                    np.float32(spec.softmax_scale),
+                                    np.full(B, kb), np.full(B, ke))
+            np.testing.assert_allclose(lse_h[b, :, s], ol[b], rtol=0, atol=2e-5)
+            assert _gpu.max_row_rel_err(po_h[b, :, s].astype(np.float64), oo[b]) <= F32_REL_TOL
+    # the combine step on these partials gives the full decode
+    out2 = out.clone()
+    pkv.paged_decode_lse_combine(lse, po, step.seq_lens, spec.window, split, out2)
+    torch.cuda.synchronize()
+    assert _gpu.max_row_rel_err(out2.cpu().numpy().astype(np.float64), full) <= F32_REL_TOL
+
+
+def test_lse_combine_on_given_partials():
+    """The combine alone, on partial states computed by the oracle."""
+    rng = np.random.default_rng(3)
+    B, Hq, ns, D = 3, 2, 4, 64
+    lens = np.array([16 * 4 * 3, 16 * 4 * 4, 16 * 4 + 1], np.int32)  # 3, 4 and 2 splits of 64
+    lse = rng.normal(size=(B, Hq, ns)).astype(np.float32) * 3
+    po = rng.normal(size=(B, Hq, ns, D)).astype(np.float32)
+    lse[0, :, 3] = np.nan  # beyond sequence 0's splits: must be ignored
+    out = torch.zeros((B, Hq, D), dtype=torch.float32, device="cuda")
+    pkv.paged_decode_lse_combine(_gpu.to_dev(lse), _gpu.to_dev(po), _gpu.to_dev(lens), 0, 64, out)
+    torch.cuda.synchronize()
+    got = out.cpu().numpy()
+    for b, nsb in enumerate((3, 4, 2)):
+        for h in range(Hq):
+            y, _ = oracle.lse_combine(lse[b, h, :nsb].astype(np.float64),
+                                      po[b, h, :nsb].astype(np.float64))
+            np.testing.assert_allclose(got[b, h], y, rtol=2e-5, atol=2e-6)
+
+
+def test_bad_block_id_is_reported_not_faulted():
+    spec = synth.Spec("badblk", batch=3, num_q_heads=4, num_kv_heads=2, head_dim=64,
+                      lens=("fixed", (40, 40, 40)), seed=8)
+    w = synth.make_workload(spec)
+    gp = _gpu.device_pool(w)
+    _gpu.append_all(w, gp)
+    op = _util.oracle_pool(w)
+    ref = _util.oracle_decode(w, op)
+    step = _gpu.DeviceStep(w)
+    pkv.device_status(clear=True)
+    bt = w.block_table.copy()
+    bt[1, 1] = w.layout.num_blocks + 1000
+    step.block_table = _gpu.to_dev(bt)
+    got = _gpu.out_to_f64(step.decode(gp, split_tokens=0))
+    torch.cuda.synchronize()
+    assert pkv.device_status(clear=True) & 1  # PKV_DEV_BAD_BLOCK
+    # the other sequences are unaffected
+    assert _gpu.max_abs_err(got[[0, 2]], ref[[0, 2]]) <= BF16_TOL
+
+
+def test_bad_slot_is_reported_not_faulted():
+    spec = synth.Spec("badslot", batch=2, num_q_heads=2, num_kv_heads=2, head_dim=64,
+                      lens=("fixed", (5, 5)), seed=9)
+    w = synth.make_workload(spec)
+    gp = _gpu.device_pool(w)
+    before = gp.k.clone()
+    pkv.device_status(clear=True)
+    slots = np.array([w.layout.num_blocks * 16 + 3, -1], np.int64)
+    pkv.paged_kv_append(_gpu.to_dev_bits(w.new_k), _gpu.to_dev_bits(w.new_v), _gpu.to_dev(slots), gp)
+    torch.cuda.synchronize()
+    assert pkv.device_status(clear=True) & 4  # PKV_DEV_BAD_SLOT
+    assert torch.equal(gp.k.view(torch.int16), before.view(torch.int16))
+
+
+def test_length_beyond_host_bound_is_reported():
+    spec = synth.Spec("bound", batch=2, num_q_heads=2, num_kv_heads=1, head_dim=64,
+                      lens=("fixed", (100, 20)), seed=10)
+    w = synth.make_workload(spec)
+    gp = _gpu.device_pool(w)
+    _gpu.append_all(w, gp)
+    step = _gpu.DeviceStep(w)
+    step.max_seq_len = 50  # lies: sequence 0 has 100 keys
+    pkv.device_status(clear=True)
+    step.decode(gp, split_tokens=16)
+    torch.cuda.synchronize()
+    assert pkv.device_status(clear=True) & 16  # PKV_DEV_LEN_BOUND
+
+
+def test_graph_capture_replays_the_step():
+    """The calls read no device data on the host, so a decode step captures
+    into a CUDA graph and replays with new inputs in the same buffers."""
+    spec = synth.shrink(synth.C2, batch=4, lens=("uniform", 100, 2000))
+    w = synth.make_workload(spec)
+    gp = _gpu.device_pool(w)
+    _gpu.append_all(w, gp, new=False)
+    op = _util.oracle_pool(w)
+    step = _gpu.DeviceStep(w)
+    k_new, v_new, slots = (_gpu.to_dev_bits(w.new_k), _gpu.to_dev_bits(w.new_v),
+                           _gpu.to_dev(w.new_slots))
+    B, Hq, D = w.q.shape
+    out = torch.empty((B, Hq, D), dtype=torch.bfloat16, device="cuda")
+    ws = torch.empty(max(1, pkv.paged_decode_workspace_bytes(B, Hq, spec.num_kv_heads, D,
+                                                             step.max_seq_len, spec.window)),
+                     dtype=torch.uint8, device="cuda")
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        # warm-up outside capture
+        pkv.paged_kv_append(k_new, v_new, slots, gp)
+        pkv.paged_decode_attention(step.q, gp, step.block_table, step.seq_lens, spec.window,
+                                   spec.softmax_scale, out, step.max_seq_len, workspace=ws)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        pkv.paged_kv_append(k_new, v_new, slots, gp)
+        pkv.paged_decode_attention(step.q, gp, step.block_table, step.seq_lens, spec.window,
+                                   spec.softmax_scale, out, step.max_seq_len, workspace=ws)
+    out.zero_()
+    g.replay()
+    torch.cuda.synchronize()
+    oracle.append(w.new_k, w.new_v, w.new_slots, op)
+    ref = _util.oracle_decode(w, op)
+    assert _gpu.max_abs_err(_gpu.out_to_f64(out), ref) <= BF16_TOL

@@ -408,3 +408,28 @@ def test_oracle_threads_do_not_change_results():
     a = _util.oracle_decode(w, pool, num_threads=1)
     b = _util.oracle_decode(w, pool, num_threads=4)
     np.testing.assert_array_equal(a, b)
+
+
+# --------------------------------------------------------------- byte model
+def test_kv_cache_bytes_worked_example():
+    """CS336 lecture 10, KV-cache size section: n_kv=64, d_h=128, bf16 gives
+    32 KiB per token per layer; S=100,000 tokens and L=80 layers give about
+    244 GiB (262 GB)."""
+    from paged_kv_decode_03_gb300 import bytes_model as bm
+    assert bm.kv_cache_bytes(1, 1, 64, 128, 2) == 32 * 1024
+    total = bm.kv_cache_bytes(80, 100_000, 64, 128, 2)
+    assert round(total / 2**30) == 244 and round(total / 1e9) == 262
+
+
+def test_decode_bytes_counts_window_keys_once():
+    from paged_kv_decode_03_gb300 import bytes_model as bm
+    spec = synth.shrink(synth.C2, batch=3, lens=("fixed", (1, 1025, 5000)))
+    w = synth.make_workload(spec)
+    d = bm.decode_bytes(spec, w.seq_lens, w.block_table)
+    assert d["keys"] == 1 + 1025 + 1025
+    assert d["kv"] == d["unique_keys"] * 8 * 256 * 2 * 2
+    # shared prefix blocks are read once
+    g = synth.shrink(synth.C5_GLOBAL, batch=10, lens=("uniform", 140, 200), shared_prefix_seqs=4)
+    wg = synth.make_workload(g)
+    dg = bm.decode_bytes(g, wg.seq_lens, wg.block_table)
+    assert dg["keys"] - dg["unique_keys"] == 3 * 8 * 16
