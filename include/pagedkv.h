@@ -22,7 +22,8 @@
  *  - All pointers are DEVICE pointers unless stated; the caller allocates and
  *    owns every buffer.  The library allocates no device memory and keeps no
  *    state except a thread-local error string, an error word in device
- *    memory (pkv_device_status) and per-device launch attributes.
+ *    memory (pkv_device_status), per-device launch attributes and the fixed
+ *    scratch array of paged_decode_attention_noalloc.
  *  - Work is enqueued asynchronously on `stream` (a cudaStream_t; NULL = the
  *    legacy default stream).  No call synchronises or reads device data on
  *    the host, so the calls may be captured in a CUDA graph.
@@ -226,6 +227,36 @@ PKV_API int paged_decode_lse_combine(const float *partial_lse, const float *part
                                      int32_t head_dim, int32_t block_size, int32_t window,
                                      int32_t split_tokens, int32_t num_splits, void *out,
                                      int32_t out_dtype, void *stream);
+
+/*
+ * paged_decode_attention_noalloc -- paged_decode_attention for callers that
+ * cannot allocate device memory and so cannot pass a workspace: a plugin
+ * whose host framework gives it only its inputs and outputs, an engine that
+ * has already reserved all of HBM for its KV pool, or a latency-critical
+ * loop in which cudaMalloc/cudaFree would synchronise the device.  None of
+ * the pages has a counterpart; this is a library convenience.
+ *   Same arguments and result as paged_decode_attention, minus the
+ *   workspace.  The split-KV partials go to a fixed array of
+ *   PKV_STATIC_SCRATCH_BYTES in device memory that every GPU which loads the
+ *   library holds until the process exits.  Sizes whose scratch would not
+ *   fit are rejected with PKV_E_WORKSPACE before anything is launched.
+ *   Nothing here calls cudaMalloc, cudaFree or any allocating routine.
+ *   The first call on a device looks the array's address up on that device
+ *   (cudaGetSymbolAddress, the device current); make that first call before
+ *   any stream capture.  All calls share the one array and it keeps the
+ *   previous call's contents (no part of it needs to start at zero: every
+ *   partial is written before it is read), so calls that overlap on the GPU
+ *   -- on two streams, or from two threads -- race and must be serialised by
+ *   the caller.
+ */
+#define PKV_STATIC_SCRATCH_BYTES (32u << 20) /* 32 MiB per device */
+PKV_API int paged_decode_attention_noalloc(const void *q, const pkv_pool *pool,
+                                           const int32_t *block_table, int32_t max_blocks_per_seq,
+                                           const int32_t *seq_lens, int32_t batch,
+                                           int32_t num_q_heads, int32_t max_seq_len,
+                                           int32_t window, float softmax_scale,
+                                           int32_t split_tokens, void *out, int32_t out_dtype,
+                                           void *stream);
 
 /* Message of the last host-side error on this thread ("" if none). */
 PKV_API const char *pkv_last_error(void);

@@ -11,6 +11,7 @@ from .binding import (  # noqa: F401
     PKV_BF16, PKV_INT8, SCALE_NONE, SCALE_PER_TOKEN, SCALE_PER_HEAD, SPLIT_AUTO, OUT_BF16, OUT_F32,
     PagedKVPool, paged_kv_append, paged_decode_attention, paged_decode_split_partial,
     paged_decode_lse_combine, paged_decode_workspace_bytes, paged_decode_num_splits,
-    paged_decode_split_tokens, PagedKVError,
+    paged_decode_split_tokens, PagedKVError, paged_decode_attention_noalloc,
+    STATIC_SCRATCH_BYTES,
     library_path, load_library, device_status, exported_symbols,
 )

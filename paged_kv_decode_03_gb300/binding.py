@@ -73,6 +73,9 @@ def load_library():
     lib.paged_decode_lse_combine.argtypes = [p, p, p, i32, i32, i32, i32, i32, i32, i32, p, i32,
                                              p]
     lib.paged_decode_lse_combine.restype = ctypes.c_int
+    lib.paged_decode_attention_noalloc.argtypes = [p, p, p, i32, p, i32, i32, i32, i32, f32,
+                                                   i32, p, i32, p]
+    lib.paged_decode_attention_noalloc.restype = ctypes.c_int
     lib.pkv_last_error.argtypes = []
     lib.pkv_last_error.restype = ctypes.c_char_p
     lib.pkv_device_status.argtypes = [i32]
@@ -257,6 +260,33 @@ def paged_decode_lse_combine(partial_lse, partial_o, seq_lens, window: int, spli
                                         _dev_ptr(seq_lens, "seq_lens"), B, Hq, D, block_size, int(window),
                                         int(split_tokens), ns, _dev_ptr(out, "out"), out_dtype,
                                         _stream(stream)), "paged_decode_lse_combine")
+
+
+STATIC_SCRATCH_BYTES = 32 << 20  # PKV_STATIC_SCRATCH_BYTES in include/pagedkv.h
+
+
+def paged_decode_attention_noalloc(q, pool: PagedKVPool, block_table, seq_lens, window: int,
+                                   softmax_scale: float, out, max_seq_len: int,
+                                   split_tokens: int = SPLIT_AUTO, stream=None):
+    """paged_decode_attention without a workspace, for callers that cannot
+    allocate device memory (a plugin handed only its inputs and outputs, an
+    engine that reserved all of HBM for its KV pool, a loop where an
+    allocation would synchronise the device).  Split partials go to the
+    library's fixed per-device scratch array (STATIC_SCRATCH_BYTES); sizes
+    that do not fit raise.  Calls share that array: do not let two of them
+    overlap on the GPU.  The first call on a device looks the array up; make
+    it before any stream capture."""
+    import torch
+    lib = load_library()
+    pc = pool.c_struct()
+    B, Hq, D = (int(x) for x in q.shape)
+    out_dtype = OUT_F32 if out.dtype == torch.float32 else OUT_BF16
+    _check(lib.paged_decode_attention_noalloc(
+        _dev_ptr(q, "q"), ctypes.byref(pc), _dev_ptr(block_table, "block_table"),
+        int(block_table.shape[1]), _dev_ptr(seq_lens, "seq_lens"), B, Hq, int(max_seq_len),
+        int(window), float(softmax_scale), int(split_tokens), _dev_ptr(out, "out"), out_dtype,
+        _stream(stream)), "paged_decode_attention_noalloc")
+    return out
 
 
 def device_status(clear: bool = True) -> int:

@@ -495,3 +495,77 @@ PKV_API int paged_decode_attention(const void *q, const pkv_pool *pool, const in
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Decode for callers that cannot allocate device memory.
+//
+// paged_decode_attention needs a caller-provided workspace whenever it splits
+// the key range.  Some callers have no way to provide one: a plugin whose
+// host framework hands it only its input and output buffers, an engine that
+// reserved all of HBM up front for its KV pool, or a latency-critical loop in
+// which cudaMalloc/cudaFree would synchronise the device.  For them the split
+// partials live in the fixed array below, which every device that loads this
+// library holds until the process exits.
+namespace pkv {
+
+constexpr size_t kStaticScratchBytes = PKV_STATIC_SCRATCH_BYTES;
+static __device__ __align__(256) unsigned char g_static_scratch[kStaticScratchBytes];
+
+// Device address of g_static_scratch on the current device.  The host-side
+// name g_static_scratch is only a stand-in; the address comes from
+// cudaGetSymbolAddress, looked up once per device with that device current.
+static void *static_scratch_ptr()
+{
+    static std::mutex mu;
+    static void *ptrs[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+        fail(PKV_E_DRIVER, "cannot query the current device");
+        return nullptr;
+    }
+    std::lock_guard<std::mutex> lock(mu);
+    if (!ptrs[dev]) {
+        void *p = nullptr;
+        cudaError_t e = cudaGetSymbolAddress(&p, g_static_scratch);
+        if (e != cudaSuccess || p == nullptr) {
+            fail(PKV_E_DRIVER, "cudaGetSymbolAddress(static scratch): %s", cudaGetErrorString(e));
+            return nullptr;
+        }
+        ptrs[dev] = p;
+    }
+    return ptrs[dev];
+}
+
+}  // namespace pkv
+
+extern "C" PKV_API int paged_decode_attention_noalloc(
+    const void *q, const pkv_pool *pool, const int32_t *block_table, int32_t max_blocks_per_seq,
+    const int32_t *seq_lens, int32_t batch, int32_t num_q_heads, int32_t max_seq_len,
+    int32_t window, float softmax_scale, int32_t split_tokens, void *out, int32_t out_dtype,
+    void *stream)
+{
+    t_last_error.clear();
+    if (int rc = check_decode_args(q, pool, block_table, max_blocks_per_seq, seq_lens, batch,
+                                   num_q_heads, max_seq_len, window, out, out_dtype))
+        return rc;
+    const int32_t st = paged_decode_split_tokens(batch, num_q_heads, pool->num_kv_heads,
+                                                 pool->block_size, max_seq_len, window,
+                                                 split_tokens);
+    if (st < 0)
+        return st;
+    const size_t need = paged_decode_workspace_bytes(batch, num_q_heads, pool->num_kv_heads,
+                                                     pool->head_dim, pool->block_size,
+                                                     max_seq_len, window, st);
+    if (need > kStaticScratchBytes)
+        return fail(PKV_E_WORKSPACE,
+                    "these sizes need %zu bytes of scratch but the static scratch holds %zu "
+                    "(PKV_STATIC_SCRATCH_BYTES); use a longer split_tokens, a smaller batch, "
+                    "or paged_decode_attention with a workspace",
+                    need, kStaticScratchBytes);
+    void *ws = nullptr;
+    if (need > 0 && !(ws = static_scratch_ptr()))
+        return PKV_E_DRIVER;
+    return paged_decode_attention(q, pool, block_table, max_blocks_per_seq, seq_lens, batch,
+                                  num_q_heads, max_seq_len, window, softmax_scale, st, ws,
+                                  need > 0 ? kStaticScratchBytes : 0, out, out_dtype, stream);
+}
