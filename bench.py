@@ -51,7 +51,20 @@ def parse_args():
                     help="CPU time budget of the oracle baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--batch", type=int, default=0,
+                    help="override the workload's batch (smaller cases for profiling)")
+    ap.add_argument("--split-tokens", type=int, default=None,
+                    help="override the split length (0 = single pass, -1 = automatic)")
     return ap.parse_args()
+
+
+def workload_spec(args):
+    spec = synth.CONFIGS[args.config]
+    if args.batch:
+        spec = synth.shrink(spec, batch=args.batch)
+    if args.split_tokens is not None:
+        spec = synth.shrink(spec, split_tokens=args.split_tokens)
+    return spec
 
 
 # ------------------------------------------------------------------ helpers
@@ -163,7 +176,7 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
     pkv.load_library()
-    spec = synth.CONFIGS[args.config]
+    spec = workload_spec(args)
     w = synth.make_workload(spec)
     B, Hq, D = w.q.shape
     P = spec.block_size
@@ -206,8 +219,9 @@ def run_ours(args, rank, world, local_rank):
     out = torch.empty((B, Hq, D), dtype=torch.bfloat16, device=dev)
     max_len = int(w.seq_lens.max())
     scale = float(np.float32(spec.softmax_scale))
-    st = pkv.paged_decode_split_tokens(B, Hq, spec.num_kv_heads, max_len, spec.window,
-                                       spec.split_tokens or pkv.SPLIT_AUTO)
+    req = args.split_tokens if args.split_tokens is not None else (spec.split_tokens
+                                                                    or pkv.SPLIT_AUTO)
+    st = pkv.paged_decode_split_tokens(B, Hq, spec.num_kv_heads, max_len, spec.window, req)
     ns = pkv.paged_decode_num_splits(max_len, spec.window, st) if st > 0 else 1
     ws_bytes = pkv.paged_decode_workspace_bytes(B, Hq, spec.num_kv_heads, D, max_len,
                                                 spec.window, st)
@@ -434,7 +448,7 @@ def run_reference(args, rank):
     if rank != 0:
         return None
     import oracle
-    spec = synth.CONFIGS[args.config]
+    spec = workload_spec(args)
     w = synth.make_workload(spec)
     pool = oracle_setup(spec, w)
     threads = oracle.max_threads()
