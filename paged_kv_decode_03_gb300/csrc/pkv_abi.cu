@@ -147,12 +147,13 @@ static int sm_count()
     return n;
 }
 
-static int stages_per_warp()
+// Ring depth override for tuning sweeps (PKV_STAGES); 0 = automatic.
+static int stages_override()
 {
     static int v = [] {
-        const char *e = getenv("PKV_STAGES_PER_WARP");
-        int s = e ? atoi(e) : 2;
-        return s < 1 ? 1 : (s > 4 ? 4 : s);
+        const char *e = getenv("PKV_STAGES");
+        int s = e ? atoi(e) : 0;
+        return s < 0 ? 0 : (s > 16 ? 16 : s);
     }();
     return v;
 }
@@ -354,7 +355,19 @@ static int run_decode(const void *q, const pkv_pool *pool, const int32_t *block_
     p.num_splits = split_tokens > 0 ? num_splits : 1;
     p.alias = alias;
     p.out_f32 = out_dtype == PKV_OUT_F32;
-    p.num_stages = 4 * stages_per_warp();
+    // Ring depth: as many stages as fit in about a quarter of an SM's
+    // shared memory (four CTAs per SM: the consumer warps' dependency chains,
+    // not bytes in flight, limit a CTA, so more CTAs beat deeper rings),
+    // 2..16; PKV_STAGES overrides it within the opt-in limit of one CTA.
+    {
+        const int i8 = pool->dtype == PKV_INT8;
+        const int pt = pool->scale_mode == PKV_SCALE_PER_TOKEN;
+        const size_t budget = stages_override() ? 227u * 1024u : 56u * 1024u;
+        int ns = stages_override() ? stages_override() : 16;
+        while (ns > 2 && decode_smem_bytes(pool->head_dim, i8, alias, pt, gt, ns) > budget)
+            --ns;
+        p.num_stages = ns;
+    }
     p.qk_scale_log2 = softmax_scale * LOG2E;
     p.err = error_word_ptr();
     if (!p.err)

@@ -38,7 +38,7 @@ namespace pkv {
 
 constexpr int NC = 4;                    // consumer warps per CTA
 constexpr int THREADS = (NC + 1) * 32;   // + one producer warp
-constexpr int BAR_BYTES = 256;           // mbarrier area at the start of smem
+constexpr int BAR_BYTES = 512;           // mbarrier area at the start of smem
 
 struct KeyRange {
     int lo, pos, blk_lo, nblk, nsplit;
@@ -66,33 +66,47 @@ __device__ __forceinline__ KeyRange key_range(int len, int window, int split_blo
 template <int D, int GT, bool INT8>
 struct Cfg {
     static constexpr int P = kBlock;
-    static constexpr int ES = INT8 ? 1 : 2;                // element bytes
+    static constexpr int ES = INT8 ? 1 : 2;                    // element bytes
     static constexpr int CHE = (D * ES > 256) ? 256 / ES : D;  // elements per TMA box row
-    static constexpr int NCH = D / CHE;                     // boxes per tile
-    static constexpr int ROWB = CHE * ES;                   // bytes of one box row
-    static constexpr int TILE = P * D * ES;                 // one kv head x one block
-    static constexpr int DPL = D / 32;                      // elements per lane
-    static constexpr int NV = (GT == 1) ? 16 : 32;          // dot products per reduction
-    static constexpr int R = NV / GT;                       // keys per reduction group
-    static constexpr int GROUPS = P / R;
+    static constexpr int NCH = D / CHE;                         // boxes per tile
+    static constexpr int ROWB = CHE * ES;                       // bytes of one box row
+    static constexpr int TILE = P * D * ES;                     // one kv head x one block
+    static constexpr int DPL = D / 32;                          // elements per lane
+    static constexpr int NP = DPL / 2;                          // element pairs per lane
+    // Paged blocks per ring stage: about 8 KB of K per stage, and at most
+    // 32 / GT keys per consumer warp so one reduce-scatter covers them.
+    static constexpr int BPS_MEM = (8192 / TILE) < 1 ? 1 : (8192 / TILE);
+    static constexpr int BPS_MAX = 8 / GT;
+    static constexpr int BPS = BPS_MEM < BPS_MAX ? BPS_MEM : BPS_MAX;
+    static constexpr int KEYS = P * BPS;                        // keys per stage
+    static constexpr int KPW = KEYS / NC;                       // keys per warp per stage
+    static constexpr int NV = KPW * GT;                         // dot products per reduction
+    static constexpr int LOGNV = NV == 4 ? 2 : NV == 8 ? 3 : NV == 16 ? 4 : 5;
+    static constexpr int DUP = 32 / NV;                         // lanes holding each sum
     static_assert(D % 32 == 0 && DPL >= 2 && DPL <= 8, "head_dim");
-    static_assert(P % R == 0, "group");
+    static_assert(NV >= 4 && NV <= 32, "reduction width");
+    static_assert(KPW <= P || KPW % P == 0, "warp keys within or across whole blocks");
 };
 
 __host__ __device__ constexpr int round_up(int x, int a) { return (x + a - 1) / a * a; }
 
-// Bytes of one ring stage: K tile, V tile (unless aliased), per-token scales.
-__host__ __device__ inline int stage_bytes(int tile, int alias, int per_token)
+// Bytes of one ring slot: bps K (or V) tiles plus their per-token scales.
+__host__ __device__ inline int slot_bytes(int tile, int bps, int per_token)
 {
-    int b = tile + (alias ? 0 : tile);
-    if (per_token)
-        b += 128;  // 16 K scales + 16 V scales
-    return round_up(b, 128);
+    return round_up(bps * tile + (per_token ? bps * 64 : 0), 128);
 }
 
-// Butterfly reduce-scatter of NV per-lane partial sums: afterwards lane l
-// holds the full warp sum of value index l (NV == 32) or l >> 1 (NV == 16).
-template <int NV>
+__host__ __device__ constexpr int blocks_per_stage(int tile, int gt)
+{
+    return (8192 / tile) < 1 ? 1 : ((8192 / tile) < 8 / gt ? (8192 / tile) : 8 / gt);
+}
+
+// Butterfly reduce-scatter of NV per-lane partial sums (NV = 4..32): after
+// log2(NV) halving steps lane l holds value index l >> (5 - log2 NV) summed
+// over the lanes that share its top bits; the remaining xor steps complete
+// the sum, so every lane of a DUP = 32/NV lane group holds the full sum.
+// Costs NV - 1 + 5 - log2(NV) shuffles for NV dot products.
+template <int NV, int LOGNV>
 __device__ __forceinline__ float reduce_scatter(float (&v)[NV], int lane)
 {
 #pragma unroll
@@ -106,16 +120,82 @@ __device__ __forceinline__ float reduce_scatter(float (&v)[NV], int lane)
         }
     }
     float r = v[0];
-    if constexpr (NV == 16)
-        r += __shfl_xor_sync(FULL_MASK, r, 1);
+    if constexpr (LOGNV < 5) {
+#pragma unroll
+        for (int off = 1 << (4 - LOGNV); off >= 1; off >>= 1)
+            r += __shfl_xor_sync(FULL_MASK, r, off);
+    }
     return r;
 }
 
-template <int NV, int R>
-__device__ __forceinline__ int lane_of(int h, int r)
+// Element pairs of one lane's slice of a tile row, as float2 (exact).
+// bf16: the two halves of each 32-bit word.  int8: each byte b is placed in
+// the low mantissa bits of 2^23 (after flipping its sign bit, giving b+128)
+// and 2^23+128 is subtracted, which yields b exactly.
+template <int NP, bool INT8>
+__device__ __forceinline__ void load_pairs(const uint8_t *p, float2 (&f)[NP])
 {
-    return NV == 32 ? h * R + r : 2 * r;
+    if constexpr (!INT8) {
+        uint32_t w[NP];
+        if constexpr (NP == 4) {
+            const uint4 u = *reinterpret_cast<const uint4 *>(p);
+            w[0] = u.x; w[1] = u.y; w[2] = u.z; w[3] = u.w;
+        } else if constexpr (NP == 2) {
+            const uint2 u = *reinterpret_cast<const uint2 *>(p);
+            w[0] = u.x; w[1] = u.y;
+        } else {
+            w[0] = *reinterpret_cast<const uint32_t *>(p);
+        }
+#pragma unroll
+        for (int i = 0; i < NP; ++i)
+            f[i] = make_float2(bf16lo(w[i]), bf16hi(w[i]));
+    } else {
+        constexpr int NW = (NP * 2 + 3) / 4;  // 32-bit words holding 2*NP bytes
+        uint32_t w[NW];
+        if constexpr (NP == 4) {
+            const uint2 u = *reinterpret_cast<const uint2 *>(p);
+            w[0] = u.x; w[1] = u.y;
+        } else if constexpr (NP == 2) {
+            w[0] = *reinterpret_cast<const uint32_t *>(p);
+        } else {
+            w[0] = *reinterpret_cast<const uint16_t *>(p);
+        }
+        const float2 bias = make_float2(-8388736.0f, -8388736.0f);  // -(2^23 + 128)
+#pragma unroll
+        for (int i = 0; i < NP; ++i) {
+            const uint32_t x = w[i / 2] ^ 0x80808080u;
+            const int b0 = (i % 2) * 2;
+            const float lo = __uint_as_float(__byte_perm(x, 0x4B000000u, 0x7540 + b0));
+            const float hi = __uint_as_float(__byte_perm(x, 0x4B000000u, 0x7540 + b0 + 1));
+            f[i] = __fadd2_rn(make_float2(lo, hi), bias);
+        }
+    }
 }
+
+// Block-table entries of a unit, read 32 at a time by a whole warp: lane j
+// holds entry base + j of the current chunk, the next chunk is fetched half
+// a chunk ahead, and entry i is shuffled out, so no iteration waits on a
+// global load.
+struct TableCursor {
+    const int32_t *row;
+    int n, cur, nxt;
+    __device__ __forceinline__ void init(const int32_t *r, int count, int lane)
+    {
+        row = r;
+        n = count;
+        cur = lane < n ? __ldg(row + lane) : -1;
+        nxt = 32 + lane < n ? __ldg(row + 32 + lane) : -1;
+    }
+    // entry i (all lanes call with the same i, in increasing order)
+    __device__ __forceinline__ int get(int i, int lane)
+    {
+        if ((i & 31) == 0 && i > 0) {
+            cur = nxt;
+            nxt = i + 32 + lane < n ? __ldg(row + i + 32 + lane) : -1;
+        }
+        return __shfl_sync(FULL_MASK, cur, i & 31);
+    }
+};
 
 template <int D, int GT, bool INT8>
 __global__ void __launch_bounds__(THREADS) decode_kernel(const DecodeParams p,
@@ -123,9 +203,12 @@ __global__ void __launch_bounds__(THREADS) decode_kernel(const DecodeParams p,
                                                          const __grid_constant__ CUtensorMap tmv)
 {
     using C = Cfg<D, GT, INT8>;
+    constexpr int BPS = C::BPS;
     extern __shared__ __align__(128) uint8_t smem[];
-    uint64_t *full = reinterpret_cast<uint64_t *>(smem);
-    uint64_t *empty = full + 16;
+    uint64_t *kfull = reinterpret_cast<uint64_t *>(smem);
+    uint64_t *kempty = kfull + 16;
+    uint64_t *vfull = kfull + 32;
+    uint64_t *vempty = kfull + 48;
     uint8_t *ring = smem + BAR_BYTES;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -134,9 +217,11 @@ __global__ void __launch_bounds__(THREADS) decode_kernel(const DecodeParams p,
     const int chunk = blockIdx.y - g * p.head_chunks;
     const int b = blockIdx.z;
     const int NS = p.num_stages;
+    const bool alias = p.alias != 0;
     const bool per_token = INT8 && p.scale_mode == PKV_SCALE_PER_TOKEN;
     const bool per_head = INT8 && p.scale_mode == PKV_SCALE_PER_HEAD;
-    const int SB = stage_bytes(C::TILE, p.alias, per_token);
+    const int KS = slot_bytes(C::TILE, BPS, per_token);
+    const int SB = alias ? KS : 2 * KS;  // one stage: K slot [+ V slot]
 
     int len = p.seq_lens[b];
     const bool reporter = threadIdx.x == 0 && split == 0 && blockIdx.y == 0;
@@ -153,13 +238,16 @@ __global__ void __launch_bounds__(THREADS) decode_kernel(const DecodeParams p,
     const int ub0 = kr.blk_lo + split * p.split_blocks;
     const int ub1 = p.split_blocks > 0 ? min(ub0 + p.split_blocks, kr.blk_lo + kr.nblk)
                                        : kr.blk_lo + kr.nblk;
-    const int n = max(0, ub1 - ub0);
+    const int n = max(0, ub1 - ub0);          // paged blocks of this unit
+    const int nst = (n + BPS - 1) / BPS;      // ring stages of this unit
     const int32_t *bt_row = p.block_table + static_cast<size_t>(b) * p.max_blocks;
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < NS; ++i) {
-            mbar_init(&full[i], 1);
-            mbar_init(&empty[i], 1);
+            mbar_init(&kfull[i], 1);
+            mbar_init(&kempty[i], NC);
+            mbar_init(&vfull[i], 1);
+            mbar_init(&vempty[i], NC);
         }
         fence_barrier_init();
     }
@@ -167,56 +255,90 @@ __global__ void __launch_bounds__(THREADS) decode_kernel(const DecodeParams p,
 
     if (warp == NC) {
         // ------------------------------------------------------ producer
-        if (lane == 0 && n > 0) {
-            prefetch_tensormap(&tmk);
+        // The producer warp walks the stages in order.  Lane 0 fills the K
+        // slot of stage s % NS as soon as the consumers have formed the
+        // scores of its previous contents, then the V slot as soon as the
+        // previous P.V on it is done; the other lanes only help read the
+        // block table.
+        if (nst > 0) {
+            if (lane == 0) {
+                prefetch_tensormap(&tmk);
+                if (!alias)
+                    prefetch_tensormap(&tmv);
+            }
             const uint64_t pol = policy_evict_first();
-            const uint32_t tx = (p.alias ? 1 : 2) * C::TILE + (per_token ? (p.alias ? 64 : 128) : 0);
-            int issued = 0;
-            for (int i = 0; i < n; ++i) {
-                const int st = i % NS;
-                if (i >= NS && !mbar_wait(&empty[st], ((i / NS) - 1) & 1, p.err))
-                    break;
-                const int phys = bt_row[ub0 + i];
-                const bool valid = static_cast<unsigned>(phys) < static_cast<unsigned>(p.num_blocks);
-                if (!valid)
-                    record_error(p.err, PKV_DEV_BAD_BLOCK);
-                mbar_arrive_expect_tx(&full[st], valid ? tx : 0u);
-                ++issued;
-                if (!valid)
-                    continue;
-                uint8_t *kt = ring + st * SB;
-                uint8_t *vt = kt + C::TILE;
-                const int row0 = phys * C::P;
+            TableCursor tc;
+            tc.init(bt_row + ub0, n, lane);
+            int issued[2] = {0, 0};
+            bool ok = true;
+            for (int sidx = 0; sidx < nst && ok; ++sidx) {
+                const int st = sidx % NS;
+                const uint32_t prev = ((sidx / NS) - 1) & 1;
+                int phys[BPS];
+                uint32_t tx = 0;
 #pragma unroll
-                for (int ch = 0; ch < C::NCH; ++ch)
-                    tma_load_3d(kt + ch * C::P * C::ROWB, &tmk, ch * C::CHE, g, row0, &full[st], pol);
-                if (!p.alias) {
+                for (int t = 0; t < BPS; ++t) {
+                    const int i = sidx * BPS + t;
+                    phys[t] = i < n ? tc.get(i, lane) : -1;
+                    const bool valid = static_cast<unsigned>(phys[t]) <
+                                       static_cast<unsigned>(p.num_blocks);
+                    if (!valid && i < n && lane == 0)
+                        record_error(p.err, PKV_DEV_BAD_BLOCK);
+                    if (!valid)
+                        phys[t] = -1;
+                    else
+                        tx += C::TILE + (per_token ? 64u : 0u);
+                }
+                for (int which = 0; which < (alias ? 1 : 2); ++which) {
+                    uint64_t *fullb = which == 0 ? kfull : vfull;
+                    uint64_t *emptyb = which == 0 ? kempty : vempty;
+                    if (sidx >= NS && !mbar_wait(&emptyb[st], prev, p.err)) {
+                        ok = false;
+                        break;
+                    }
+                    issued[which] = sidx + 1;
+                    if (lane != 0)
+                        continue;
+                    mbar_arrive_expect_tx(&fullb[st], tx);
+                    uint8_t *dst = ring + st * SB + which * KS;
+                    const CUtensorMap *map = which == 0 ? &tmk : &tmv;
+                    const float *scales = which == 0 ? p.k_scale : p.v_scale;
 #pragma unroll
-                    for (int ch = 0; ch < C::NCH; ++ch)
-                        tma_load_3d(vt + ch * C::P * C::ROWB, &tmv, ch * C::CHE, g, row0, &full[st],
-                                    pol);
+                    for (int t = 0; t < BPS; ++t) {
+                        if (phys[t] < 0)
+                            continue;
+                        const int row0 = phys[t] * C::P;
+#pragma unroll
+                        for (int ch = 0; ch < C::NCH; ++ch)
+                            tma_load_3d(dst + t * C::TILE + ch * C::P * C::ROWB, map, ch * C::CHE,
+                                        g, row0, &fullb[st], pol);
+                        if (per_token)
+                            bulk_load(dst + BPS * C::TILE + t * 64, scales + row0, 64, &fullb[st]);
+                    }
                 }
-                if (per_token) {
-                    uint8_t *sc = kt + (p.alias ? 1 : 2) * C::TILE;
-                    bulk_load(sc, p.k_scale + row0, 64, &full[st]);
-                    if (!p.alias)
-                        bulk_load(sc + 64, p.v_scale + row0, 64, &full[st]);
-                }
+                ok = __all_sync(FULL_MASK, ok);
             }
             // Drain: do not let the CTA retire with copies in flight.
-            for (int i = max(0, issued - NS); i < issued; ++i)
-                mbar_wait(&full[i % NS], (i / NS) & 1, p.err, 100000000ull);
+            if (lane == 0)
+                for (int which = 0; which < 2; ++which)
+                    for (int i = max(0, issued[which] - NS); i < issued[which]; ++i)
+                        mbar_wait(&(which == 0 ? kfull : vfull)[i % NS], (i / NS) & 1, p.err,
+                                  100000000ull);
         }
         return;
     }
 
     // ---------------------------------------------------------- consumers
-    constexpr int DPL = C::DPL, NV = C::NV, R = C::R;
+    // Every consumer warp works on every stage: warp w takes the stage's
+    // keys [w*KPW, (w+1)*KPW), so a stage is released after a quarter of
+    // its work and the rest of the ring stays in flight.
+    constexpr int NP = C::NP, NV = C::NV, KPW = C::KPW, DUP = C::DUP;
     const int G = p.group;
-    const int lane_elem = lane * DPL;
+    const int lane_elem = lane * C::DPL;
     const int lane_off = (lane_elem / C::CHE) * C::P * C::ROWB + (lane_elem % C::CHE) * C::ES;
+    const int k0w = warp * KPW;  // this warp's first key within a stage
 
-    float qf[GT][DPL];
+    float2 qf[GT][NP];
     {
         float qmul = p.qk_scale_log2;
         if (per_head)
@@ -225,141 +347,157 @@ __global__ void __launch_bounds__(THREADS) decode_kernel(const DecodeParams p,
         for (int h = 0; h < GT; ++h) {
             const int hl = chunk * GT + h;
             if (hl < G) {
-                const uint16_t *qr =
-                    p.q + (static_cast<size_t>(b) * p.num_q_heads + g * G + hl) * D + lane_elem;
+                const uint8_t *qr = reinterpret_cast<const uint8_t *>(
+                    p.q + (static_cast<size_t>(b) * p.num_q_heads + g * G + hl) * D + lane_elem);
+                float2 t[NP];
+                load_pairs<NP, false>(qr, t);
 #pragma unroll
-                for (int i = 0; i < DPL; ++i)
-                    qf[h][i] = __uint_as_float(static_cast<uint32_t>(qr[i]) << 16) * qmul;
+                for (int i = 0; i < NP; ++i)
+                    qf[h][i] = make_float2(t[i].x * qmul, t[i].y * qmul);
             } else {
 #pragma unroll
-                for (int i = 0; i < DPL; ++i)
-                    qf[h][i] = 0.f;
+                for (int i = 0; i < NP; ++i)
+                    qf[h][i] = make_float2(0.f, 0.f);
             }
         }
     }
 
-    float o[GT][DPL];
+    float2 o[GT][NP];
     float m[GT];
 #pragma unroll
     for (int h = 0; h < GT; ++h) {
         m[h] = -INFINITY;
 #pragma unroll
-        for (int i = 0; i < DPL; ++i)
-            o[h][i] = 0.f;
+        for (int i = 0; i < NP; ++i)
+            o[h][i] = make_float2(0.f, 0.f);
     }
     float l_lane = 0.f;
-    const int my_idx = (NV == 32) ? lane : (lane >> 1);
-    const int my_h = my_idx / R, my_r = my_idx % R;
+    const int my_idx = lane / DUP;          // value index this lane holds
+    const int my_h = my_idx / KPW, my_r = my_idx % KPW;
+    const bool l_owner = (lane % DUP) == 0;  // one lane per value adds to l
 
-    for (int i = warp; i < n; i += NC) {
-        const int st = i % NS;
-        if (!mbar_wait(&full[st], (i / NS) & 1, p.err))
+    TableCursor tc;
+    tc.init(bt_row + ub0, n, lane);
+    for (int sidx = 0; sidx < nst; ++sidx) {
+        const int st = sidx % NS;
+        const uint32_t par = (sidx / NS) & 1;
+        uint32_t vmask = 0;  // blocks of the stage that hold data
+#pragma unroll
+        for (int t = 0; t < BPS; ++t) {
+            const int i = sidx * BPS + t;
+            const int phys = i < n ? tc.get(i, lane) : -1;
+            if (static_cast<unsigned>(phys) < static_cast<unsigned>(p.num_blocks))
+                vmask |= 1u << t;
+        }
+        if (!__all_sync(FULL_MASK, mbar_wait(&kfull[st], par, p.err)))
             break;
-        const int phys = bt_row[ub0 + i];
-        if (static_cast<unsigned>(phys) < static_cast<unsigned>(p.num_blocks)) {
-            const uint8_t *kt = ring + st * SB;
-            const uint8_t *vt = p.alias ? kt : kt + C::TILE;
-            const float *ksc = reinterpret_cast<const float *>(kt + (p.alias ? 1 : 2) * C::TILE);
-            const float *vsc = p.alias ? ksc : ksc + 16;
-            const int j0 = (ub0 + i) * C::P;
-            const bool all_in = j0 >= kr.lo && j0 + C::P - 1 <= kr.pos;
+        const uint8_t *kt = ring + st * SB;
+        const uint8_t *vt = alias ? kt : kt + KS;
+        const float *ksc = reinterpret_cast<const float *>(kt + BPS * C::TILE);
+        const float *vsc = reinterpret_cast<const float *>(vt + BPS * C::TILE);
+        const int jst = (ub0 + sidx * BPS) * C::P;  // key index of the stage's first row
+        const int jw = jst + k0w;
+        // all of this warp's keys hold data and lie in [lo, pos]
+        bool all_in = jw >= kr.lo && jw + KPW - 1 <= kr.pos;
 #pragma unroll
-            for (int grp = 0; grp < C::GROUPS; ++grp) {
-                const int r0 = grp * R;
-                float acc[NV];
+        for (int t = 0; t < BPS; ++t)
+            if (t * C::P < k0w + KPW && (t + 1) * C::P > k0w && !(vmask >> t & 1u))
+                all_in = false;
+        // ---- scores of this warp's KPW keys for the GT heads
+        float acc[NV];
 #pragma unroll
-                for (int r = 0; r < R; ++r) {
-                    float kf[DPL];
-                    load_row_chunk<DPL, INT8>(kt + lane_off + (r0 + r) * C::ROWB, kf);
+        for (int r = 0; r < KPW; ++r) {
+            const int k = k0w + r;
+            float2 kf[NP];
+            load_pairs<NP, INT8>(kt + (k / C::P) * C::TILE + lane_off + (k % C::P) * C::ROWB, kf);
 #pragma unroll
-                    for (int h = 0; h < GT; ++h) {
-                        float a = 0.f;
+            for (int h = 0; h < GT; ++h) {
+                float2 a = __fmul2_rn(qf[h][0], kf[0]);
 #pragma unroll
-                        for (int e = 0; e < DPL; ++e)
-                            a = fmaf(qf[h][e], kf[e], a);
-                        acc[h * R + r] = a;
-                    }
-                }
-                float sc = reduce_scatter<NV>(acc, lane);
-                const int jm = j0 + r0 + my_r;
-                const bool ok = all_in || (jm >= kr.lo && jm <= kr.pos);
-                if (per_token)
-                    sc *= ksc[r0 + my_r];
-                sc = ok ? sc : -INFINITY;
-                // max over the R keys of this lane's head
-                float mx = sc;
-                if constexpr (NV == 32) {
+                for (int e = 1; e < NP; ++e)
+                    a = __ffma2_rn(qf[h][e], kf[e], a);
+                acc[h * KPW + r] = a.x + a.y;
+            }
+        }
+        float s = reduce_scatter<NV, C::LOGNV>(acc, lane);
+        const int km = k0w + my_r;
+        const int jm = jst + km;
+        const bool ok = (vmask >> (km / C::P) & 1u) && jm >= kr.lo && jm <= kr.pos;
+        if (per_token)
+            s *= ksc[km];
+        s = ok ? s : -INFINITY;
+        if (!alias) {
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(&kempty[st]);
+        }
+        // ---- online softmax over the KPW keys
+        float mx = s;
 #pragma unroll
-                    for (int off = 1; off < R; off <<= 1)
-                        mx = fmaxf(mx, __shfl_xor_sync(FULL_MASK, mx, off));
-                } else {
+        for (int off = DUP; off < 32 / GT; off <<= 1)
+            mx = fmaxf(mx, __shfl_xor_sync(FULL_MASK, mx, off));
+        float alpha[GT];
+        float m_mine = 0.f, a_mine = 1.f;
 #pragma unroll
-                    for (int off = 2; off < 32; off <<= 1)
-                        mx = fmaxf(mx, __shfl_xor_sync(FULL_MASK, mx, off));
-                }
-                float alpha[GT];
-                float m_mine = 0.f, a_mine = 1.f;
+        for (int h = 0; h < GT; ++h) {
+            const float tm = __shfl_sync(FULL_MASK, mx, h * KPW * DUP);
+            const float mn = fmaxf(m[h], tm);
+            alpha[h] = (mn == -INFINITY) ? 1.f : fast_exp2(m[h] - mn);
+            m[h] = mn;
+            if (h == my_h) {
+                m_mine = mn;
+                a_mine = alpha[h];
+            }
+        }
+        const float pr = ok ? fast_exp2(s - m_mine) : 0.f;
+        l_lane = l_lane * a_mine + (l_owner ? pr : 0.f);
 #pragma unroll
-                for (int h = 0; h < GT; ++h) {
-                    const float tm = __shfl_sync(FULL_MASK, mx, lane_of<NV, R>(h, 0));
-                    const float mn = fmaxf(m[h], tm);
-                    alpha[h] = (mn == -INFINITY) ? 1.f : fast_exp2(m[h] - mn);
-                    m[h] = mn;
-                    if (h == my_h) {
-                        m_mine = mn;
-                        a_mine = alpha[h];
-                    }
-                }
-                const float pr = ok ? fast_exp2(sc - m_mine) : 0.f;
-                l_lane = l_lane * a_mine + ((NV == 16 && (lane & 1)) ? 0.f : pr);
+        for (int h = 0; h < GT; ++h) {
+            const float2 a2 = make_float2(alpha[h], alpha[h]);
 #pragma unroll
-                for (int h = 0; h < GT; ++h)
+            for (int e = 0; e < NP; ++e)
+                o[h][e] = __fmul2_rn(o[h][e], a2);
+        }
+        if (!alias && !__all_sync(FULL_MASK, mbar_wait(&vfull[st], par, p.err)))
+            break;
+        float pv = pr;
+        if (per_token)
+            pv = ok ? pr * vsc[km] : 0.f;
+        // ---- P.V over the KPW keys
 #pragma unroll
-                    for (int e = 0; e < DPL; ++e)
-                        o[h][e] *= alpha[h];
-                float pv = pr;
-                if (per_token)
-                    pv = ok ? pr * vsc[r0 + my_r] : 0.f;
+        for (int r = 0; r < KPW; ++r) {
+            const int k = k0w + r;
+            const int j = jst + k;
+            if (!all_in && (!(vmask >> (k / C::P) & 1u) || j < kr.lo || j > kr.pos))
+                continue;  // warp-uniform: masked key, data may be stale
+            float2 vf[NP];
+            load_pairs<NP, INT8>(vt + (k / C::P) * C::TILE + lane_off + (k % C::P) * C::ROWB, vf);
 #pragma unroll
-                for (int r = 0; r < R; ++r) {
-                    const int j = j0 + r0 + r;
-                    if (!all_in && (j < kr.lo || j > kr.pos))
-                        continue;  // warp-uniform: masked key, data may be stale
-                    float vf[DPL];
-                    load_row_chunk<DPL, INT8>(vt + lane_off + (r0 + r) * C::ROWB, vf);
+            for (int h = 0; h < GT; ++h) {
+                const float w = __shfl_sync(FULL_MASK, pv, (h * KPW + r) * DUP);
+                const float2 w2 = make_float2(w, w);
 #pragma unroll
-                    for (int h = 0; h < GT; ++h) {
-                        const float w = __shfl_sync(FULL_MASK, pv, lane_of<NV, R>(h, r));
-#pragma unroll
-                        for (int e = 0; e < DPL; ++e)
-                            o[h][e] = fmaf(w, vf[e], o[h][e]);
-                    }
-                }
+                for (int e = 0; e < NP; ++e)
+                    o[h][e] = __ffma2_rn(w2, vf[e], o[h][e]);
             }
         }
         __syncwarp();
         if (lane == 0)
-            mbar_arrive(&empty[st]);
+            mbar_arrive(alias ? &kempty[st] : &vempty[st]);
     }
 
-    // per-head l: sum the lanes of each head
+    // per-head l: sum the owner lanes of each head's lane group
     {
         float ls = l_lane;
-        if constexpr (NV == 32) {
 #pragma unroll
-            for (int off = 1; off < R; off <<= 1)
-                ls += __shfl_xor_sync(FULL_MASK, ls, off);
-        } else {
-#pragma unroll
-            for (int off = 1; off < 32; off <<= 1)
-                ls += __shfl_xor_sync(FULL_MASK, ls, off);
-        }
+        for (int off = 1; off < 32 / GT; off <<= 1)
+            ls += __shfl_xor_sync(FULL_MASK, ls, off);
         l_lane = ls;
     }
     float lh[GT];
 #pragma unroll
     for (int h = 0; h < GT; ++h)
-        lh[h] = __shfl_sync(FULL_MASK, l_lane, lane_of<NV, R>(h, 0));
+        lh[h] = __shfl_sync(FULL_MASK, l_lane, h * (32 / GT));
 
     // ------------------------------------------- merge the warps' states
     asm volatile("bar.sync 1, %0;" ::"r"(NC * 32) : "memory");  // ring no longer read
@@ -380,8 +518,8 @@ __global__ void __launch_bounds__(THREADS) decode_kernel(const DecodeParams p,
 #pragma unroll
     for (int h = 0; h < GT; ++h)
 #pragma unroll
-        for (int e = 0; e < DPL; ++e)
-            mrg_o[(warp * GT + h) * D + lane_elem + e] = o[h][e];
+        for (int e = 0; e < NP; ++e)
+            *reinterpret_cast<float2 *>(&mrg_o[(warp * GT + h) * D + lane_elem + 2 * e]) = o[h][e];
     asm volatile("bar.sync 1, %0;" ::"r"(NC * 32) : "memory");
 
     const bool single = kr.nsplit == 1;
@@ -473,7 +611,9 @@ size_t decode_smem_bytes(int head_dim, int int8, int alias, int per_token, int g
                          int num_stages)
 {
     const int tile = kBlock * head_dim * (int8 ? 1 : 2);
-    const size_t ring = static_cast<size_t>(num_stages) * stage_bytes(tile, alias, per_token);
+    const int bps = blocks_per_stage(tile, group_tile);
+    const size_t ring = static_cast<size_t>(num_stages) * (alias ? 1 : 2) *
+                        slot_bytes(tile, bps, per_token);
     const size_t merge = (2 * NC * group_tile + static_cast<size_t>(NC) * group_tile * head_dim) *
                          sizeof(float);
     return BAR_BYTES + (ring > merge ? ring : merge);
@@ -486,6 +626,8 @@ static cudaError_t launch_one(const DecodeParams &p, const CUtensorMap &tmk,
     const size_t smem =
         decode_smem_bytes(D, INT8, p.alias, INT8 && p.scale_mode == PKV_SCALE_PER_TOKEN, GT,
                           p.num_stages);
+    static_assert(Cfg<D, GT, INT8>::BPS == blocks_per_stage(Cfg<D, GT, INT8>::TILE, GT),
+                  "host and device stage geometry");
     auto kern = decode_kernel<D, GT, INT8>;
     static int configured = 0;  // largest dynamic smem set so far (per process)
     if (static_cast<int>(smem) > configured) {
