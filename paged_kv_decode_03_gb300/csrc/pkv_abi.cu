@@ -100,6 +100,48 @@ static int encode_pool_map(CUtensorMap *map, void *base, const pkv_pool &pool)
     return PKV_OK;
 }
 
+// Tensor map for the tensor-core kernel: box = {64 dims, 1 head,
+// block_size rows} with the 128-byte swizzle that tcgen05.mma expects of a
+// K-major (and, read transposed, MN-major) bf16 operand.
+static int encode_pool_map_tc(CUtensorMap *map, void *base, const pkv_pool &pool)
+{
+    auto fn = encode_fn();
+    if (!fn)
+        return fail(PKV_E_DRIVER, "cuTensorMapEncodeTiled is unavailable");
+    cuuint64_t dims[3] = {(cuuint64_t)pool.head_dim, (cuuint64_t)pool.num_kv_heads,
+                          (cuuint64_t)pool.num_blocks * (cuuint64_t)pool.block_size};
+    cuuint64_t strides[2] = {(cuuint64_t)pool.head_dim * 2,
+                             (cuuint64_t)pool.num_kv_heads * pool.head_dim * 2};
+    cuuint32_t box[3] = {64u, 1u, (cuuint32_t)pool.block_size};
+    cuuint32_t estr[3] = {1u, 1u, 1u};
+    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, base, dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS)
+        return fail(PKV_E_DRIVER, "cuTensorMapEncodeTiled (swizzled) failed (%d)", (int)r);
+    return PKV_OK;
+}
+
+// Whether a decode runs on the tensor-core kernel: bf16 pool, head_dim 128
+// or 256, and 8 to 16 query heads per KV head.  Below 8 heads the CUDA-core
+// kernel keeps up with HBM and, with several CTAs per SM, measures faster.
+// PKV_DISABLE_TC=1 forces the CUDA-core kernel and PKV_FORCE_TC=1 the
+// tensor-core kernel for any group <= 16 (both read at every call).
+static bool use_tc(const pkv_pool *pool, int group)
+{
+    if (pool->dtype != PKV_BF16 || (pool->head_dim != 128 && pool->head_dim != 256))
+        return false;
+    if (decode_tc_group_pad(group) == 0)
+        return false;
+    const char *e = getenv("PKV_DISABLE_TC");
+    if (e && e[0] == '1')
+        return false;
+    const char *f = getenv("PKV_FORCE_TC");
+    if (f && f[0] == '1')
+        return true;
+    return group >= 8;
+}
+
 // ---------------------------------------------------------- validation
 static int check_pool(const pkv_pool *pool)
 {
@@ -323,15 +365,17 @@ static int run_decode(const void *q, const pkv_pool *pool, const int32_t *block_
                       int32_t num_splits, void *out, int32_t out_dtype, cudaStream_t s)
 {
     const bool alias = pool->v == nullptr || pool->v == pool->k;
+    const int group = num_q_heads / pool->num_kv_heads;
+    const bool tc = use_tc(pool, group);
+    auto encode = tc ? encode_pool_map_tc : encode_pool_map;
     CUtensorMap tmk, tmv;
-    if (int rc = encode_pool_map(&tmk, pool->k, *pool))
+    if (int rc = encode(&tmk, pool->k, *pool))
         return rc;
     if (alias)
         tmv = tmk;
-    else if (int rc = encode_pool_map(&tmv, pool->v, *pool))
+    else if (int rc = encode(&tmv, pool->v, *pool))
         return rc;
-    const int group = num_q_heads / pool->num_kv_heads;
-    const int gt = decode_group_tile(group);
+    const int gt = tc ? group : decode_group_tile(group);
     DecodeParams p{};
     p.q = static_cast<const uint16_t *>(q);
     p.block_table = block_table;
@@ -347,7 +391,7 @@ static int run_decode(const void *q, const pkv_pool *pool, const int32_t *block_
     p.num_q_heads = num_q_heads;
     p.num_kv_heads = pool->num_kv_heads;
     p.group = group;
-    p.head_chunks = (group + gt - 1) / gt;
+    p.head_chunks = tc ? 1 : (group + gt - 1) / gt;
     p.num_blocks = pool->num_blocks;
     p.window = window;
     p.max_seq_len = max_seq_len;
@@ -374,6 +418,17 @@ static int run_decode(const void *q, const pkv_pool *pool, const int32_t *block_
         return fail(PKV_E_DRIVER, "cannot resolve the device error word");
     if ((int64_t)p.num_kv_heads * p.head_chunks > 65535)
         return fail(PKV_E_UNSUPPORTED, "too many kv heads");
+    if (tc) {
+        // ring of 32 KB units: 6 by default (one CTA per SM), PKV_STAGES overrides
+        int nu = stages_override() ? stages_override() : 6;
+        while (nu > 2 && decode_tc_smem_bytes(nu) > 227u * 1024u)
+            --nu;
+        p.num_stages = nu < 6 ? nu : 6;  // one producer warp per ring unit
+        cudaError_t e = launch_decode_tc(p, tmk, tmv, pool->head_dim, s);
+        if (e != cudaSuccess)
+            return cuda_fail(e, "tensor-core decode launch");
+        return PKV_OK;
+    }
     cudaError_t e = launch_decode(p, tmk, tmv, pool->head_dim, pool->dtype == PKV_INT8, gt, s);
     if (e != cudaSuccess)
         return cuda_fail(e, "decode launch");

@@ -172,31 +172,6 @@ __device__ __forceinline__ void load_pairs(const uint8_t *p, float2 (&f)[NP])
     }
 }
 
-// Block-table entries of a unit, read 32 at a time by a whole warp: lane j
-// holds entry base + j of the current chunk, the next chunk is fetched half
-// a chunk ahead, and entry i is shuffled out, so no iteration waits on a
-// global load.
-struct TableCursor {
-    const int32_t *row;
-    int n, cur, nxt;
-    __device__ __forceinline__ void init(const int32_t *r, int count, int lane)
-    {
-        row = r;
-        n = count;
-        cur = lane < n ? __ldg(row + lane) : -1;
-        nxt = 32 + lane < n ? __ldg(row + 32 + lane) : -1;
-    }
-    // entry i (all lanes call with the same i, in increasing order)
-    __device__ __forceinline__ int get(int i, int lane)
-    {
-        if ((i & 31) == 0 && i > 0) {
-            cur = nxt;
-            nxt = i + 32 + lane < n ? __ldg(row + i + 32 + lane) : -1;
-        }
-        return __shfl_sync(FULL_MASK, cur, i & 31);
-    }
-};
-
 template <int D, int GT, bool INT8>
 __global__ void __launch_bounds__(THREADS) decode_kernel(const DecodeParams p,
                                                          const __grid_constant__ CUtensorMap tmk,

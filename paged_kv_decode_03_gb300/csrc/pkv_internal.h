@@ -80,6 +80,13 @@ size_t decode_smem_bytes(int head_dim, int int8, int alias, int per_token, int g
 cudaError_t launch_decode(const DecodeParams &p, const CUtensorMap &tmk, const CUtensorMap &tmv,
                           int head_dim, int int8, int group_tile, cudaStream_t s);
 cudaError_t launch_combine(const CombineParams &p, cudaStream_t s);
+
+// Tensor-core decode kernel (bf16 pools, head_dim 128/256, group <= 16):
+// one CTA per (split, kv head, sequence); num_stages = ring units of 32 KB.
+int decode_tc_group_pad(int group);  // 0 if the group is too large
+size_t decode_tc_smem_bytes(int num_units);
+cudaError_t launch_decode_tc(const DecodeParams &p, const CUtensorMap &tmk,
+                             const CUtensorMap &tmv, int head_dim, cudaStream_t s);
 cudaError_t launch_append(const AppendParams &p, int int8, cudaStream_t s);
 
 }  // namespace pkv

@@ -280,3 +280,53 @@ def test_graph_capture_replays_the_step():
     oracle.append(w.new_k, w.new_v, w.new_slots, op)
     ref = _util.oracle_decode(w, op)
     assert _gpu.max_abs_err(_gpu.out_to_f64(out), ref) <= BF16_TOL
+
+
+@pytest.mark.parametrize("case", ["c2", "c3", "edge"])
+def test_cuda_core_kernel_on_bf16_shapes(case, monkeypatch):
+    """bf16 pools with head_dim 128/256 normally run on the tensor-core
+    kernel; PKV_DISABLE_TC=1 selects the CUDA-core kernel, which must match
+    the oracle on the same shapes."""
+    monkeypatch.setenv("PKV_DISABLE_TC", "1")
+    if case == "c2":
+        spec = synth.shrink(synth.C2, batch=6, lens=("uniform", 1, 2500))
+    elif case == "c3":
+        spec = synth.shrink(synth.C3, batch=3, lens=("uniform", 1, 4000))
+    else:
+        spec = synth.Spec("edge_cc", batch=9, num_q_heads=6, num_kv_heads=2, head_dim=128,
+                          lens=("fixed", (0, 1, 15, 16, 17, 33, 64, 100, 257)), window=40, seed=3)
+    _run_case(spec, splits=(0, 32, pkv.SPLIT_AUTO))
+
+
+@pytest.mark.parametrize("case", ["c2", "edge128", "edge256"])
+def test_tensor_core_kernel_on_small_groups(case, monkeypatch):
+    """GQA groups below 8 normally run on the CUDA-core kernel;
+    PKV_FORCE_TC=1 runs them on the tensor-core kernel, which must match the
+    oracle too (padded query heads, masked edges, splits)."""
+    monkeypatch.setenv("PKV_FORCE_TC", "1")
+    if case == "c2":
+        spec = synth.shrink(synth.C2, batch=6, lens=("uniform", 1, 2500))
+    else:
+        D = 128 if case == "edge128" else 256
+        spec = synth.Spec(f"edge_tc_{D}", batch=9, num_q_heads=6, num_kv_heads=2, head_dim=D,
+                          lens=("fixed", (0, 1, 15, 16, 17, 33, 64, 100, 257)), window=40, seed=4)
+    _run_case(spec, splits=(0, 32, 128, pkv.SPLIT_AUTO))
+
+
+def test_tensor_core_and_cuda_core_kernels_agree():
+    """Both kernels on one workload, fp32 output: they reduce in different
+    orders, so they agree to the oracle tolerance, not bit for bit."""
+    import os
+    spec = synth.shrink(synth.C3, batch=4, lens=("uniform", 100, 3000))
+    w = synth.make_workload(spec)
+    gp = _gpu.device_pool(w)
+    _gpu.append_all(w, gp)
+    step = _gpu.DeviceStep(w)
+    a = _gpu.out_to_f64(step.decode(gp, split_tokens=0, out_f32=True))  # tensor cores (G=16)
+    os.environ["PKV_DISABLE_TC"] = "1"
+    try:
+        c = _gpu.out_to_f64(step.decode(gp, split_tokens=0, out_f32=True))
+    finally:
+        del os.environ["PKV_DISABLE_TC"]
+    torch.cuda.synchronize()
+    assert _gpu.max_row_rel_err(a, c) <= 2 * F32_REL_TOL
