@@ -131,9 +131,10 @@ PKV_API int paged_kv_append(const void *k, const void *v, const int64_t *slot_ma
 
 /*
  * paged_decode_split_tokens -- the split length paged_decode_attention uses
- * for split_tokens (resolves PKV_SPLIT_AUTO from the batch shape and the
- * current device's SM count).  Returns 0 for a single pass, a positive
- * multiple of block_size, or a negative PKV_E_* code.
+ * for split_tokens.  PKV_SPLIT_AUTO resolves to 4096 keys for GQA groups of
+ * 8 or more and 2048 otherwise, or to 0 (a single pass) when the longest key
+ * range (max_seq_len, window) fits in one split.  Returns 0 for a single
+ * pass, a positive multiple of block_size, or a negative PKV_E_* code.
  */
 PKV_API int32_t paged_decode_split_tokens(int32_t batch, int32_t num_q_heads,
                                           int32_t num_kv_heads, int32_t block_size,

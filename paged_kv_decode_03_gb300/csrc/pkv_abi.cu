@@ -179,16 +179,6 @@ static int check_pool(const pkv_pool *pool)
     return PKV_OK;
 }
 
-static int sm_count()
-{
-    int dev = 0, n = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess)
-        return -1;
-    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-        return -1;
-    return n;
-}
-
 // Ring depth override for tuning sweeps (PKV_STAGES); 0 = automatic.
 static int stages_override()
 {
@@ -296,24 +286,18 @@ PKV_API int32_t paged_decode_split_tokens(int32_t batch, int32_t num_q_heads, in
     }
     if (split_tokens != PKV_SPLIT_AUTO)
         return fail(PKV_E_ARG, "split_tokens %d", split_tokens);
-    // Auto: enough CTAs for about four per SM, splits of at least 8 blocks.
-    const int sms = sm_count();
-    if (sms <= 0)
-        return fail(PKV_E_DRIVER, "cannot query the SM count");
+    // Auto: split each sequence's key range into pieces of a fixed length --
+    // 4096 keys for GQA groups of 8 or more (tensor-core kernel, one CTA per
+    // SM), 2048 otherwise -- and run a single pass (no combine) when the
+    // longest range fits in one piece.  Sequences shorter than a piece take
+    // one CTA whatever their neighbours' lengths, which keeps ragged batches
+    // balanced without knowing the lengths on the host.
     const int group = num_q_heads / num_kv_heads;
-    const int gt = decode_group_tile(group);
-    const int64_t units = (int64_t)batch * num_kv_heads * ((group + gt - 1) / gt);
+    const int64_t piece = group >= 8 ? 4096 : 2048;
     const int64_t nblk = max_range_blocks(block_size, max_seq_len, window);
-    if (units <= 0 || nblk <= 8)
+    if (nblk * block_size <= piece)
         return 0;
-    int64_t want = (4LL * sms + units - 1) / units;
-    const int64_t cap = nblk / 8;
-    if (want > cap)
-        want = cap;
-    if (want <= 1)
-        return 0;
-    const int64_t sb = (nblk + want - 1) / want;
-    return static_cast<int32_t>(sb * block_size);
+    return static_cast<int32_t>(piece);
 }
 
 PKV_API size_t paged_decode_workspace_bytes(int32_t batch, int32_t num_q_heads,
