@@ -18,14 +18,18 @@
 //     its GQA chunk from it.
 //   * Warp specialisation: one producer thread issues TMA tile loads
 //     (cp.async.bulk.tensor, 16 rows x head_dim of one kv head per paged
-//     block) into an NS-stage shared-memory ring guarded by mbarriers; four
-//     consumer warps each own every fourth stage and run an independent
-//     online softmax over their blocks; the four states merge at the end.
-//   * A consumer warp spreads head_dim over its 32 lanes (16-byte shared
-//     loads for bf16 D=256), forms the partial dot products of R keys x GT
-//     heads (R*GT = 32 or 16) and finishes them with one butterfly
-//     reduce-scatter (31 shuffles per 32 dot products), after which lane
-//     (h, r) owns score (key r, head h).
+//     block) into an NS-stage shared-memory ring guarded by mbarriers, with
+//     separate K and V slots; all four consumer warps work on every stage
+//     (a quarter of its keys each) and keep independent online-softmax
+//     states that merge at the end.
+//   * A lane owns one 16-byte chunk of a key row (8 bf16 or 16 int8
+//     values), so head_dim spans LPK = head_dim*bytes/16 lanes and a warp
+//     reads 32/LPK keys at once with 16-byte shared loads.  The partial dot
+//     products of a lane's keys x GT heads finish with one butterfly
+//     reduce-scatter inside its LPK-lane group; P.V accumulates per lane and
+//     the key groups are summed once at the end.
+//   * The running max is warp-uniform, so o and l are rescaled only in
+//     stages where a max grows.
 //   * Keys outside [lo, pos] in the first/last block are masked with a
 //     select (never arithmetic), so stale or NaN slots contribute nothing.
 #include <cuda_bf16.h>
@@ -71,8 +75,11 @@ struct Cfg {
     static constexpr int NCH = D / CHE;                         // boxes per tile
     static constexpr int ROWB = CHE * ES;                       // bytes of one box row
     static constexpr int TILE = P * D * ES;                     // one kv head x one block
-    static constexpr int DPL = D / 32;                          // elements per lane
-    static constexpr int NP = DPL / 2;                          // element pairs per lane
+    // A lane owns one 16-byte chunk of a key row: EPL elements, NPR pairs.
+    static constexpr int EPL = 16 / ES;
+    static constexpr int NPR = EPL / 2;
+    static constexpr int LPK = D / EPL;                         // lanes per key row
+    static constexpr int KG = 32 / LPK;                         // keys a warp reads at once
     // Paged blocks per ring stage: about 8 KB of K per stage, and at most
     // 32 / GT keys per consumer warp so one reduce-scatter covers them.
     static constexpr int BPS_MEM = (8192 / TILE) < 1 ? 1 : (8192 / TILE);
@@ -80,11 +87,12 @@ struct Cfg {
     static constexpr int BPS = BPS_MEM < BPS_MAX ? BPS_MEM : BPS_MAX;
     static constexpr int KEYS = P * BPS;                        // keys per stage
     static constexpr int KPW = KEYS / NC;                       // keys per warp per stage
-    static constexpr int NV = KPW * GT;                         // dot products per reduction
-    static constexpr int LOGNV = NV == 4 ? 2 : NV == 8 ? 3 : NV == 16 ? 4 : 5;
-    static constexpr int DUP = 32 / NV;                         // lanes holding each sum
-    static_assert(D % 32 == 0 && DPL >= 2 && DPL <= 8, "head_dim");
-    static_assert(NV >= 4 && NV <= 32, "reduction width");
+    static constexpr int KPL = KPW / KG;                        // keys per lane per stage
+    static constexpr int NV = KPL * GT;                         // dot products per lane
+    static constexpr int DUP = LPK / NV;                        // lanes holding each sum
+    static_assert(D % EPL == 0 && LPK >= 4 && LPK <= 32, "head_dim");
+    static_assert(KPL >= 1 && KPW % KG == 0, "keys per lane");
+    static_assert(NV >= 1 && NV <= LPK && LPK % NV == 0, "reduction width");
     static_assert(KPW <= P || KPW % P == 0, "warp keys within or across whole blocks");
 };
 
@@ -101,16 +109,17 @@ __host__ __device__ constexpr int blocks_per_stage(int tile, int gt)
     return (8192 / tile) < 1 ? 1 : ((8192 / tile) < 8 / gt ? (8192 / tile) : 8 / gt);
 }
 
-// Butterfly reduce-scatter of NV per-lane partial sums (NV = 4..32): after
-// log2(NV) halving steps lane l holds value index l >> (5 - log2 NV) summed
-// over the lanes that share its top bits; the remaining xor steps complete
-// the sum, so every lane of a DUP = 32/NV lane group holds the full sum.
-// Costs NV - 1 + 5 - log2(NV) shuffles for NV dot products.
-template <int NV, int LOGNV>
+// Butterfly reduce-scatter of NV per-lane partial sums within aligned groups
+// of W lanes (NV <= W, both powers of two): after log2(NV) halving steps lane
+// l holds value index (l % W) / (W / NV) summed over the lanes of its group
+// that share those bits; the remaining xor steps complete the sum, so the
+// W / NV lanes of each value hold its full sum.  NV - 1 + log2(W / NV)
+// shuffles for NV dot products.
+template <int NV, int W>
 __device__ __forceinline__ float reduce_scatter(float (&v)[NV], int lane)
 {
 #pragma unroll
-    for (int half = NV / 2, off = 16; half >= 1; half >>= 1, off >>= 1) {
+    for (int half = NV / 2, off = W / 2; half >= 1; half >>= 1, off >>= 1) {
         const bool upper = (lane & off) != 0;
 #pragma unroll
         for (int i = 0; i < half; ++i) {
@@ -120,49 +129,29 @@ __device__ __forceinline__ float reduce_scatter(float (&v)[NV], int lane)
         }
     }
     float r = v[0];
-    if constexpr (LOGNV < 5) {
 #pragma unroll
-        for (int off = 1 << (4 - LOGNV); off >= 1; off >>= 1)
-            r += __shfl_xor_sync(FULL_MASK, r, off);
-    }
+    for (int off = W / NV / 2; off >= 1; off >>= 1)
+        r += __shfl_xor_sync(FULL_MASK, r, off);
     return r;
 }
 
-// Element pairs of one lane's slice of a tile row, as float2 (exact).
-// bf16: the two halves of each 32-bit word.  int8: each byte b is placed in
-// the low mantissa bits of 2^23 (after flipping its sign bit, giving b+128)
-// and 2^23+128 is subtracted, which yields b exactly.
-template <int NP, bool INT8>
-__device__ __forceinline__ void load_pairs(const uint8_t *p, float2 (&f)[NP])
+// Sixteen bytes of a tile row as float2 pairs (exact).  bf16: the two halves
+// of each 32-bit word.  int8: each byte b is placed in the low mantissa bits
+// of 2^23 (after flipping its sign bit, giving b+128) and 2^23+128 is
+// subtracted, which yields b exactly.
+template <bool INT8>
+__device__ __forceinline__ void load_chunk(const uint8_t *p, float2 (&f)[INT8 ? 8 : 4])
 {
+    const uint4 u = *reinterpret_cast<const uint4 *>(p);
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
     if constexpr (!INT8) {
-        uint32_t w[NP];
-        if constexpr (NP == 4) {
-            const uint4 u = *reinterpret_cast<const uint4 *>(p);
-            w[0] = u.x; w[1] = u.y; w[2] = u.z; w[3] = u.w;
-        } else if constexpr (NP == 2) {
-            const uint2 u = *reinterpret_cast<const uint2 *>(p);
-            w[0] = u.x; w[1] = u.y;
-        } else {
-            w[0] = *reinterpret_cast<const uint32_t *>(p);
-        }
 #pragma unroll
-        for (int i = 0; i < NP; ++i)
+        for (int i = 0; i < 4; ++i)
             f[i] = make_float2(bf16lo(w[i]), bf16hi(w[i]));
     } else {
-        constexpr int NW = (NP * 2 + 3) / 4;  // 32-bit words holding 2*NP bytes
-        uint32_t w[NW];
-        if constexpr (NP == 4) {
-            const uint2 u = *reinterpret_cast<const uint2 *>(p);
-            w[0] = u.x; w[1] = u.y;
-        } else if constexpr (NP == 2) {
-            w[0] = *reinterpret_cast<const uint32_t *>(p);
-        } else {
-            w[0] = *reinterpret_cast<const uint16_t *>(p);
-        }
         const float2 bias = make_float2(-8388736.0f, -8388736.0f);  // -(2^23 + 128)
 #pragma unroll
-        for (int i = 0; i < NP; ++i) {
+        for (int i = 0; i < 8; ++i) {
             const uint32_t x = w[i / 2] ^ 0x80808080u;
             const int b0 = (i % 2) * 2;
             const float lo = __uint_as_float(__byte_perm(x, 0x4B000000u, 0x7540 + b0));
@@ -306,14 +295,27 @@ __global__ void __launch_bounds__(THREADS) decode_kernel(const DecodeParams p,
     // ---------------------------------------------------------- consumers
     // Every consumer warp works on every stage: warp w takes the stage's
     // keys [w*KPW, (w+1)*KPW), so a stage is released after a quarter of
-    // its work and the rest of the ring stays in flight.
-    constexpr int NP = C::NP, NV = C::NV, KPW = C::KPW, DUP = C::DUP;
+    // its work and the rest of the ring stays in flight.  Within a warp,
+    // lane (kg, dl) owns the 16-byte chunk dl of a key row and reads keys
+    // kg, kg+KG, kg+2KG, ... of the warp's share: every shared load is 16
+    // bytes, eight consecutive lanes cover 128 consecutive bytes, and the
+    // score reductions stay within the LPK lanes of one key.
+    constexpr int NPR = C::NPR, NV = C::NV, KPW = C::KPW, KPL = C::KPL, KG = C::KG;
+    constexpr int LPK = C::LPK, DUP = C::DUP;
     const int G = p.group;
-    const int lane_elem = lane * C::DPL;
+    const int kg = lane / LPK, dl = lane % LPK;
+    const int lane_elem = dl * C::EPL;
     const int lane_off = (lane_elem / C::CHE) * C::P * C::ROWB + (lane_elem % C::CHE) * C::ES;
-    const int k0w = warp * KPW;  // this warp's first key within a stage
+    const int k0w = warp * KPW;   // this warp's first key within a stage
+    const int kb = k0w + kg;      // this lane's first key within a stage
+    int koff[KPL];                // smem offset of key r of this lane in a slot
+#pragma unroll
+    for (int r = 0; r < KPL; ++r) {
+        const int k = kb + KG * r;
+        koff[r] = (k / C::P) * C::TILE + (k % C::P) * C::ROWB + lane_off;
+    }
 
-    float2 qf[GT][NP];
+    float2 qf[GT][NPR];
     {
         float qmul = p.qk_scale_log2;
         if (per_head)
@@ -324,32 +326,36 @@ __global__ void __launch_bounds__(THREADS) decode_kernel(const DecodeParams p,
             if (hl < G) {
                 const uint8_t *qr = reinterpret_cast<const uint8_t *>(
                     p.q + (static_cast<size_t>(b) * p.num_q_heads + g * G + hl) * D + lane_elem);
-                float2 t[NP];
-                load_pairs<NP, false>(qr, t);
 #pragma unroll
-                for (int i = 0; i < NP; ++i)
-                    qf[h][i] = make_float2(t[i].x * qmul, t[i].y * qmul);
+                for (int c = 0; c < NPR / 4; ++c) {
+                    float2 t[4];
+                    load_chunk<false>(qr + 16 * c, t);
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+                        qf[h][4 * c + i] = make_float2(t[i].x * qmul, t[i].y * qmul);
+                }
             } else {
 #pragma unroll
-                for (int i = 0; i < NP; ++i)
+                for (int i = 0; i < NPR; ++i)
                     qf[h][i] = make_float2(0.f, 0.f);
             }
         }
     }
 
-    float2 o[GT][NP];
+    float2 o[GT][NPR];
     float m[GT];
 #pragma unroll
     for (int h = 0; h < GT; ++h) {
         m[h] = -INFINITY;
 #pragma unroll
-        for (int i = 0; i < NP; ++i)
+        for (int i = 0; i < NPR; ++i)
             o[h][i] = make_float2(0.f, 0.f);
     }
     float l_lane = 0.f;
-    const int my_idx = lane / DUP;          // value index this lane holds
-    const int my_h = my_idx / KPW, my_r = my_idx % KPW;
-    const bool l_owner = (lane % DUP) == 0;  // one lane per value adds to l
+    const int my_idx = dl / DUP;            // value index this lane holds
+    const int my_h = my_idx / KPL, my_r = my_idx % KPL;
+    const int km = kb + KG * my_r;          // its key within a stage
+    const bool l_owner = (dl % DUP) == 0;   // one lane per value adds to l
 
     TableCursor tc;
     tc.init(bt_row + ub0, n, lane);
@@ -378,24 +384,22 @@ __global__ void __launch_bounds__(THREADS) decode_kernel(const DecodeParams p,
         for (int t = 0; t < BPS; ++t)
             if (t * C::P < k0w + KPW && (t + 1) * C::P > k0w && !(vmask >> t & 1u))
                 all_in = false;
-        // ---- scores of this warp's KPW keys for the GT heads
+        // ---- scores of this lane's KPL keys for the GT heads
         float acc[NV];
 #pragma unroll
-        for (int r = 0; r < KPW; ++r) {
-            const int k = k0w + r;
-            float2 kf[NP];
-            load_pairs<NP, INT8>(kt + (k / C::P) * C::TILE + lane_off + (k % C::P) * C::ROWB, kf);
+        for (int r = 0; r < KPL; ++r) {
+            float2 kf[NPR];
+            load_chunk<INT8>(kt + koff[r], kf);
 #pragma unroll
             for (int h = 0; h < GT; ++h) {
                 float2 a = __fmul2_rn(qf[h][0], kf[0]);
 #pragma unroll
-                for (int e = 1; e < NP; ++e)
+                for (int e = 1; e < NPR; ++e)
                     a = __ffma2_rn(qf[h][e], kf[e], a);
-                acc[h * KPW + r] = a.x + a.y;
+                acc[h * KPL + r] = a.x + a.y;
             }
         }
-        float s = reduce_scatter<NV, C::LOGNV>(acc, lane);
-        const int km = k0w + my_r;
+        float s = reduce_scatter<NV, LPK>(acc, lane);
         const int jm = jst + km;
         const bool ok = (vmask >> (km / C::P) & 1u) && jm >= kr.lo && jm <= kr.pos;
         if (per_token)
@@ -406,53 +410,72 @@ __global__ void __launch_bounds__(THREADS) decode_kernel(const DecodeParams p,
             if (lane == 0)
                 mbar_arrive(&kempty[st]);
         }
-        // ---- online softmax over the KPW keys
+        // ---- online softmax over the warp's KPW keys
         float mx = s;
 #pragma unroll
-        for (int off = DUP; off < 32 / GT; off <<= 1)
+        for (int off = DUP; off < DUP * KPL; off <<= 1)
             mx = fmaxf(mx, __shfl_xor_sync(FULL_MASK, mx, off));
+#pragma unroll
+        for (int off = LPK; off < 32; off <<= 1)
+            mx = fmaxf(mx, __shfl_xor_sync(FULL_MASK, mx, off));
+        // m is warp-uniform (every lane takes it from the same lanes), so the
+        // rescale below is a uniform branch taken only when a max grows.
         float alpha[GT];
+        bool grow = false;
         float m_mine = 0.f, a_mine = 1.f;
 #pragma unroll
         for (int h = 0; h < GT; ++h) {
-            const float tm = __shfl_sync(FULL_MASK, mx, h * KPW * DUP);
+            const float tm = __shfl_sync(FULL_MASK, mx, h * DUP * KPL);
             const float mn = fmaxf(m[h], tm);
-            alpha[h] = (mn == -INFINITY) ? 1.f : fast_exp2(m[h] - mn);
-            m[h] = mn;
+            alpha[h] = 1.f;
+            if (mn > m[h]) {
+                grow = true;
+                alpha[h] = (m[h] == -INFINITY) ? 0.f : fast_exp2(m[h] - mn);
+                m[h] = mn;
+            }
             if (h == my_h) {
-                m_mine = mn;
+                m_mine = m[h];
                 a_mine = alpha[h];
             }
         }
         const float pr = ok ? fast_exp2(s - m_mine) : 0.f;
-        l_lane = l_lane * a_mine + (l_owner ? pr : 0.f);
+        if (grow) {
+            l_lane *= a_mine;
 #pragma unroll
-        for (int h = 0; h < GT; ++h) {
-            const float2 a2 = make_float2(alpha[h], alpha[h]);
+            for (int h = 0; h < GT; ++h) {
+                const float2 a2 = make_float2(alpha[h], alpha[h]);
 #pragma unroll
-            for (int e = 0; e < NP; ++e)
-                o[h][e] = __fmul2_rn(o[h][e], a2);
+                for (int e = 0; e < NPR; ++e)
+                    o[h][e] = __fmul2_rn(o[h][e], a2);
+            }
         }
+        l_lane += l_owner ? pr : 0.f;
         if (!alias && !__all_sync(FULL_MASK, mbar_wait(&vfull[st], par, p.err)))
             break;
         float pv = pr;
         if (per_token)
             pv = ok ? pr * vsc[km] : 0.f;
-        // ---- P.V over the KPW keys
+        // ---- P.V over this lane's KPL keys
 #pragma unroll
-        for (int r = 0; r < KPW; ++r) {
-            const int k = k0w + r;
-            const int j = jst + k;
-            if (!all_in && (!(vmask >> (k / C::P) & 1u) || j < kr.lo || j > kr.pos))
-                continue;  // warp-uniform: masked key, data may be stale
-            float2 vf[NP];
-            load_pairs<NP, INT8>(vt + (k / C::P) * C::TILE + lane_off + (k % C::P) * C::ROWB, vf);
+        for (int r = 0; r < KPL; ++r) {
+            float w[GT];
+#pragma unroll
+            for (int h = 0; h < GT; ++h)
+                w[h] = __shfl_sync(FULL_MASK, pv, kg * LPK + (h * KPL + r) * DUP);
+            if (!all_in) {
+                // masked key: its slot may hold stale data, do not touch it
+                const int k = kb + KG * r;
+                const int j = jst + k;
+                if (!(vmask >> (k / C::P) & 1u) || j < kr.lo || j > kr.pos)
+                    continue;
+            }
+            float2 vf[NPR];
+            load_chunk<INT8>(vt + koff[r], vf);
 #pragma unroll
             for (int h = 0; h < GT; ++h) {
-                const float w = __shfl_sync(FULL_MASK, pv, (h * KPW + r) * DUP);
-                const float2 w2 = make_float2(w, w);
+                const float2 w2 = make_float2(w[h], w[h]);
 #pragma unroll
-                for (int e = 0; e < NP; ++e)
+                for (int e = 0; e < NPR; ++e)
                     o[h][e] = __ffma2_rn(w2, vf[e], o[h][e]);
             }
         }
@@ -461,18 +484,30 @@ __global__ void __launch_bounds__(THREADS) decode_kernel(const DecodeParams p,
             mbar_arrive(alias ? &kempty[st] : &vempty[st]);
     }
 
-    // per-head l: sum the owner lanes of each head's lane group
+    // sum o over the key groups, l over the lanes of each head
+#pragma unroll
+    for (int off = LPK; off < 32; off <<= 1)
+#pragma unroll
+        for (int h = 0; h < GT; ++h)
+#pragma unroll
+            for (int e = 0; e < NPR; ++e) {
+                o[h][e].x += __shfl_xor_sync(FULL_MASK, o[h][e].x, off);
+                o[h][e].y += __shfl_xor_sync(FULL_MASK, o[h][e].y, off);
+            }
     {
         float ls = l_lane;
 #pragma unroll
-        for (int off = 1; off < 32 / GT; off <<= 1)
+        for (int off = 1; off < DUP * KPL; off <<= 1)
+            ls += __shfl_xor_sync(FULL_MASK, ls, off);
+#pragma unroll
+        for (int off = LPK; off < 32; off <<= 1)
             ls += __shfl_xor_sync(FULL_MASK, ls, off);
         l_lane = ls;
     }
     float lh[GT];
 #pragma unroll
     for (int h = 0; h < GT; ++h)
-        lh[h] = __shfl_sync(FULL_MASK, l_lane, h * (32 / GT));
+        lh[h] = __shfl_sync(FULL_MASK, l_lane, h * DUP * KPL);
 
     // ------------------------------------------- merge the warps' states
     asm volatile("bar.sync 1, %0;" ::"r"(NC * 32) : "memory");  // ring no longer read
@@ -490,11 +525,14 @@ __global__ void __launch_bounds__(THREADS) decode_kernel(const DecodeParams p,
         mrg_m[warp * GT + lane] = mm;
         mrg_l[warp * GT + lane] = ll;
     }
+    if (kg == 0) {
 #pragma unroll
-    for (int h = 0; h < GT; ++h)
+        for (int h = 0; h < GT; ++h)
 #pragma unroll
-        for (int e = 0; e < NP; ++e)
-            *reinterpret_cast<float2 *>(&mrg_o[(warp * GT + h) * D + lane_elem + 2 * e]) = o[h][e];
+            for (int e = 0; e < NPR; ++e)
+                *reinterpret_cast<float2 *>(&mrg_o[(warp * GT + h) * D + lane_elem + 2 * e]) =
+                    o[h][e];
+    }
     asm volatile("bar.sync 1, %0;" ::"r"(NC * 32) : "memory");
 
     const bool single = kr.nsplit == 1;
