@@ -383,18 +383,20 @@ static int run_decode(const void *q, const pkv_pool *pool, const int32_t *block_
     p.num_splits = split_tokens > 0 ? num_splits : 1;
     p.alias = alias;
     p.out_f32 = out_dtype == PKV_OUT_F32;
-    // Ring depth: as many stages as fit in about a quarter of an SM's
-    // shared memory (four CTAs per SM: the consumer warps' dependency chains,
-    // not bytes in flight, limit a CTA, so more CTAs beat deeper rings),
-    // 2..16; PKV_STAGES overrides it within the opt-in limit of one CTA.
+    // Ring depth: the most CTAs per SM, then the deepest ring that keeps
+    // them (decode_ring_stages); PKV_STAGES overrides it within the opt-in
+    // shared-memory limit of one CTA.
     {
         const int i8 = pool->dtype == PKV_INT8;
-        const int pt = pool->scale_mode == PKV_SCALE_PER_TOKEN;
-        const size_t budget = stages_override() ? 227u * 1024u : 56u * 1024u;
-        int ns = stages_override() ? stages_override() : 16;
-        while (ns > 2 && decode_smem_bytes(pool->head_dim, i8, alias, pt, gt, ns) > budget)
-            --ns;
-        p.num_stages = ns;
+        const int pt = i8 && pool->scale_mode == PKV_SCALE_PER_TOKEN;
+        int ns = stages_override();
+        if (ns) {
+            while (ns > 2 && decode_smem_bytes(pool->head_dim, i8, alias, pt, gt, ns) > 227u * 1024u)
+                --ns;
+        } else if (!tc) {
+            ns = decode_ring_stages(pool->head_dim, i8, alias, pt, gt);
+        }
+        p.num_stages = ns < 2 ? 2 : ns;
     }
     p.qk_scale_log2 = softmax_scale * LOG2E;
     p.err = error_word_ptr();

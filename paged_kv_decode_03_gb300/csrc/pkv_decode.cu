@@ -23,8 +23,9 @@
 //     (a quarter of its keys each) and keep independent online-softmax
 //     states that merge at the end.
 //   * A lane owns one 16-byte chunk of a key row (8 bf16 or 16 int8
-//     values), so head_dim spans LPK = head_dim*bytes/16 lanes and a warp
-//     reads 32/LPK keys at once with 16-byte shared loads.  The partial dot
+//     values; 8 bytes for int8 rows of 256 bytes), so head_dim spans
+//     LPK = row bytes / chunk bytes lanes and a warp reads 32/LPK keys at
+//     once with vector shared loads.  The partial dot
 //     products of a lane's keys x GT heads finish with one butterfly
 //     reduce-scatter inside its LPK-lane group; P.V accumulates per lane and
 //     the key groups are summed once at the end.
@@ -35,6 +36,8 @@
 #include <cuda_bf16.h>
 #include <math.h>
 
+#include <atomic>
+
 #include "pkv_device.cuh"
 #include "pkv_internal.h"
 
@@ -42,7 +45,23 @@ namespace pkv {
 
 constexpr int NC = 4;                    // consumer warps per CTA
 constexpr int THREADS = (NC + 1) * 32;   // + one producer warp
-constexpr int BAR_BYTES = 512;           // mbarrier area at the start of smem
+constexpr int BAR_BYTES = 640;           // mbarriers + stage masks at the start of smem
+
+// Paged blocks per ring stage: about 8 KB of K per stage (int8: at least four
+// blocks, i.e. 16 keys per consumer warp, since unpacking makes its per-key
+// work larger and the per-stage costs must be spread over more keys), and at
+// most 8 / GT so that one reduce-scatter covers a warp's dot products.
+__host__ __device__ constexpr int blocks_per_stage(int tile, int gt, bool int8)
+{
+    const int by_bytes = 8192 / tile;
+    const int least = int8 ? 4 : 1;
+    const int want = by_bytes > least ? by_bytes : least;
+    return want < 8 / gt ? want : 8 / gt;
+}
+
+#ifndef PKV_CHUNK_RULE
+#define PKV_CHUNK_RULE ((INT8 ? GT >= 4 : (GT >= 4 && D <= 128)) ? 8 : 16)
+#endif
 
 struct KeyRange {
     int lo, pos, blk_lo, nblk, nsplit;
@@ -75,16 +94,15 @@ struct Cfg {
     static constexpr int NCH = D / CHE;                         // boxes per tile
     static constexpr int ROWB = CHE * ES;                       // bytes of one box row
     static constexpr int TILE = P * D * ES;                     // one kv head x one block
-    // A lane owns one 16-byte chunk of a key row: EPL elements, NPR pairs.
-    static constexpr int EPL = 16 / ES;
+    // A lane owns one CB-byte chunk of a key row: EPL elements, NPR pairs.
+    // 8-byte chunks where 16 would hold 32 or more q (and o) values per lane
+    // over the GT heads (registers, hence CTAs per SM); 16 bytes elsewhere.
+    static constexpr int CB = PKV_CHUNK_RULE;
+    static constexpr int EPL = CB / ES;
     static constexpr int NPR = EPL / 2;
     static constexpr int LPK = D / EPL;                         // lanes per key row
     static constexpr int KG = 32 / LPK;                         // keys a warp reads at once
-    // Paged blocks per ring stage: about 8 KB of K per stage, and at most
-    // 32 / GT keys per consumer warp so one reduce-scatter covers them.
-    static constexpr int BPS_MEM = (8192 / TILE) < 1 ? 1 : (8192 / TILE);
-    static constexpr int BPS_MAX = 8 / GT;
-    static constexpr int BPS = BPS_MEM < BPS_MAX ? BPS_MEM : BPS_MAX;
+    static constexpr int BPS = blocks_per_stage(TILE, GT, INT8);
     static constexpr int KEYS = P * BPS;                        // keys per stage
     static constexpr int KPW = KEYS / NC;                       // keys per warp per stage
     static constexpr int KPL = KPW / KG;                        // keys per lane per stage
@@ -104,10 +122,6 @@ __host__ __device__ inline int slot_bytes(int tile, int bps, int per_token)
     return round_up(bps * tile + (per_token ? bps * 64 : 0), 128);
 }
 
-__host__ __device__ constexpr int blocks_per_stage(int tile, int gt)
-{
-    return (8192 / tile) < 1 ? 1 : ((8192 / tile) < 8 / gt ? (8192 / tile) : 8 / gt);
-}
 
 // Butterfly reduce-scatter of NV per-lane partial sums within aligned groups
 // of W lanes (NV <= W, both powers of two): after log2(NV) halving steps lane
@@ -135,23 +149,31 @@ __device__ __forceinline__ float reduce_scatter(float (&v)[NV], int lane)
     return r;
 }
 
-// Sixteen bytes of a tile row as float2 pairs (exact).  bf16: the two halves
-// of each 32-bit word.  int8: each byte b is placed in the low mantissa bits
-// of 2^23 (after flipping its sign bit, giving b+128) and 2^23+128 is
-// subtracted, which yields b exactly.
-template <bool INT8>
-__device__ __forceinline__ void load_chunk(const uint8_t *p, float2 (&f)[INT8 ? 8 : 4])
+// CB (8 or 16) bytes of a tile row as float2 pairs (exact).  bf16: the two
+// halves of each 32-bit word.  int8: each byte b is placed in the low
+// mantissa bits of 2^23 (after flipping its sign bit, giving b+128) and
+// 2^23+128 is subtracted, which yields b exactly.
+template <bool INT8, int CB>
+__device__ __forceinline__ void load_chunk(const uint8_t *p, float2 (&f)[INT8 ? CB / 2 : CB / 4])
 {
-    const uint4 u = *reinterpret_cast<const uint4 *>(p);
-    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+    constexpr int NW = CB / 4;
+    uint32_t w[NW];
+    if constexpr (CB == 16) {
+        const uint4 u = *reinterpret_cast<const uint4 *>(p);
+        w[0] = u.x; w[1] = u.y; w[2] = u.z; w[3] = u.w;
+    } else {
+        static_assert(CB == 8, "chunk bytes");
+        const uint2 u = *reinterpret_cast<const uint2 *>(p);
+        w[0] = u.x; w[1] = u.y;
+    }
     if constexpr (!INT8) {
 #pragma unroll
-        for (int i = 0; i < 4; ++i)
+        for (int i = 0; i < NW; ++i)
             f[i] = make_float2(bf16lo(w[i]), bf16hi(w[i]));
     } else {
         const float2 bias = make_float2(-8388736.0f, -8388736.0f);  // -(2^23 + 128)
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
+        for (int i = 0; i < 2 * NW; ++i) {
             const uint32_t x = w[i / 2] ^ 0x80808080u;
             const int b0 = (i % 2) * 2;
             const float lo = __uint_as_float(__byte_perm(x, 0x4B000000u, 0x7540 + b0));
@@ -173,6 +195,7 @@ __global__ void __launch_bounds__(THREADS) decode_kernel(const DecodeParams p,
     uint64_t *kempty = kfull + 16;
     uint64_t *vfull = kfull + 32;
     uint64_t *vempty = kfull + 48;
+    uint32_t *smask = reinterpret_cast<uint32_t *>(kfull + 64);  // valid blocks per stage
     uint8_t *ring = smem + BAR_BYTES;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -222,8 +245,8 @@ __global__ void __launch_bounds__(THREADS) decode_kernel(const DecodeParams p,
         // The producer warp walks the stages in order.  Lane 0 fills the K
         // slot of stage s % NS as soon as the consumers have formed the
         // scores of its previous contents, then the V slot as soon as the
-        // previous P.V on it is done; the other lanes only help read the
-        // block table.
+        // previous P.V on it is done, and publishes which blocks of the
+        // stage hold data; the other lanes only help read the block table.
         if (nst > 0) {
             if (lane == 0) {
                 prefetch_tensormap(&tmk);
@@ -235,11 +258,11 @@ __global__ void __launch_bounds__(THREADS) decode_kernel(const DecodeParams p,
             tc.init(bt_row + ub0, n, lane);
             int issued[2] = {0, 0};
             bool ok = true;
+            int st = 0;             // ring slot of stage sidx
+            uint32_t rpar = 0;      // parity of the ring round of stage sidx
             for (int sidx = 0; sidx < nst && ok; ++sidx) {
-                const int st = sidx % NS;
-                const uint32_t prev = ((sidx / NS) - 1) & 1;
                 int phys[BPS];
-                uint32_t tx = 0;
+                uint32_t tx = 0, vm = 0;
 #pragma unroll
                 for (int t = 0; t < BPS; ++t) {
                     const int i = sidx * BPS + t;
@@ -248,21 +271,25 @@ __global__ void __launch_bounds__(THREADS) decode_kernel(const DecodeParams p,
                                        static_cast<unsigned>(p.num_blocks);
                     if (!valid && i < n && lane == 0)
                         record_error(p.err, PKV_DEV_BAD_BLOCK);
-                    if (!valid)
+                    if (!valid) {
                         phys[t] = -1;
-                    else
+                    } else {
                         tx += C::TILE + (per_token ? 64u : 0u);
+                        vm |= 1u << t;
+                    }
                 }
                 for (int which = 0; which < (alias ? 1 : 2); ++which) {
                     uint64_t *fullb = which == 0 ? kfull : vfull;
                     uint64_t *emptyb = which == 0 ? kempty : vempty;
-                    if (sidx >= NS && !mbar_wait(&emptyb[st], prev, p.err)) {
+                    if (sidx >= NS && !mbar_wait(&emptyb[st], rpar ^ 1u, p.err)) {
                         ok = false;
                         break;
                     }
                     issued[which] = sidx + 1;
                     if (lane != 0)
                         continue;
+                    if (which == 0)
+                        smask[st] = vm;  // released by the arrive below
                     mbar_arrive_expect_tx(&fullb[st], tx);
                     uint8_t *dst = ring + st * SB + which * KS;
                     const CUtensorMap *map = which == 0 ? &tmk : &tmv;
@@ -281,6 +308,10 @@ __global__ void __launch_bounds__(THREADS) decode_kernel(const DecodeParams p,
                     }
                 }
                 ok = __all_sync(FULL_MASK, ok);
+                if (++st == NS) {
+                    st = 0;
+                    rpar ^= 1u;
+                }
             }
             // Drain: do not let the CTA retire with copies in flight.
             if (lane == 0)
@@ -296,10 +327,10 @@ __global__ void __launch_bounds__(THREADS) decode_kernel(const DecodeParams p,
     // Every consumer warp works on every stage: warp w takes the stage's
     // keys [w*KPW, (w+1)*KPW), so a stage is released after a quarter of
     // its work and the rest of the ring stays in flight.  Within a warp,
-    // lane (kg, dl) owns the 16-byte chunk dl of a key row and reads keys
-    // kg, kg+KG, kg+2KG, ... of the warp's share: every shared load is 16
-    // bytes, eight consecutive lanes cover 128 consecutive bytes, and the
-    // score reductions stay within the LPK lanes of one key.
+    // lane (kg, dl) owns the CB-byte chunk dl of a key row and reads keys
+    // kg, kg+KG, kg+2KG, ... of the warp's share: consecutive lanes read
+    // consecutive bytes, and the score reductions stay within the LPK lanes
+    // of one key.
     constexpr int NPR = C::NPR, NV = C::NV, KPW = C::KPW, KPL = C::KPL, KG = C::KG;
     constexpr int LPK = C::LPK, DUP = C::DUP;
     const int G = p.group;
@@ -308,12 +339,11 @@ __global__ void __launch_bounds__(THREADS) decode_kernel(const DecodeParams p,
     const int lane_off = (lane_elem / C::CHE) * C::P * C::ROWB + (lane_elem % C::CHE) * C::ES;
     const int k0w = warp * KPW;   // this warp's first key within a stage
     const int kb = k0w + kg;      // this lane's first key within a stage
-    int koff[KPL];                // smem offset of key r of this lane in a slot
-#pragma unroll
-    for (int r = 0; r < KPL; ++r) {
-        const int k = kb + KG * r;
-        koff[r] = (k / C::P) * C::TILE + (k % C::P) * C::ROWB + lane_off;
-    }
+    // Slot offset of this lane's key r = its first key's offset + koff(r): KG
+    // divides P and KPW is a divisor or a multiple of P, so the keys
+    // kb + KG*r never straddle a block differently from KG*r.
+    const int lane_base = (k0w / C::P) * C::TILE + (k0w % C::P + kg) * C::ROWB + lane_off;
+    auto koff = [](int r) { return ((KG * r) / C::P) * C::TILE + ((KG * r) % C::P) * C::ROWB; };
 
     float2 qf[GT][NPR];
     {
@@ -327,12 +357,12 @@ __global__ void __launch_bounds__(THREADS) decode_kernel(const DecodeParams p,
                 const uint8_t *qr = reinterpret_cast<const uint8_t *>(
                     p.q + (static_cast<size_t>(b) * p.num_q_heads + g * G + hl) * D + lane_elem);
 #pragma unroll
-                for (int c = 0; c < NPR / 4; ++c) {
-                    float2 t[4];
-                    load_chunk<false>(qr + 16 * c, t);
+                for (int c = 0; c < NPR / 2; ++c) {
+                    float2 t[2];
+                    load_chunk<false, 8>(qr + 8 * c, t);
 #pragma unroll
-                    for (int i = 0; i < 4; ++i)
-                        qf[h][4 * c + i] = make_float2(t[i].x * qmul, t[i].y * qmul);
+                    for (int i = 0; i < 2; ++i)
+                        qf[h][2 * c + i] = make_float2(t[i].x * qmul, t[i].y * qmul);
                 }
             } else {
 #pragma unroll
@@ -357,21 +387,12 @@ __global__ void __launch_bounds__(THREADS) decode_kernel(const DecodeParams p,
     const int km = kb + KG * my_r;          // its key within a stage
     const bool l_owner = (dl % DUP) == 0;   // one lane per value adds to l
 
-    TableCursor tc;
-    tc.init(bt_row + ub0, n, lane);
-    for (int sidx = 0; sidx < nst; ++sidx) {
-        const int st = sidx % NS;
-        const uint32_t par = (sidx / NS) & 1;
-        uint32_t vmask = 0;  // blocks of the stage that hold data
-#pragma unroll
-        for (int t = 0; t < BPS; ++t) {
-            const int i = sidx * BPS + t;
-            const int phys = i < n ? tc.get(i, lane) : -1;
-            if (static_cast<unsigned>(phys) < static_cast<unsigned>(p.num_blocks))
-                vmask |= 1u << t;
-        }
+    int st = 0;          // ring slot of stage sidx
+    uint32_t par = 0;    // parity of its fill
+    for (int sidx = 0; sidx < nst; ++sidx, st = (st + 1 == NS) ? 0 : st + 1, par ^= (st == 0)) {
         if (!__all_sync(FULL_MASK, mbar_wait(&kfull[st], par, p.err)))
             break;
+        const uint32_t vmask = smask[st];  // blocks of the stage that hold data
         const uint8_t *kt = ring + st * SB;
         const uint8_t *vt = alias ? kt : kt + KS;
         const float *ksc = reinterpret_cast<const float *>(kt + BPS * C::TILE);
@@ -389,7 +410,7 @@ __global__ void __launch_bounds__(THREADS) decode_kernel(const DecodeParams p,
 #pragma unroll
         for (int r = 0; r < KPL; ++r) {
             float2 kf[NPR];
-            load_chunk<INT8>(kt + koff[r], kf);
+            load_chunk<INT8, C::CB>(kt + lane_base + koff(r), kf);
 #pragma unroll
             for (int h = 0; h < GT; ++h) {
                 float2 a = __fmul2_rn(qf[h][0], kf[0]);
@@ -461,7 +482,7 @@ __global__ void __launch_bounds__(THREADS) decode_kernel(const DecodeParams p,
             float w[GT];
 #pragma unroll
             for (int h = 0; h < GT; ++h)
-                w[h] = __shfl_sync(FULL_MASK, pv, kg * LPK + (h * KPL + r) * DUP);
+                w[h] = __shfl_sync(FULL_MASK, pv, (h * KPL + r) * DUP, LPK);
             if (!all_in) {
                 // masked key: its slot may hold stale data, do not touch it
                 const int k = kb + KG * r;
@@ -470,7 +491,7 @@ __global__ void __launch_bounds__(THREADS) decode_kernel(const DecodeParams p,
                     continue;
             }
             float2 vf[NPR];
-            load_chunk<INT8>(vt + koff[r], vf);
+            load_chunk<INT8, C::CB>(vt + lane_base + koff(r), vf);
 #pragma unroll
             for (int h = 0; h < GT; ++h) {
                 const float2 w2 = make_float2(w[h], w[h]);
@@ -624,12 +645,85 @@ size_t decode_smem_bytes(int head_dim, int int8, int alias, int per_token, int g
                          int num_stages)
 {
     const int tile = kBlock * head_dim * (int8 ? 1 : 2);
-    const int bps = blocks_per_stage(tile, group_tile);
+    const int bps = blocks_per_stage(tile, group_tile, int8 != 0);
     const size_t ring = static_cast<size_t>(num_stages) * (alias ? 1 : 2) *
                         slot_bytes(tile, bps, per_token);
     const size_t merge = (2 * NC * group_tile + static_cast<size_t>(NC) * group_tile * head_dim) *
                          sizeof(float);
     return BAR_BYTES + (ring > merge ? ring : merge);
+}
+
+// Let the kernel use the opt-in maximum of dynamic shared memory (once).
+template <int D, int GT, bool INT8>
+static cudaError_t configure_smem()
+{
+    static std::atomic<int> done{0};
+    if (done.load(std::memory_order_acquire))
+        return cudaSuccess;
+    int dev = 0, optin = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess)
+        e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(decode_kernel<D, GT, INT8>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, optin);
+    if (e == cudaSuccess)
+        done.store(1, std::memory_order_release);
+    return e;
+}
+
+// Ring depth: the most CTAs per SM first (registers or shared memory limit
+// them; the consumer warps' dependency chains, not bytes in flight, limit a
+// CTA), then the deepest ring (2..8 stages) that keeps that many.
+template <int D, int GT, bool INT8>
+static int ring_stages_one(int alias, int per_token)
+{
+    static std::atomic<int> cache[2][2];
+    int v = cache[alias][per_token].load(std::memory_order_relaxed);
+    if (v)
+        return v;
+    if (configure_smem<D, GT, INT8>() != cudaSuccess)
+        return 2;
+    int best = 2, best_occ = -1;
+    for (int ns = 2; ns <= 8; ++ns) {
+        const size_t smem = decode_smem_bytes(D, INT8, alias, per_token, GT, ns);
+        int occ = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, decode_kernel<D, GT, INT8>,
+                                                          THREADS, smem) != cudaSuccess ||
+            occ < 1)
+            break;
+        if (occ >= best_occ) {
+            best_occ = occ;
+            best = ns;
+        }
+    }
+    cache[alias][per_token].store(best, std::memory_order_relaxed);
+    return best;
+}
+
+template <int D>
+static int ring_stages_d(int int8, int alias, int per_token, int gt)
+{
+    if (int8) {
+        if (gt == 1) return ring_stages_one<D, 1, true>(alias, per_token);
+        if (gt == 2) return ring_stages_one<D, 2, true>(alias, per_token);
+        return ring_stages_one<D, 4, true>(alias, per_token);
+    }
+    if (gt == 1) return ring_stages_one<D, 1, false>(alias, per_token);
+    if (gt == 2) return ring_stages_one<D, 2, false>(alias, per_token);
+    return ring_stages_one<D, 4, false>(alias, per_token);
+}
+
+int decode_ring_stages(int head_dim, int int8, int alias, int per_token, int group_tile)
+{
+    alias = alias != 0;
+    per_token = per_token != 0;
+    switch (head_dim) {
+    case 64: return ring_stages_d<64>(int8, alias, per_token, group_tile);
+    case 128: return ring_stages_d<128>(int8, alias, per_token, group_tile);
+    case 256: return ring_stages_d<256>(int8, alias, per_token, group_tile);
+    default: return 2;
+    }
 }
 
 template <int D, int GT, bool INT8>
@@ -639,19 +733,11 @@ static cudaError_t launch_one(const DecodeParams &p, const CUtensorMap &tmk,
     const size_t smem =
         decode_smem_bytes(D, INT8, p.alias, INT8 && p.scale_mode == PKV_SCALE_PER_TOKEN, GT,
                           p.num_stages);
-    static_assert(Cfg<D, GT, INT8>::BPS == blocks_per_stage(Cfg<D, GT, INT8>::TILE, GT),
-                  "host and device stage geometry");
-    auto kern = decode_kernel<D, GT, INT8>;
-    static int configured = 0;  // largest dynamic smem set so far (per process)
-    if (static_cast<int>(smem) > configured) {
-        cudaError_t e =
-            cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess)
-            return e;
-        configured = static_cast<int>(smem);
-    }
+    cudaError_t e = configure_smem<D, GT, INT8>();
+    if (e != cudaSuccess)
+        return e;
     dim3 grid(p.num_splits, p.num_kv_heads * p.head_chunks, p.batch);
-    kern<<<grid, THREADS, smem, s>>>(p, tmk, tmv);
+    decode_kernel<D, GT, INT8><<<grid, THREADS, smem, s>>>(p, tmk, tmv);
     return cudaGetLastError();
 }
 

@@ -77,6 +77,7 @@ struct CombineParams {
 int decode_group_tile(int group);  // query heads per CTA for a GQA group
 size_t decode_smem_bytes(int head_dim, int int8, int alias, int per_token, int group_tile,
                          int num_stages);
+int decode_ring_stages(int head_dim, int int8, int alias, int per_token, int group_tile);
 cudaError_t launch_decode(const DecodeParams &p, const CUtensorMap &tmk, const CUtensorMap &tmv,
                           int head_dim, int int8, int group_tile, cudaStream_t s);
 cudaError_t launch_combine(const CombineParams &p, cudaStream_t s);
