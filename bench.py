@@ -221,13 +221,20 @@ def run_ours(args, rank, world, local_rank):
     scale = float(np.float32(spec.softmax_scale))
     req = args.split_tokens if args.split_tokens is not None else (spec.split_tokens
                                                                     or pkv.SPLIT_AUTO)
+    # A workload that names its split length (or --split-tokens) runs the two
+    # split-KV calls; otherwise one paged_decode_attention call.
+    split_api = req != pkv.SPLIT_AUTO and req > 0
     st = pkv.paged_decode_split_tokens(B, Hq, spec.num_kv_heads, max_len, spec.window, req)
     ns = pkv.paged_decode_num_splits(max_len, spec.window, st) if st > 0 else 1
+    split_api = split_api and st > 0
     ws_bytes = pkv.paged_decode_workspace_bytes(B, Hq, spec.num_kv_heads, D, max_len,
                                                 spec.window, st)
     ws = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device=dev)
-    lse = torch.empty((B, Hq, ns), dtype=torch.float32, device=dev)
-    po = torch.empty((B, Hq, ns, D), dtype=torch.float32, device=dev)
+    pws = torch.empty(max(pkv.paged_decode_partial_workspace_bytes(B, Hq, spec.num_kv_heads, D),
+                          256), dtype=torch.uint8, device=dev)
+    lse = torch.empty((B, ns, Hq), dtype=torch.float32, device=dev)
+    po = torch.empty((B, ns, Hq, D), dtype=torch.float32, device=dev)
+    tc = pkv.uses_tensor_cores(pool, Hq)
     torch.cuda.synchronize()
     pkv.device_status(clear=True)
 
@@ -237,28 +244,72 @@ def run_ours(args, rank, world, local_rank):
         pkv.paged_kv_append(k_new, v_new, slots, pool)
         if ev is not None:
             ev[1].record()
-        if st > 0:
+        if split_api:
             pkv.paged_decode_split_partial(q, pool, bt, sl, spec.window, scale, st, lse, po, out,
-                                           max_len)
+                                           max_len, workspace=pws)
             if ev is not None:
                 ev[2].record()
             pkv.paged_decode_lse_combine(lse, po, sl, spec.window, st, out)
         else:
             pkv.paged_decode_attention(q, pool, bt, sl, spec.window, scale, out, max_len,
-                                       split_tokens=0)
+                                       split_tokens=st, workspace=ws)
             if ev is not None:
                 ev[2].record()
         if ev is not None:
             ev[3].record()
 
-    launches_per_step = 1 + (2 if st > 0 else 1)
+    # kernels per step: append; decode (tensor cores: plan + stream-K decode +
+    # fix-up; CUDA cores: decode [+ combine when split])
+    if tc:
+        launches_per_step = 1 + 3 + (1 if split_api else 0)
+    else:
+        launches_per_step = 1 + 1 + (1 if st > 0 else 0)
     dbytes = bytes_model.decode_bytes(spec, w.seq_lens, w.block_table)
     abytes = bytes_model.append_bytes(spec, int((w.new_slots >= 0).sum()))
     step_bytes = dbytes["kv"] + dbytes["q"] + dbytes["out"] + abytes
-    decode_kernel_bytes = dbytes["kv"] + dbytes["q"] + (dbytes["out"] if st == 0 else 0)
+    decode_kernel_bytes = dbytes["kv"] + dbytes["q"] + (dbytes["out"] if not split_api else 0)
 
     for _ in range(max(3, args.warmup)):
         step()
+    torch.cuda.synchronize()
+    # The step's three parts (append, decode, combine) are captured as CUDA
+    # graphs and replayed, so that the timed region measures the GPU and not
+    # the Python loop that enqueues the calls; events between the replays
+    # give the per-part device times.
+    parts = [None, None, None]
+    cap = torch.cuda.Stream()
+    cap.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(cap):
+        parts[0] = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(parts[0], stream=cap):
+            pkv.paged_kv_append(k_new, v_new, slots, pool)
+        parts[1] = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(parts[1], stream=cap):
+            if split_api:
+                pkv.paged_decode_split_partial(q, pool, bt, sl, spec.window, scale, st, lse, po,
+                                               out, max_len, workspace=pws)
+            else:
+                pkv.paged_decode_attention(q, pool, bt, sl, spec.window, scale, out, max_len,
+                                           split_tokens=st, workspace=ws)
+        if split_api:
+            parts[2] = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(parts[2], stream=cap):
+                pkv.paged_decode_lse_combine(lse, po, sl, spec.window, st, out)
+    torch.cuda.current_stream().wait_stream(cap)
+    torch.cuda.synchronize()
+
+    def replay(ev):
+        ev[0].record()
+        parts[0].replay()
+        ev[1].record()
+        parts[1].replay()
+        ev[2].record()
+        if parts[2] is not None:
+            parts[2].replay()
+        ev[3].record()
+
+    for _ in range(3):
+        replay([torch.cuda.Event(enable_timing=True) for _ in range(4)])
     torch.cuda.synchronize()
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
     if world > 1:
@@ -271,7 +322,7 @@ def run_ours(args, rank, world, local_rank):
     t0 = time.time()
     start.record()
     for i in range(args.steps):
-        step(evs[i])
+        replay(evs[i])
     end.record()
     torch.cuda.synchronize()
     t1 = time.time()
@@ -369,8 +420,11 @@ def run_ours(args, rank, world, local_rank):
             "batch": B, "num_q_heads": Hq, "num_kv_heads": spec.num_kv_heads, "head_dim": D,
             "window": spec.window, "block_size": P, "num_blocks": w.layout.num_blocks,
             "split_tokens": st, "num_splits": ns,
-            "step": "append 1 token/seq + decode (split partial + combine)" if st > 0
-                    else "append 1 token/seq + single-pass decode",
+            "step": ("append 1 token/seq + decode (split partial + combine)" if split_api
+                     else "append 1 token/seq + paged_decode_attention"),
+            "timing": "CUDA-graph replays of the step's parts, CUDA events between them",
+            "decode_kernel": ("tensor cores (tcgen05), persistent stream-K" if tc
+                              else "CUDA cores"),
             "l2": f"inputs larger than L2 ({dbytes['kv'] / 1e6:.0f} MB of KV read per step vs 129 MB L2); no flush",
             "parallelism": f"replicas: one independent batch per GPU x{world}",
         },
@@ -381,7 +435,9 @@ def run_ours(args, rank, world, local_rank):
                            "append": abytes, "total": step_bytes},
         "kernels_us": {"append": round(app_us, 3), "decode": round(dec_us, 3),
                        "combine": round(cmb_us, 3)},
-        "roofline": {"bound": "hbm", "kernel": "decode_kernel (split partial)" if st > 0 else "decode_kernel",
+        "roofline": {"bound": "hbm",
+                     "kernel": ("decode_tc_kernel (+ plan, fix-up)" if tc else "decode_kernel")
+                     + (" split partial" if split_api else ""),
                      "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "peak_source": peak_kind,
                      "algorithmic_bytes_per_launch": decode_kernel_bytes,

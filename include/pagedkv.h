@@ -150,14 +150,28 @@ PKV_API int32_t paged_decode_num_splits(int32_t block_size, int32_t max_seq_len,
 
 /*
  * paged_decode_workspace_bytes -- device scratch paged_decode_attention needs
- * for these sizes (0 when it runs as a single pass).  Layout: partial
- * log-sum-exp [batch][num_q_heads][num_splits] fp32, then (256-byte
- * aligned) partial outputs [batch][num_q_heads][num_splits][head_dim] fp32.
+ * for these sizes: the larger of the split partials (when the key ranges
+ * are split: partial log-sum-exp [batch][num_splits][num_q_heads] fp32,
+ * then, 256-byte aligned, partial outputs
+ * [batch][num_splits][num_q_heads][head_dim] fp32) and the tensor-core
+ * kernel's scratch (paged_decode_partial_workspace_bytes).  0 when neither
+ * is needed.
  */
 PKV_API size_t paged_decode_workspace_bytes(int32_t batch, int32_t num_q_heads,
                                             int32_t num_kv_heads, int32_t head_dim,
                                             int32_t block_size, int32_t max_seq_len,
                                             int32_t window, int32_t split_tokens);
+
+/*
+ * paged_decode_partial_workspace_bytes -- device scratch of the tensor-core
+ * kernel (bf16 pools, head_dim 128 or 256, 8 to 16 query heads per KV head),
+ * which paged_decode_split_partial needs as its workspace and which
+ * paged_decode_workspace_bytes includes: the stream-K plan (one entry per
+ * SM and a prefix sum per sequence) and the partial states of key ranges
+ * cut between SMs.  0 for shapes that run on the CUDA-core kernel.
+ */
+PKV_API size_t paged_decode_partial_workspace_bytes(int32_t batch, int32_t num_q_heads,
+                                                    int32_t num_kv_heads, int32_t head_dim);
 
 /*
  * paged_decode_attention -- one decode step of one layer: for every sequence
@@ -181,7 +195,9 @@ PKV_API size_t paged_decode_workspace_bytes(int32_t batch, int32_t num_q_heads,
  *   split_tokens: 0 = single pass; > 0 = split each key range into pieces
  *                 of this many keys (multiple of block_size) and merge them
  *                 with a log-sum-exp combine; PKV_SPLIT_AUTO = library's
- *                 choice.
+ *                 choice.  The tensor-core kernel balances the key ranges
+ *                 across SMs itself and ignores it (same result up to
+ *                 rounding).
  *   workspace:    device scratch of paged_decode_workspace_bytes(...) bytes,
  *                 256-byte aligned (NULL allowed when that is 0).
  *   out:          [batch][num_q_heads][head_dim], bf16 (out_dtype
@@ -201,10 +217,14 @@ PKV_API int paged_decode_attention(const void *q, const pkv_pool *pool, const in
  * holding lo (splits are block-aligned: split s covers logical blocks
  * lo/bs + s*split_tokens/bs ... of the sequence, clipped to [lo, pos]).
  * For a sequence whose range has a single split the final output row is
- * written to `out` directly; otherwise partial_lse[b][h][s] (natural log of
- * the sum of exp(score)) and partial_o[b][h][s][:] (the split's normalised
- * output) are written.  split_tokens must be a positive multiple of
- * block_size; num_splits >= paged_decode_num_splits(...).
+ * written to `out` directly; otherwise partial_lse[b][s][h] (natural log of
+ * the sum of exp(score)) and partial_o[b][s][h][:] (the split's normalised
+ * output) are written: split-major, so that one split's query heads are
+ * contiguous.  split_tokens must be a positive multiple of
+ * block_size; num_splits >= paged_decode_num_splits(...); both partial
+ * arrays 16-byte aligned.  workspace: device
+ * scratch of paged_decode_partial_workspace_bytes(...) bytes, 256-byte
+ * aligned (NULL allowed when that is 0).
  */
 PKV_API int paged_decode_split_partial(const void *q, const pkv_pool *pool,
                                        const int32_t *block_table, int32_t max_blocks_per_seq,
@@ -212,7 +232,8 @@ PKV_API int paged_decode_split_partial(const void *q, const pkv_pool *pool,
                                        int32_t num_q_heads, int32_t max_seq_len, int32_t window,
                                        float softmax_scale, int32_t split_tokens,
                                        float *partial_lse, float *partial_o, int32_t num_splits,
-                                       void *out, int32_t out_dtype, void *stream);
+                                       void *workspace, size_t workspace_bytes, void *out,
+                                       int32_t out_dtype, void *stream);
 
 /*
  * paged_decode_lse_combine -- the second step: for each sequence with more
@@ -237,7 +258,8 @@ PKV_API int paged_decode_lse_combine(const float *partial_lse, const float *part
  * loop in which cudaMalloc/cudaFree would synchronise the device.  None of
  * the pages has a counterpart; this is a library convenience.
  *   Same arguments and result as paged_decode_attention, minus the
- *   workspace.  The split-KV partials go to a fixed array of
+ *   workspace.  The split-KV partials (and the tensor-core kernel's
+ *   scratch) go to a fixed array of
  *   PKV_STATIC_SCRATCH_BYTES in device memory that every GPU which loads the
  *   library holds until the process exits.  Sizes whose scratch would not
  *   fit are rejected with PKV_E_WORKSPACE before anything is launched.
@@ -258,6 +280,15 @@ PKV_API int paged_decode_attention_noalloc(const void *q, const pkv_pool *pool,
                                            int32_t window, float softmax_scale,
                                            int32_t split_tokens, void *out, int32_t out_dtype,
                                            void *stream);
+
+/*
+ * paged_decode_uses_tensor_cores -- 1 if decodes over this pool with
+ * num_q_heads query heads run on the tensor-core kernel (bf16 pool,
+ * head_dim 128 or 256, 8 to 16 query heads per KV head; PKV_DISABLE_TC=1 /
+ * PKV_FORCE_TC=1 in the environment override it), 0 if on the CUDA-core
+ * kernel, or a negative PKV_E_* code for an invalid pool.  Host only.
+ */
+PKV_API int32_t paged_decode_uses_tensor_cores(const pkv_pool *pool, int32_t num_q_heads);
 
 /* Message of the last host-side error on this thread ("" if none). */
 PKV_API const char *pkv_last_error(void);

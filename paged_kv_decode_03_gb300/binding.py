@@ -67,8 +67,10 @@ def load_library():
     lib.paged_decode_attention.argtypes = [p, p, p, i32, p, i32, i32, i32, i32, f32, i32, p, sz,
                                            p, i32, p]
     lib.paged_decode_attention.restype = ctypes.c_int
+    lib.paged_decode_partial_workspace_bytes.argtypes = [i32] * 4
+    lib.paged_decode_partial_workspace_bytes.restype = sz
     lib.paged_decode_split_partial.argtypes = [p, p, p, i32, p, i32, i32, i32, i32, f32, i32, p,
-                                               p, i32, p, i32, p]
+                                               p, i32, p, sz, p, i32, p]
     lib.paged_decode_split_partial.restype = ctypes.c_int
     lib.paged_decode_lse_combine.argtypes = [p, p, p, i32, i32, i32, i32, i32, i32, i32, p, i32,
                                              p]
@@ -76,6 +78,8 @@ def load_library():
     lib.paged_decode_attention_noalloc.argtypes = [p, p, p, i32, p, i32, i32, i32, i32, f32,
                                                    i32, p, i32, p]
     lib.paged_decode_attention_noalloc.restype = ctypes.c_int
+    lib.paged_decode_uses_tensor_cores.argtypes = [p, i32]
+    lib.paged_decode_uses_tensor_cores.restype = i32
     lib.pkv_last_error.argtypes = []
     lib.pkv_last_error.restype = ctypes.c_char_p
     lib.pkv_device_status.argtypes = [i32]
@@ -229,31 +233,56 @@ def paged_decode_attention(q, pool: PagedKVPool, block_table, seq_lens, window: 
     return out
 
 
+def uses_tensor_cores(pool: PagedKVPool, num_q_heads: int) -> bool:
+    """Whether decodes over ``pool`` run on the tensor-core kernel."""
+    lib = load_library()
+    pc = pool.c_struct()
+    r = int(lib.paged_decode_uses_tensor_cores(ctypes.byref(pc), int(num_q_heads)))
+    _check(min(r, 0), "paged_decode_uses_tensor_cores")
+    return r == 1
+
+
+def paged_decode_partial_workspace_bytes(batch, num_q_heads, num_kv_heads, head_dim) -> int:
+    return int(load_library().paged_decode_partial_workspace_bytes(batch, num_q_heads,
+                                                                   num_kv_heads, head_dim))
+
+
 def paged_decode_split_partial(q, pool: PagedKVPool, block_table, seq_lens, window: int,
                                softmax_scale: float, split_tokens: int, partial_lse, partial_o,
-                               out, max_seq_len: int, stream=None):
-    """Split-KV step 1: partial_lse [B, H_q, S] and partial_o [B, H_q, S, D]
-    (fp32) for multi-split sequences; final rows of single-split ones in out."""
+                               out, max_seq_len: int, workspace=None, stream=None):
+    """Split-KV step 1: partial_lse [B, S, H_q] and partial_o [B, S, H_q, D]
+    (fp32, split-major) for multi-split sequences; final rows of single-split
+    ones in out.
+    ``workspace``: a uint8 CUDA tensor of at least
+    paged_decode_partial_workspace_bytes(...) bytes (allocated through torch
+    if None and needed)."""
     import torch
     lib = load_library()
     pc = pool.c_struct()
     B, Hq, D = (int(x) for x in q.shape)
-    ns = int(partial_lse.shape[2])
+    ns = int(partial_lse.shape[1])
+    need = lib.paged_decode_partial_workspace_bytes(B, Hq, pool.num_kv_heads, D)
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    ws_ptr = _dev_ptr(workspace, "workspace") if workspace is not None else None
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
     out_dtype = OUT_F32 if out.dtype == torch.float32 else OUT_BF16
     _check(lib.paged_decode_split_partial(_dev_ptr(q, "q"), ctypes.byref(pc), _dev_ptr(block_table, "block_table"),
                                           int(block_table.shape[1]), _dev_ptr(seq_lens, "seq_lens"), B, Hq,
                                           int(max_seq_len), int(window), float(softmax_scale),
                                           int(split_tokens), _dev_ptr(partial_lse, "partial_lse"),
-                                          _dev_ptr(partial_o, "partial_o"), ns, _dev_ptr(out, "out"),
-                                          out_dtype, _stream(stream)), "paged_decode_split_partial")
+                                          _dev_ptr(partial_o, "partial_o"), ns, ws_ptr, ws_bytes,
+                                          _dev_ptr(out, "out"), out_dtype, _stream(stream)),
+           "paged_decode_split_partial")
 
 
 def paged_decode_lse_combine(partial_lse, partial_o, seq_lens, window: int, split_tokens: int, out,
                              block_size: int = 16, stream=None):
-    """Split-KV step 2: merge the partials of multi-split sequences into out."""
+    """Split-KV step 2: merge the partials (split-major, as step 1 writes them)
+    of multi-split sequences into out."""
     import torch
     lib = load_library()
-    B, Hq, ns = (int(x) for x in partial_lse.shape)
+    B, ns, Hq = (int(x) for x in partial_lse.shape)
     D = int(partial_o.shape[3])
     out_dtype = OUT_F32 if out.dtype == torch.float32 else OUT_BF16
     _check(lib.paged_decode_lse_combine(_dev_ptr(partial_lse, "partial_lse"), _dev_ptr(partial_o, "partial_o"),

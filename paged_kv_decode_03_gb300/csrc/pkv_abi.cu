@@ -122,6 +122,44 @@ static int encode_pool_map_tc(CUtensorMap *map, void *base, const pkv_pool &pool
     return PKV_OK;
 }
 
+// Tensor map over q [batch*num_q_heads][head_dim] bf16 for the tensor-core
+// kernel: box = {64 dims, 16 rows} with the 128-byte swizzle, i.e. one
+// 64-dim column of Q^T for 16 query heads as the K-major B operand.
+static int encode_q_map(CUtensorMap *map, const void *q, int32_t rows, int32_t head_dim)
+{
+    auto fn = encode_fn();
+    if (!fn)
+        return fail(PKV_E_DRIVER, "cuTensorMapEncodeTiled is unavailable");
+    cuuint64_t dims[2] = {(cuuint64_t)head_dim, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)head_dim * 2};
+    cuuint32_t box[2] = {64u, 16u};
+    cuuint32_t estr[2] = {1u, 1u};
+    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(q), dims, strides,
+                    box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS)
+        return fail(PKV_E_DRIVER, "cuTensorMapEncodeTiled (q) failed (%d)", (int)r);
+    return PKV_OK;
+}
+
+static bool env_flag(const char *name)
+{
+    const char *e = getenv(name);
+    return e && e[0] == '1';
+}
+
+// Whether shapes alone allow the tensor-core kernel (and so its workspace):
+// head_dim 128 or 256 and 8 to 16 query heads per KV head (any group up to
+// 16 with PKV_FORCE_TC=1).
+static bool tc_shape(int group, int head_dim)
+{
+    if ((head_dim != 128 && head_dim != 256) || group < 1 || decode_tc_group_pad(group) == 0)
+        return false;
+    if (env_flag("PKV_DISABLE_TC"))
+        return false;
+    return group >= 8 || env_flag("PKV_FORCE_TC");
+}
+
 // Whether a decode runs on the tensor-core kernel: bf16 pool, head_dim 128
 // or 256, and 8 to 16 query heads per KV head.  Below 8 heads the CUDA-core
 // kernel keeps up with HBM and, with several CTAs per SM, measures faster.
@@ -131,15 +169,7 @@ static bool use_tc(const pkv_pool *pool, int group)
 {
     if (pool->dtype != PKV_BF16 || (pool->head_dim != 128 && pool->head_dim != 256))
         return false;
-    if (decode_tc_group_pad(group) == 0)
-        return false;
-    const char *e = getenv("PKV_DISABLE_TC");
-    if (e && e[0] == '1')
-        return false;
-    const char *f = getenv("PKV_FORCE_TC");
-    if (f && f[0] == '1')
-        return true;
-    return group >= 8;
+    return tc_shape(group, pool->head_dim);
 }
 
 // ---------------------------------------------------------- validation
@@ -222,6 +252,17 @@ PKV_API int pkv_device_status(int32_t clear)
             return fail(PKV_E_DRIVER, "clearing the device error word: %s", cudaGetErrorString(e));
     }
     return static_cast<int>(w);
+}
+
+PKV_API int32_t paged_decode_uses_tensor_cores(const pkv_pool *pool, int32_t num_q_heads)
+{
+    t_last_error.clear();
+    if (int rc = check_pool(pool))
+        return rc;
+    if (num_q_heads <= 0 || num_q_heads % pool->num_kv_heads)
+        return fail(PKV_E_SHAPE, "num_q_heads %d is not a multiple of num_kv_heads %d",
+                    num_q_heads, pool->num_kv_heads);
+    return use_tc(pool, num_q_heads / pool->num_kv_heads) ? 1 : 0;
 }
 
 PKV_API int paged_kv_append(const void *k, const void *v, const int64_t *slot_mapping,
@@ -307,12 +348,26 @@ PKV_API size_t paged_decode_workspace_bytes(int32_t batch, int32_t num_q_heads,
 {
     const int32_t st = paged_decode_split_tokens(batch, num_q_heads, num_kv_heads, block_size,
                                                  max_seq_len, window, split_tokens);
-    if (st <= 0)
+    size_t need = 0;
+    if (st > 0) {
+        const size_t ns = paged_decode_num_splits(block_size, max_seq_len, window, st);
+        const size_t rows = (size_t)batch * num_q_heads * ns;
+        const size_t lse = (rows * sizeof(float) + 255) / 256 * 256;
+        need = lse + rows * head_dim * sizeof(float);
+    }
+    const size_t tc = paged_decode_partial_workspace_bytes(batch, num_q_heads, num_kv_heads,
+                                                           head_dim);
+    return need > tc ? need : tc;
+}
+
+PKV_API size_t paged_decode_partial_workspace_bytes(int32_t batch, int32_t num_q_heads,
+                                                    int32_t num_kv_heads, int32_t head_dim)
+{
+    if (batch <= 0 || num_q_heads <= 0 || num_kv_heads <= 0 || num_q_heads % num_kv_heads)
         return 0;
-    const size_t ns = paged_decode_num_splits(block_size, max_seq_len, window, st);
-    const size_t rows = (size_t)batch * num_q_heads * ns;
-    const size_t lse = (rows * sizeof(float) + 255) / 256 * 256;
-    return lse + rows * head_dim * sizeof(float);
+    if (!tc_shape(num_q_heads / num_kv_heads, head_dim))
+        return 0;
+    return decode_tc_scratch_bytes(batch, head_dim);
 }
 
 static int check_decode_args(const void *q, const pkv_pool *pool, const int32_t *block_table,
@@ -346,11 +401,21 @@ static int run_decode(const void *q, const pkv_pool *pool, const int32_t *block_
                       int32_t max_blocks_per_seq, const int32_t *seq_lens, int32_t batch,
                       int32_t num_q_heads, int32_t max_seq_len, int32_t window,
                       float softmax_scale, int32_t split_tokens, float *part_lse, float *part_o,
-                      int32_t num_splits, void *out, int32_t out_dtype, cudaStream_t s)
+                      int32_t num_splits, void *out, int32_t out_dtype, void *workspace,
+                      size_t workspace_bytes, cudaStream_t s)
 {
     const bool alias = pool->v == nullptr || pool->v == pool->k;
     const int group = num_q_heads / pool->num_kv_heads;
     const bool tc = use_tc(pool, group);
+    if (tc) {
+        const size_t need = decode_tc_scratch_bytes(batch, pool->head_dim);
+        if (!workspace || workspace_bytes < need)
+            return fail(PKV_E_WORKSPACE,
+                        "the tensor-core kernel needs a workspace of %zu bytes, %zu given", need,
+                        workspace ? workspace_bytes : (size_t)0);
+        if (!aligned(workspace, 256))
+            return fail(PKV_E_ALIGN, "workspace must be 256-byte aligned");
+    }
     auto encode = tc ? encode_pool_map_tc : encode_pool_map;
     CUtensorMap tmk, tmv;
     if (int rc = encode(&tmk, pool->k, *pool))
@@ -399,6 +464,7 @@ static int run_decode(const void *q, const pkv_pool *pool, const int32_t *block_
         p.num_stages = ns < 2 ? 2 : ns;
     }
     p.qk_scale_log2 = softmax_scale * LOG2E;
+    p.head_dim = pool->head_dim;
     p.err = error_word_ptr();
     if (!p.err)
         return fail(PKV_E_DRIVER, "cannot resolve the device error word");
@@ -410,7 +476,11 @@ static int run_decode(const void *q, const pkv_pool *pool, const int32_t *block_
         while (nu > 2 && decode_tc_smem_bytes(nu) > 227u * 1024u)
             --nu;
         p.num_stages = nu < 6 ? nu : 6;  // one producer warp per ring unit
-        cudaError_t e = launch_decode_tc(p, tmk, tmv, pool->head_dim, s);
+        CUtensorMap tmq;
+        if (int rc = encode_q_map(&tmq, q, batch * num_q_heads, pool->head_dim))
+            return rc;
+        decode_tc_bind_scratch(p, workspace, batch);
+        cudaError_t e = launch_decode_tc(p, tmk, tmv, tmq, pool->head_dim, s);
         if (e != cudaSuccess)
             return cuda_fail(e, "tensor-core decode launch");
         return PKV_OK;
@@ -426,7 +496,8 @@ PKV_API int paged_decode_split_partial(const void *q, const pkv_pool *pool,
                                        const int32_t *seq_lens, int32_t batch, int32_t num_q_heads,
                                        int32_t max_seq_len, int32_t window, float softmax_scale,
                                        int32_t split_tokens, float *partial_lse, float *partial_o,
-                                       int32_t num_splits, void *out, int32_t out_dtype,
+                                       int32_t num_splits, void *workspace,
+                                       size_t workspace_bytes, void *out, int32_t out_dtype,
                                        void *stream)
 {
     t_last_error.clear();
@@ -442,13 +513,14 @@ PKV_API int paged_decode_split_partial(const void *q, const pkv_pool *pool,
         return fail(PKV_E_UNSUPPORTED, "more than 1024 splits");
     if (!partial_lse || !partial_o)
         return fail(PKV_E_NULL, "partial buffers are NULL");
-    if (!aligned(partial_lse, 4) || !aligned(partial_o, 16))
-        return fail(PKV_E_ALIGN, "partial_o must be 16-byte aligned");
+    if (!aligned(partial_lse, 16) || !aligned(partial_o, 16))
+        return fail(PKV_E_ALIGN, "partial_lse and partial_o must be 16-byte aligned");
     if (batch == 0)
         return PKV_OK;
     return run_decode(q, pool, block_table, max_blocks_per_seq, seq_lens, batch, num_q_heads,
                       max_seq_len, window, softmax_scale, split_tokens, partial_lse, partial_o,
-                      num_splits, out, out_dtype, static_cast<cudaStream_t>(stream));
+                      num_splits, out, out_dtype, workspace, workspace_bytes,
+                      static_cast<cudaStream_t>(stream));
 }
 
 PKV_API int paged_decode_lse_combine(const float *partial_lse, const float *partial_o,
@@ -508,10 +580,12 @@ PKV_API int paged_decode_attention(const void *q, const pkv_pool *pool, const in
     if (batch == 0)
         return PKV_OK;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (st == 0)
+    // The tensor-core kernel balances the key ranges across SMs itself
+    // (stream-K) and writes the outputs without a split pass.
+    if (st == 0 || use_tc(pool, num_q_heads / pool->num_kv_heads))
         return run_decode(q, pool, block_table, max_blocks_per_seq, seq_lens, batch, num_q_heads,
                           max_seq_len, window, softmax_scale, 0, nullptr, nullptr, 1, out,
-                          out_dtype, s);
+                          out_dtype, workspace, workspace_bytes, s);
     const int32_t ns = paged_decode_num_splits(pool->block_size, max_seq_len, window, st);
     if (ns > 1024)
         return fail(PKV_E_UNSUPPORTED, "more than 1024 splits; use a longer split_tokens");
@@ -528,7 +602,8 @@ PKV_API int paged_decode_attention(const void *q, const pkv_pool *pool, const in
     float *po = reinterpret_cast<float *>(static_cast<char *>(workspace) +
                                           (rows * sizeof(float) + 255) / 256 * 256);
     if (int rc = run_decode(q, pool, block_table, max_blocks_per_seq, seq_lens, batch, num_q_heads,
-                            max_seq_len, window, softmax_scale, st, lse, po, ns, out, out_dtype, s))
+                            max_seq_len, window, softmax_scale, st, lse, po, ns, out, out_dtype,
+                            nullptr, 0, s))
         return rc;
     CombineParams c{};
     c.part_lse = lse;

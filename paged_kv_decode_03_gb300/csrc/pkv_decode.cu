@@ -588,9 +588,10 @@ __global__ void __launch_bounds__(THREADS) decode_kernel(const DecodeParams p,
             else
                 reinterpret_cast<__nv_bfloat16 *>(p.out)[row * D + d] = __float2bfloat16_rn(y);
         } else {
-            p.part_o[(row * p.num_splits + split) * D + d] = y;
+            const size_t prow = (static_cast<size_t>(b) * p.num_splits + split) * p.num_q_heads + hq;
+            p.part_o[prow * D + d] = y;
             if (d == 0)
-                p.part_lse[row * p.num_splits + split] =
+                p.part_lse[prow] =
                     L > 0.f ? (M + log2f(L)) * LN2 : -INFINITY;
         }
     }
@@ -607,14 +608,17 @@ __global__ void __launch_bounds__(128) combine_kernel(const CombineParams p)
     if (ns <= 1)
         return;
     const size_t row = static_cast<size_t>(b) * p.num_q_heads + hq;
-    const float *lse = p.part_lse + row * p.num_splits;
+    // split s of this row: lse at [(b*S + s)*H_q + hq], o at that index * D
+    const size_t stride = static_cast<size_t>(p.num_q_heads);
+    const float *lse = p.part_lse + static_cast<size_t>(b) * p.num_splits * stride + hq;
     if (threadIdx.x == 0) {
         float M = -INFINITY;
         for (int s = 0; s < ns; ++s)
-            M = fmaxf(M, lse[s]);
+            M = fmaxf(M, lse[s * stride]);
         float Z = 0.f;
         for (int s = 0; s < ns && s < 1024; ++s) {
-            const float w = (M == -INFINITY || lse[s] == -INFINITY) ? 0.f : expf(lse[s] - M);
+            const float l = lse[s * stride];
+            const float w = (M == -INFINITY || l == -INFINITY) ? 0.f : expf(l - M);
             w_s[s] = w;
             Z += w;
         }
@@ -622,11 +626,11 @@ __global__ void __launch_bounds__(128) combine_kernel(const CombineParams p)
     }
     __syncthreads();
     const float Z = red[0];
-    const float *po = p.part_o + row * p.num_splits * p.head_dim;
+    const float *po = p.part_o + (static_cast<size_t>(b) * p.num_splits * stride + hq) * p.head_dim;
     for (int d = threadIdx.x; d < p.head_dim; d += blockDim.x) {
         float acc = 0.f;
         for (int s = 0; s < ns && s < 1024; ++s)
-            acc = fmaf(w_s[s], po[static_cast<size_t>(s) * p.head_dim + d], acc);
+            acc = fmaf(w_s[s], po[s * stride * p.head_dim + d], acc);
         const float y = Z > 0.f ? acc / Z : 0.f;
         if (p.out_f32)
             reinterpret_cast<float *>(p.out)[row * p.head_dim + d] = y;

@@ -1,19 +1,36 @@
 // pkv_decode_tc.cu -- decode attention over a bf16 paged KV pool on the
-// 5th-generation tensor cores (tcgen05.mma, accumulators in TMEM).
+// 5th-generation tensor cores (tcgen05.mma, accumulators in TMEM), run as a
+// persistent stream-K kernel.
 //
 // Same problem and sources as pkv_decode.cu: y = softmax(scale * q K^T) V
 // over the keys [lo, pos] of each sequence ("CS336 · 第 10 课", KV-cache
 // section; "实验五：Gemma4 端到端推理优化", sliding-window, GQA and Flash
 // Attention sections: online softmax with running max/sum in fp32, blocks
-// outside the window never read).
+// outside the window never read; the split-KV log-sum-exp merge of the
+// flash-decoding design those pages describe).
 //
-// Why tensor cores here: at head_dim 256 the bf16 inner products cost the
-// CUDA cores more issue slots than HBM needs time to deliver the bytes (a
-// variant of the CUDA-core kernel that skips every memory wait runs longer
-// than the memory-bound time), so both contractions move to tcgen05 and the
-// CUDA cores only do the softmax.
+// Why tensor cores here: at head_dim 256 the bf16 inner products of 8-16
+// query heads cost the CUDA cores more issue slots than HBM needs time to
+// deliver the bytes, so both contractions move to tcgen05 and the CUDA cores
+// only do the softmax.
 //
-// One CTA per (split, kv head, sequence), 12 warps:
+// Work decomposition (stream-K).  An item is one (sequence, kv head, split)
+// key range (one split when the caller does not split); the 128-key tiles of
+// all items, in (sequence, kv head, split, tile) order, each item followed by
+// KAPPA virtual tiles that stand for its fixed cost (the last P.V drains and
+// the result is written), form one sequence of W units.
+// tc_plan_kernel (one CTA) scans the lengths and gives CTA c the units
+// [c*W/C, (c+1)*W/C), C = min(grid, W): it records the first item with real
+// tiles there (or an empty item starting there).  A CTA walks its items in order with one pipeline that never
+// drains between them; an item it covers entirely is finished in place (the
+// output, or that split's partial state), an item cut at a CTA boundary
+// leaves one partial state per CTA (log-sum-exp and normalised o), which
+// tc_fixup_kernel merges.  Every SM gets the same number of tiles within
+// one, whatever the mix of lengths, and the per-CTA start-up and drain
+// (TMEM allocation, first loads, last softmax and P.V) are paid once per SM
+// instead of once per item.
+//
+// One CTA per SM, 12 warps:
 //   warps 4-9 (producers): TMA loads of 128-key tiles into a ring of six
 //     32 KB units.  With K and V separate the ring is split into a K ring
 //     (read only by the score warp) and a V ring (read only by the P.V
@@ -22,26 +39,30 @@
 //     what makes parity waits sound.  Producer warp w owns slot w and
 //     issues its uses in order; several issuing warps are needed because
 //     the rate of 2 KB TMA boxes scales with the number of issuing warps.
+//     Producer 0 also loads each item's Q^T (TMA, 128-byte swizzle) into one
+//     of two buffers.
 //   warp 10 (one thread): S^T[128 keys x 16] = K Q^T (M=128, N=16 query
 //     heads padded, K=16 per instruction) into TMEM;
 //   warp 11 (one thread): O^T[128 dims x 16] = V^T P^T per 128-dim half.
-//     A thread issues small tcgen05.mma one after another at a fixed cost
-//     each (about 40 ns here); two issuing threads run side by side, so
-//     each contraction has its own.  tcgen05.commit signals the mbarriers
-//     that free ring units and hand results on.
+//     tcgen05.commit signals the mbarriers that free ring units, Q buffers
+//     and hand results on.
 //   warps 0-3 (softmax): thread t owns key t of the tile (TMEM lane t):
 //     loads its 16 scores, masks keys outside [lo, pos], forms the tile max
 //     per head (warp shuffles + one exchange through shared memory), keeps
 //     running max / sums in fp32, writes P^T in bf16 (K-major, swizzled)
 //     for the P.V MMA -- for fp32 output also the bf16 residual p - bf16(p),
 //     multiplied in a second pass, which keeps the error near 2^-17 -- and
-//     accumulates the per-tile O^T (thread t owns
-//     output dims t and 128+t) with the rescale alpha = 2^(m_old - m_new).
+//     accumulates the per-tile O^T (thread t owns output dims t and 128+t)
+//     with the rescale alpha = 2^(m_old - m_new).
 //     The P.V warp zeroes the V rows of masked keys inside loaded blocks
 //     (stale slots past pos, keys before the window start) before its MMAs
 //     read them, so no stale value (not even a NaN) reaches the output.
+//   Q^T rows past the group hold other heads' queries (or zeros past the
+//   end of q); their score columns are masked and their P^T rows stay zero.
 #include <cuda_bf16.h>
 #include <math.h>
+
+#include <atomic>
 
 #include "pkv_device.cuh"
 #include "pkv_internal.h"
@@ -60,7 +81,8 @@ constexpr int NPAD = 16;          // N of every MMA: query heads padded to 16
 constexpr int UNIT = 32768;       // 128 keys x 128 dims bf16
 constexpr int CHUNK = 16384;      // 128 keys x 64 dims bf16 (one swizzled column)
 constexpr int CTRL = 1024;        // barriers, TMEM address, flags, exchange
-constexpr int QBYTES = 8192;      // Q^T: up to 4 columns x 16 heads x 128 B
+constexpr int QBUF = 8192;        // Q^T of one item: up to 4 columns x 16 heads x 128 B
+constexpr int QBYTES = 2 * QBUF;  // two Q^T buffers
 constexpr int PBYTES = 16384;     // P^T: 2 buffers x (hi, lo) x 2 columns x 16 heads x 128 B
 constexpr int RING_OFF = CTRL + QBYTES + PBYTES;
 constexpr uint32_t TMEM_COLS = 128;
@@ -116,16 +138,218 @@ __device__ __forceinline__ bool softmax_any(bool pred)
     return r != 0;
 }
 
+// Virtual tiles charged per item for its fixed cost (about two tiles of
+// streaming: the wait for the last P.V and the write of the result).
+constexpr int KAPPA = 2;
+
+// One (sequence, kv head, split) item and its key range.
+struct Item {
+    int b, g, s;   // position in (sequence, kv head, split) order
+    int start;     // global index of its first tile
+    int pos, lo;   // attended keys [lo, pos]
+    int ub0, ub1;  // paged blocks [ub0, ub1) of this split
+    int n, T;      // blocks and 128-key tiles
+    int nsplit;    // splits of the sequence
+};
+
+// Key range of an item (the same arithmetic as the CUDA-core kernel's
+// key_range; lengths past the block table are clipped there and reported by
+// the plan kernel).
+__device__ __forceinline__ void item_geom(const DecodeParams &p, Item &it)
+{
+    int len = p.seq_lens[it.b];
+    const int cap = p.max_blocks * kBlock;
+    len = len > cap ? cap : len;
+    it.pos = len - 1;
+    it.lo = p.window > 0 ? max(0, it.pos - p.window) : 0;
+    const int blk_lo = len > 0 ? it.lo / kBlock : 0;
+    const int nblk = len > 0 ? it.pos / kBlock - blk_lo + 1 : 0;
+    it.nsplit =
+        (p.split_blocks > 0 && nblk > 0) ? (nblk + p.split_blocks - 1) / p.split_blocks : 1;
+    it.ub0 = blk_lo + it.s * p.split_blocks;
+    it.ub1 = p.split_blocks > 0 ? min(it.ub0 + p.split_blocks, blk_lo + nblk) : blk_lo + nblk;
+    it.n = max(0, it.ub1 - it.ub0);
+    it.T = (it.n + 7) / 8;
+}
+
+__device__ __forceinline__ Item item_at(const DecodeParams &p, int4 e)
+{
+    Item it;
+    it.b = e.x;
+    it.g = e.y;
+    it.s = e.z;
+    it.start = e.w;
+    it.T = 0;
+    it.nsplit = 1;
+    if (it.b < p.batch)
+        item_geom(p, it);
+    return it;
+}
+
+__device__ __forceinline__ void item_next(const DecodeParams &p, Item &it)
+{
+    it.start += it.T + KAPPA;
+    if (++it.s >= it.nsplit) {
+        it.s = 0;
+        if (++it.g >= p.num_kv_heads) {
+            it.g = 0;
+            ++it.b;
+        }
+    }
+    it.T = 0;
+    it.nsplit = 1;
+    if (it.b < p.batch)
+        item_geom(p, it);
+}
+
+// CTA c's share of the W tiles.
+__device__ __forceinline__ int tile_bound(int c, int W, int C)
+{
+    return static_cast<int>(static_cast<int64_t>(c) * W / C);
+}
+
+
 }  // namespace
 
+// ------------------------------------------------------------------ plan
+// One CTA: units per sequence (tiles + KAPPA per item, all kv heads and
+// splits), their prefix sums (workspace), and for each of the C CTAs the
+// first item it processes: the first item whose real tiles reach into its
+// units, or an empty item starting in them.  plan[0] = {W, C}; plan[1 + c] =
+// {b, g, s, first unit of that item}; plan[1 + C] = {batch, 0, 0, W}.
+__global__ void __launch_bounds__(1024) tc_plan_kernel(const DecodeParams p, int grid)
+{
+    __shared__ int wsum[32];
+    __shared__ int carry_s;
+    const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+    const int sb = p.split_blocks;
+    const int F = sb > 0 ? (sb + 7) / 8 : 0;  // tiles of a whole split
+    if (tid == 0)
+        carry_s = 0;
+    __syncthreads();
+    for (int base = 0; base < p.batch; base += 1024) {
+        const int b = base + tid;
+        int v = 0;
+        if (b < p.batch) {
+            int len = p.seq_lens[b];
+            const int cap = p.max_blocks * kBlock;
+            if (len > cap) {
+                record_error(p.err, PKV_DEV_LEN_TABLE);
+                len = cap;
+            }
+            if (len > p.max_seq_len)
+                record_error(p.err, PKV_DEV_LEN_BOUND);
+            int tiles = 0, ns = 1;
+            if (len > 0) {
+                const int pos = len - 1;
+                const int lo = p.window > 0 ? max(0, pos - p.window) : 0;
+                const int nblk = pos / kBlock - lo / kBlock + 1;
+                if (sb > 0) {
+                    const int whole = nblk / sb, rem = nblk - whole * sb;
+                    tiles = whole * F + (rem + 7) / 8;
+                    ns = whole + (rem > 0 ? 1 : 0);
+                } else {
+                    tiles = (nblk + 7) / 8;
+                }
+            }
+            v = (tiles + KAPPA * ns) * p.num_kv_heads;
+        }
+        int x = v;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int y = __shfl_up_sync(FULL_MASK, x, off);
+            if (lane >= off)
+                x += y;
+        }
+        if (lane == 31)
+            wsum[wid] = x;
+        __syncthreads();
+        if (wid == 0) {
+            int w = wsum[lane];
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const int y = __shfl_up_sync(FULL_MASK, w, off);
+                if (lane >= off)
+                    w += y;
+            }
+            wsum[lane] = w;
+        }
+        __syncthreads();
+        const int incl = x + (wid > 0 ? wsum[wid - 1] : 0);
+        const int carry = carry_s;
+        if (b < p.batch)
+            p.tc_seqoff[b] = carry + incl - v;
+        __syncthreads();
+        if (tid == 1023)
+            carry_s = carry + incl;
+        __syncthreads();
+    }
+    const int W = carry_s;  // >= KAPPA: every sequence has an item per kv head
+    if (tid == 0)
+        p.tc_seqoff[p.batch] = W;
+    __syncthreads();
+    const int C = min(grid, W);
+    if (tid == 0)
+        p.tc_plan[0] = make_int4(W, C, 0, 0);
+    const int H = p.num_kv_heads;
+    for (int c = tid; c <= C; c += 1024) {
+        int4 e;
+        if (c == C) {
+            e = make_int4(p.batch, 0, 0, W);
+        } else {
+            const int x = tile_bound(c, W, C);
+            // the sequence whose units hold x, then the item whose units hold it
+            int lo_b = 0, hi_b = p.batch;
+            while (lo_b < hi_b) {
+                const int mid = (lo_b + hi_b) >> 1;
+                if (p.tc_seqoff[mid + 1] > x)
+                    hi_b = mid;
+                else
+                    lo_b = mid + 1;
+            }
+            Item it;
+            it.b = lo_b;
+            it.g = 0;
+            it.s = 0;
+            it.start = p.tc_seqoff[lo_b];
+            item_geom(p, it);
+            const int Eg = (p.tc_seqoff[lo_b + 1] - it.start) / H;  // units per kv head
+            const int rel = x - it.start;
+            if (rel > 0) {
+                it.g = rel / Eg;
+                const int r2 = rel - it.g * Eg;
+                it.s = sb > 0 ? min(r2 / (F + KAPPA), it.nsplit - 1) : 0;
+                it.start += it.g * Eg + it.s * (F + KAPPA);
+                item_geom(p, it);
+                // x in this item's virtual tail: CTA c starts with the next item
+                if (it.start + it.T <= x && !(it.T == 0 && it.start >= x))
+                    item_next(p, it);
+            }
+            e = make_int4(it.b, it.g, it.s, it.start);
+        }
+        p.tc_plan[1 + c] = e;
+    }
+}
+
+// ------------------------------------------------------------------ decode
 template <int D, int GP>
 __global__ void __launch_bounds__(TC_THREADS, 1)
     decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmk,
-                     const __grid_constant__ CUtensorMap tmv)
+                     const __grid_constant__ CUtensorMap tmv,
+                     const __grid_constant__ CUtensorMap tmq)
 {
     constexpr int HALVES = D / 128;
+    constexpr uint32_t QB = NPAD * D * 2;  // Q^T bytes of one item
     static_assert(D == 128 || D == 256, "head_dim");
     static_assert(GP == 2 || GP == 4 || GP == 8 || GP == 16, "padded group");
+
+    const int4 hdr = p.tc_plan[0];
+    const int W = hdr.x, C = hdr.y;
+    const int c = blockIdx.x;
+    if (c >= C)
+        return;  // the whole CTA: no barrier below is reached
+    const int t0 = tile_bound(c, W, C), t1 = tile_bound(c + 1, W, C);
+    const int4 first = p.tc_plan[1 + c];
 
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
@@ -137,45 +361,25 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     uint64_t *p_full = s_full + 4;                           // [2]
     uint64_t *o_full = s_full + 6;                           // [2]
     uint64_t *o_empty = s_full + 8;                          // [2]
-    uint64_t *q_full = s_full + 10;                          // [1]
+    uint64_t *q_full = s_full + 10;                          // [2]
+    uint64_t *q_empty = s_full + 12;                         // [2]
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + 256);
     Flags flags{reinterpret_cast<volatile int *>(sm + 260)};
     float *red = reinterpret_cast<float *>(sm + 512);        // [4][16]
+    // running max per head and the last rescale factors: the same in every
+    // softmax thread, so kept once in shared memory instead of in registers
+    float *mrun_s = reinterpret_cast<float *>(sm + 768);     // [16]
+    float *alpha_s = reinterpret_cast<float *>(sm + 832);    // [16]
+    float *lse_s = reinterpret_cast<float *>(sm + 896);      // [16] an item's log-sum-exps
     uint8_t *qs = sm + CTRL;
     uint8_t *ps = sm + CTRL + QBYTES;
     uint8_t *units = sm + RING_OFF;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int split = blockIdx.x;
-    const int g = blockIdx.y;
-    const int b = blockIdx.z;
     const int G = p.group;
     const bool alias = p.alias != 0;
     const int NU = p.num_stages;
     const bool precise = p.out_f32 != 0;  // P as bf16 hi + lo: two P.V passes
-
-    int len = p.seq_lens[b];
-    const bool reporter = threadIdx.x == 0 && split == 0 && g == 0;
-    if (len > p.max_blocks * kBlock) {
-        if (reporter)
-            record_error(p.err, PKV_DEV_LEN_TABLE);
-        len = p.max_blocks * kBlock;
-    }
-    if (len > p.max_seq_len && reporter)
-        record_error(p.err, PKV_DEV_LEN_BOUND);
-    // key range and block-aligned split (as in the CUDA-core kernel)
-    const int pos = len - 1;
-    const int lo = p.window > 0 ? max(0, pos - p.window) : 0;
-    const int blk_lo = len > 0 ? lo / kBlock : 0;
-    const int nblk = len > 0 ? pos / kBlock - blk_lo + 1 : 0;
-    const int nsplit = (p.split_blocks > 0 && nblk > 0) ? (nblk + p.split_blocks - 1) / p.split_blocks : 1;
-    if (split >= nsplit)
-        return;
-    const int ub0 = blk_lo + split * p.split_blocks;
-    const int ub1 = p.split_blocks > 0 ? min(ub0 + p.split_blocks, blk_lo + nblk) : blk_lo + nblk;
-    const int n = max(0, ub1 - ub0);
-    const int T = (n + 7) / 8;  // 128-key tiles
-    const int32_t *bt_row = p.block_table + static_cast<size_t>(b) * p.max_blocks + ub0;
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < 8; ++i) {
@@ -188,41 +392,28 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             mbar_init(&p_full[i], 4);
             mbar_init(&o_full[i], 1);
             mbar_init(&o_empty[i], 4);
+            mbar_init(&q_full[i], 1);
+            mbar_init(&q_empty[i], 1);
         }
-        mbar_init(q_full, 4);
         *flags.abort = 0;
         fence_barrier_init();
     }
     if (warp == MMA_WARP)
         tmem_alloc(tmem_slot, TMEM_COLS);
-    __syncthreads();
-    tc_fence_after();
-    const uint32_t tmem = *tmem_slot;
     if (warp < 4) {
-        // Q^T (B operand of the score MMA): K-major, [D/64 columns][16 heads][64 dims].
-        // Staged while the first tiles are already in flight; the MMA thread
-        // waits on q_full.
-        for (int idx = threadIdx.x; idx < NPAD * (D / 8); idx += 128) {
-            const int h = idx / (D / 8), c8 = idx % (D / 8);
-            uint4 v = make_uint4(0u, 0u, 0u, 0u);
-            if (h < G)
-                v = *reinterpret_cast<const uint4 *>(
-                    p.q + (static_cast<size_t>(b) * p.num_q_heads + g * G + h) * D + c8 * 8);
-            const int d0 = c8 * 8;
-            *reinterpret_cast<uint4 *>(qs + (d0 / 64) * 2048 + swz(h, d0 % 64)) = v;
-        }
         // P^T buffers start at zero: padded heads stay zero for the whole kernel
         for (int idx = threadIdx.x; idx < PBYTES / 16; idx += 128)
             reinterpret_cast<uint4 *>(ps)[idx] = make_uint4(0u, 0u, 0u, 0u);
         fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0)
-            mbar_arrive(q_full);
     }
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
 
     constexpr int GL = GP < 16 ? GP : 16;  // TMEM columns read per result
-    // Unit j = tile * HALVES + half of the K stream lives in slot j % NKU,
-    // use j / NKU; of the V stream in slot VBASE + j % NVU, use j / NVU.
+    // Unit j (a 128-dim half of a 128-key tile, counted over the CTA's whole
+    // walk) of the K stream lives in slot j % NKU, use j / NKU; of the V
+    // stream in slot VBASE + j % NVU, use j / NVU.
     const int NKU = alias ? NU : NU / 2;
     const int NVU = alias ? NU : NU - NKU;
     const int VBASE = alias ? 0 : NKU;
@@ -232,75 +423,120 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         const int slot = warp - PRODUCER_WARP;  // the ring slot this warp owns
         const bool vwarp = !alias && slot >= NKU;
         const int ring = vwarp ? NVU : NKU, rbase = vwarp ? VBASE : 0;
-        if (T > 0 && slot < NU) {
+        if (slot < NU) {
             const CUtensorMap *map = vwarp ? &tmv : &tmk;
-            if (lane == 0)
+            if (lane == 0) {
                 prefetch_tensormap(map);
+                if (slot == 0)
+                    prefetch_tensormap(&tmq);
+            }
             const uint64_t pol = policy_evict_first();
-            TableCursor tc;
-            tc.init(bt_row, n, lane);
-            int last_use = -1;
+            int j = 0, kq = 0, last_use = -1, q_last = -1;
             bool stop = false;
-            for (int i = 0; i < T && !stop; ++i) {
-                int row[8];
-#pragma unroll
-                for (int t = 0; t < 8; ++t) {
-                    const int blk = i * 8 + t;
-                    const int phys = blk < n ? tc.get(blk, lane) : -1;
-                    const bool valid =
-                        static_cast<unsigned>(phys) < static_cast<unsigned>(p.num_blocks);
-                    if (blk < n && !valid && lane == 0 && slot == 0)
-                        record_error(p.err, PKV_DEV_BAD_BLOCK);
-                    // an out-of-range row: the TMA fills the box with zeros
-                    row[t] = valid ? phys * kBlock : p.num_blocks * kBlock;
-                }
-                for (int h = 0; h < HALVES; ++h) {
-                    const int j = i * HALVES + h;
-                    if (rbase + j % ring != slot)
-                        continue;
-                    const int use = j / ring;
-                    const bool room =
-                        use == 0 || wait_or_abort(&unit_empty[slot], (use - 1) & 1, flags, p.err);
-                    if (!__all_sync(FULL_MASK, room)) {
-                        stop = true;
+            Item it = item_at(p, first);
+            for (; !stop && it.b < p.batch && it.start < t1; item_next(p, it)) {
+                const int lt0 = max(0, t0 - it.start), lt1 = min(it.T, t1 - it.start);
+                if (lt1 <= lt0)
+                    continue;
+                if (slot == 0) {
+                    // Q^T of this item: 16 rows (heads g*G ...) x D dims
+                    const int qb = kq & 1;
+                    const bool room = kq < 2 ||
+                                      wait_or_abort(&q_empty[qb], ((kq >> 1) - 1) & 1, flags, p.err);
+                    if (!__all_sync(FULL_MASK, room))
                         break;
-                    }
-                    // lane 0 posts the unit's byte count, then 16 lanes issue
-                    // one 2 KB box each (block t = lane / 2, column c = lane % 2)
-                    if (lane == 0)
-                        mbar_arrive_expect_tx(&unit_full[slot], UNIT);
-                    __syncwarp();
-                    if (lane < 16) {
-                        const int t = lane >> 1, c = lane & 1;
-                        int rt = row[0];
+                    if (lane == 0) {
+                        mbar_arrive_expect_tx(&q_full[qb], QB);
 #pragma unroll
-                        for (int k = 1; k < 8; ++k)
-                            rt = (t == k) ? row[k] : rt;
-                        tma_load_3d(units + slot * UNIT + c * CHUNK + t * 2048, map,
-                                    h * 128 + c * 64, g, rt, &unit_full[slot], pol);
+                        for (int col = 0; col < D / 64; ++col)
+                            tma_load_2d(qs + qb * QBUF + col * 2048, &tmq, col * 64,
+                                        it.b * p.num_q_heads + it.g * G, &q_full[qb]);
                     }
-                    last_use = use;
+                    q_last = kq;
                 }
-                __syncwarp();
+                ++kq;
+                const int32_t *bt_row =
+                    p.block_table + static_cast<size_t>(it.b) * p.max_blocks + it.ub0 + lt0 * 8;
+                TableCursor tc;
+                tc.init(bt_row, it.n - lt0 * 8, lane);
+                for (int i = lt0; i < lt1 && !stop; ++i) {
+                    int row[8];
+#pragma unroll
+                    for (int t = 0; t < 8; ++t) {
+                        const int blk = i * 8 + t;
+                        const int phys = blk < it.n ? tc.get(blk - lt0 * 8, lane) : -1;
+                        const bool valid =
+                            static_cast<unsigned>(phys) < static_cast<unsigned>(p.num_blocks);
+                        if (blk < it.n && !valid && lane == 0 && slot == 0)
+                            record_error(p.err, PKV_DEV_BAD_BLOCK);
+                        // an out-of-range row: the TMA fills the box with zeros
+                        row[t] = valid ? phys * kBlock : p.num_blocks * kBlock;
+                    }
+                    for (int h = 0; h < HALVES; ++h) {
+                        const int jj = j++;
+                        if (rbase + jj % ring != slot)
+                            continue;
+                        const int use = jj / ring;
+                        const bool room = use == 0 ||
+                                          wait_or_abort(&unit_empty[slot], (use - 1) & 1, flags, p.err);
+                        if (!__all_sync(FULL_MASK, room)) {
+                            stop = true;
+                            break;
+                        }
+                        // lane 0 posts the unit's byte count, then 16 lanes issue
+                        // one 2 KB box each (block t = lane / 2, column c = lane % 2)
+                        if (lane == 0)
+                            mbar_arrive_expect_tx(&unit_full[slot], UNIT);
+                        __syncwarp();
+                        if (lane < 16) {
+                            const int t = lane >> 1, cc = lane & 1;
+                            int rt = row[0];
+#pragma unroll
+                            for (int k = 1; k < 8; ++k)
+                                rt = (t == k) ? row[k] : rt;
+                            tma_load_3d(units + slot * UNIT + cc * CHUNK + t * 2048, map,
+                                        h * 128 + cc * 64, it.g, rt, &unit_full[slot], pol);
+                        }
+                        last_use = use;
+                    }
+                    __syncwarp();
+                }
             }
             // Drain: do not retire with this warp's copies in flight.
-            if (lane == 0 && last_use >= 0)
-                mbar_wait(&unit_full[slot], last_use & 1, p.err, 100000000ull);
+            if (lane == 0) {
+                if (last_use >= 0)
+                    mbar_wait(&unit_full[slot], last_use & 1, p.err, 100000000ull);
+                if (q_last >= 0)
+                    mbar_wait(&q_full[q_last & 1], (q_last >> 1) & 1, p.err, 100000000ull);
+            }
         }
     } else if (warp == MMA_WARP) {
         // ------------------------------------------------------ score MMAs
-        // tile i needs its K units and a free S buffer
-        if (lane == 0 && T > 0) {
+        // tile i needs its item's Q^T, its K units and a free S buffer
+        if (lane == 0) {
             constexpr uint32_t IDESC_QK = umma_idesc_bf16(128, NPAD, false, false);
-            const uint32_t q_base = smem_u32(qs), u_base = smem_u32(units);
-            if (wait_or_abort(q_full, 0, flags, p.err)) {
-                for (int i = 0; i < T; ++i) {
-                    const int sb = i & 1;
-                    if (i >= 2 && !wait_or_abort(&s_empty[sb], ((i / 2) - 1) & 1, flags, p.err))
+            const uint32_t u_base = smem_u32(units);
+            int i_g = 0, j = 0, kq = 0;
+            bool ok = true;
+            Item it = item_at(p, first);
+            for (; ok && it.b < p.batch && it.start < t1; item_next(p, it)) {
+                const int lt0 = max(0, t0 - it.start), lt1 = min(it.T, t1 - it.start);
+                if (lt1 <= lt0)
+                    continue;
+                const int qb = kq & 1;
+                ok = wait_or_abort(&q_full[qb], (kq >> 1) & 1, flags, p.err);
+                if (!ok)
+                    break;
+                tc_fence_after();
+                const uint32_t q_base = smem_u32(qs + qb * QBUF);
+                for (int i = lt0; i < lt1 && ok; ++i, ++i_g) {
+                    const int sb = i_g & 1;
+                    if (i_g >= 2 && !wait_or_abort(&s_empty[sb], ((i_g >> 1) - 1) & 1, flags, p.err)) {
+                        ok = false;
                         break;
-                    bool ok = true;
-                    for (int h = 0; h < HALVES; ++h) {
-                        const int j = i * HALVES + h, slot = j % NKU;
+                    }
+                    for (int h = 0; h < HALVES; ++h, ++j) {
+                        const int slot = j % NKU;
                         ok = wait_or_abort(&unit_full[slot], (j / NKU) & 1, flags, p.err);
                         if (!ok)
                             break;
@@ -309,18 +545,20 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                         for (int kk = 0; kk < 8; ++kk) {
                             const uint64_t a = umma_smem_desc(
                                 u_base + slot * UNIT + (kk >> 2) * CHUNK + (kk & 3) * 32, 16, 1024);
-                            const int kq = h * 8 + kk;
-                            const uint64_t bd =
-                                umma_smem_desc(q_base + (kq >> 2) * 2048 + (kq & 3) * 32, 16, 1024);
+                            const int kqd = h * 8 + kk;
+                            const uint64_t bd = umma_smem_desc(
+                                q_base + (kqd >> 2) * 2048 + (kqd & 3) * 32, 16, 1024);
                             umma_bf16(tmem + s_col(sb), a, bd, IDESC_QK, (h | kk) != 0);
                         }
                         if (!alias)
                             umma_commit(&unit_empty[slot]);  // K unit free once read
                     }
-                    if (!ok)
-                        break;
-                    umma_commit(&s_full[sb]);
+                    if (ok)
+                        umma_commit(&s_full[sb]);
                 }
+                if (ok)
+                    umma_commit(&q_empty[qb]);  // Q^T buffer free once its MMAs are done
+                ++kq;
             }
         }
         __syncwarp();
@@ -330,32 +568,40 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         // first zeroes V rows of masked keys inside loaded blocks (only the
         // block holding the window start and the block holding pos can have
         // them), lane 0 then issues the MMAs.
-        if (T > 0) {
-            constexpr uint32_t IDESC_PV = umma_idesc_bf16(128, NPAD, true, false);
-            const uint32_t p_base = smem_u32(ps), u_base = smem_u32(units);
-            const int lo_blk = lo / kBlock, pos_blk = pos / kBlock;
-            for (int i = 0; i < T; ++i) {
-                const int sb = i & 1;
-                bool go = wait_or_abort(&p_full[sb], (i / 2) & 1, flags, p.err);
-                go = go && (i < 2 || wait_or_abort(&o_empty[sb], ((i / 2) - 1) & 1, flags, p.err));
-                if (!__all_sync(FULL_MASK, go))
+        constexpr uint32_t IDESC_PV = umma_idesc_bf16(128, NPAD, true, false);
+        const uint32_t p_base = smem_u32(ps), u_base = smem_u32(units);
+        int i_g = 0, j = 0;
+        bool ok = true;
+        Item it = item_at(p, first);
+        for (; ok && it.b < p.batch && it.start < t1; item_next(p, it)) {
+            const int lt0 = max(0, t0 - it.start), lt1 = min(it.T, t1 - it.start);
+            if (lt1 <= lt0)
+                continue;
+            const int lo_blk = it.lo / kBlock, pos_blk = it.pos / kBlock;
+            for (int i = lt0; i < lt1 && ok; ++i, ++i_g) {
+                const int sb = i_g & 1;
+                bool go = wait_or_abort(&p_full[sb], (i_g >> 1) & 1, flags, p.err);
+                go = go &&
+                     (i_g < 2 || wait_or_abort(&o_empty[sb], ((i_g >> 1) - 1) & 1, flags, p.err));
+                if (!__all_sync(FULL_MASK, go)) {
+                    ok = false;
                     break;
-                const int tb0 = ub0 + i * 8;  // first block of the tile
+                }
+                const int tb0 = it.ub0 + i * 8;  // first block of the tile
                 const int key0 = tb0 * kBlock;
                 // rows [z0a, z0b) before lo and [z1a, z1b) after pos, in this tile
                 int z0a = 0, z0b = 0, z1a = 0, z1b = 0;
-                if (lo_blk >= tb0 && lo_blk < tb0 + 8 && lo_blk < ub1 && lo > lo_blk * kBlock) {
+                if (lo_blk >= tb0 && lo_blk < tb0 + 8 && lo_blk < it.ub1 && it.lo > lo_blk * kBlock) {
                     z0a = lo_blk * kBlock - key0;
-                    z0b = lo - key0;
+                    z0b = it.lo - key0;
                 }
-                if (pos_blk >= tb0 && pos_blk < tb0 + 8 && pos_blk < ub1 &&
-                    pos < pos_blk * kBlock + kBlock - 1) {
-                    z1a = pos + 1 - key0;
+                if (pos_blk >= tb0 && pos_blk < tb0 + 8 && pos_blk < it.ub1 &&
+                    it.pos < pos_blk * kBlock + kBlock - 1) {
+                    z1a = it.pos + 1 - key0;
                     z1b = (pos_blk + 1) * kBlock - key0;
                 }
-                bool ok = true;
-                for (int h = 0; h < HALVES; ++h) {
-                    const int j = i * HALVES + h, slot = VBASE + j % NVU;
+                for (int h = 0; h < HALVES; ++h, ++j) {
+                    const int slot = VBASE + j % NVU;
                     ok = wait_or_abort(&unit_full[slot], (j / NVU) & 1, flags, p.err);
                     if (!__all_sync(FULL_MASK, ok)) {
                         ok = false;
@@ -403,21 +649,11 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         const int t = threadIdx.x;  // key row of the tile == TMEM lane
         const uint32_t lane_base = tmem + (static_cast<uint32_t>(warp * 32) << 16);
         const float qk = p.qk_scale_log2;
-        // oacc holds the running O^T relative to the current running max:
-        // after tile i-1's O^T is added it is rescaled by tile i's alpha.
-        float m_run[GP], lpart[GP];
-        float oacc[HALVES][GP];
-#pragma unroll
-        for (int h = 0; h < GP; ++h) {
-            m_run[h] = -INFINITY;
-            lpart[h] = 0.f;
-#pragma unroll
-            for (int hv = 0; hv < HALVES; ++hv)
-                oacc[hv][h] = 0.f;
-        }
+        float lpart[GP], m_run[GP];
+        float oacc[HALVES][GP];  // running O^T relative to the running max
         auto accumulate_o = [&](int k) {
             const int sb = k & 1;
-            const bool live = wait_or_abort(&o_full[sb], (k / 2) & 1, flags, p.err);
+            const bool live = wait_or_abort(&o_full[sb], (k >> 1) & 1, flags, p.err);
             tc_fence_after();
 #pragma unroll
             for (int hv = 0; hv < HALVES; ++hv) {
@@ -433,145 +669,281 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             if (lane == 0)
                 mbar_arrive(&o_empty[sb]);
         };
-        int phys_next = (t >> 4) < n ? __ldg(bt_row + (t >> 4)) : -1;
-        for (int i = 0; i < T; ++i) {
-            const int sb = i & 1;
-            const int blk = i * 8 + (t >> 4);
-            const int phys = phys_next;
-            {
-                const int nb = (i + 1) * 8 + (t >> 4);
-                phys_next = nb < n ? __ldg(bt_row + nb) : -1;
-            }
-            const bool loaded = blk < n && static_cast<unsigned>(phys) < static_cast<unsigned>(p.num_blocks);
-            const int j = (ub0 + i * 8) * kBlock + t;
-            const bool ok = loaded && j >= lo && j <= pos;
-            // ---- scores
-            const bool live = wait_or_abort(&s_full[sb], (i / 2) & 1, flags, p.err);
-            tc_fence_after();
-            float s[GL];
-            if (live)
-                ld_cols<GL>(lane_base + s_col(sb), s);
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0)
-                mbar_arrive(&s_empty[sb]);
-            float sc[GP];
-            bool big = false;
+        int i_g = 0;
+        Item it = item_at(p, first);
+        for (; it.b < p.batch && it.start < t1; item_next(p, it)) {
+            const int lt0 = max(0, t0 - it.start), lt1 = min(it.T, t1 - it.start);
+            const bool whole = lt0 == 0 && lt1 == it.T;
 #pragma unroll
             for (int h = 0; h < GP; ++h) {
-                sc[h] = (live && ok && h < G) ? s[h] * qk : -INFINITY;
-                big |= sc[h] > m_run[h] + 8.f;
-            }
-            // ---- running max: reduce only when some score exceeds it by more
-            // than 2^8 (any reference max >= the true one gives the same
-            // result; this one keeps every p <= 256)
-            float alpha[GP];
+                lpart[h] = 0.f;
+                m_run[h] = -INFINITY;
 #pragma unroll
-            for (int h = 0; h < GP; ++h)
-                alpha[h] = 1.f;
-            const bool rescale = softmax_any(big);
-            if (rescale) {
-                float mx[GP];
+                for (int hv = 0; hv < HALVES; ++hv)
+                    oacc[hv][h] = 0.f;
+            }
+            if (t < 16)
+                mrun_s[t] = -INFINITY;
+            asm volatile("bar.sync 1, 128;" ::: "memory");
+            const int32_t *bt_row = p.block_table + static_cast<size_t>(it.b) * p.max_blocks + it.ub0;
+            int phys_next = (lt0 * 8 + (t >> 4)) < it.n ? __ldg(bt_row + lt0 * 8 + (t >> 4)) : -1;
+            for (int i = lt0; i < lt1; ++i, ++i_g) {
+                const int sb = i_g & 1;
+                const int blk = i * 8 + (t >> 4);
+                const int phys = phys_next;
+                {
+                    const int nb = (i + 1) * 8 + (t >> 4);
+                    phys_next = (i + 1 < lt1 && nb < it.n) ? __ldg(bt_row + nb) : -1;
+                }
+                const bool loaded =
+                    blk < it.n && static_cast<unsigned>(phys) < static_cast<unsigned>(p.num_blocks);
+                const int jk = (it.ub0 + i * 8) * kBlock + t;
+                const bool ok = loaded && jk >= it.lo && jk <= it.pos;
+                // ---- scores
+                const bool live = wait_or_abort(&s_full[sb], (i_g >> 1) & 1, flags, p.err);
+                tc_fence_after();
+                float s[GL];
+                if (live)
+                    ld_cols<GL>(lane_base + s_col(sb), s);
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(&s_empty[sb]);
+                float sc[GP];
+                bool big = false;
 #pragma unroll
                 for (int h = 0; h < GP; ++h) {
-                    float v = sc[h];
-#pragma unroll
-                    for (int off = 16; off > 0; off >>= 1)
-                        v = fmaxf(v, __shfl_xor_sync(FULL_MASK, v, off));
-                    mx[h] = v;
+                    sc[h] = (live && ok && h < G) ? s[h] * qk : -INFINITY;
+                    big |= sc[h] > m_run[h] + 8.f;
                 }
-                if (lane == 0) {
+                // ---- running max: reduce only when some score exceeds it by more
+                // than 2^8 (any reference max >= the true one gives the same
+                // result; this one keeps every p <= 256).  softmax_any is also
+                // the barrier after which mrun_s / alpha_s may be rewritten.
+                const bool rescale = softmax_any(big);
+                if (rescale) {
+                    float mx[GP];
+#pragma unroll
+                    for (int h = 0; h < GP; ++h) {
+                        float v = sc[h];
+#pragma unroll
+                        for (int off = 16; off > 0; off >>= 1)
+                            v = fmaxf(v, __shfl_xor_sync(FULL_MASK, v, off));
+                        mx[h] = v;
+                    }
+                    if (lane == 0) {
+#pragma unroll
+                        for (int h = 0; h < GP; ++h)
+                            red[warp * 16 + h] = mx[h];
+                    }
+                    asm volatile("bar.sync 1, 128;" ::: "memory");
+                    if (t < GP) {
+                        const float tm =
+                            fmaxf(fmaxf(red[t], red[16 + t]), fmaxf(red[32 + t], red[48 + t]));
+                        const float mo = mrun_s[t];
+                        const float mn = fmaxf(mo, tm);
+                        alpha_s[t] = mn == -INFINITY ? 1.f : fast_exp2(mo - mn);
+                        mrun_s[t] = mn;
+                    }
+                    asm volatile("bar.sync 1, 128;" ::: "memory");  // red is reused
 #pragma unroll
                     for (int h = 0; h < GP; ++h)
-                        red[warp * 16 + h] = mx[h];
+                        m_run[h] = mrun_s[h];
                 }
-                asm volatile("bar.sync 1, 128;" ::: "memory");
+                // ---- probabilities, running sums, P^T (bf16, K-major, swizzled)
+                uint8_t *pb = ps + sb * 8192 + (t >> 6) * 2048;
 #pragma unroll
                 for (int h = 0; h < GP; ++h) {
-                    const float tm =
-                        fmaxf(fmaxf(red[h], red[16 + h]), fmaxf(red[32 + h], red[48 + h]));
-                    const float mn = fmaxf(m_run[h], tm);
-                    alpha[h] = mn == -INFINITY ? 1.f : fast_exp2(m_run[h] - mn);
-                    m_run[h] = mn;
+                    const float pr = sc[h] == -INFINITY ? 0.f : fast_exp2(sc[h] - m_run[h]);
+                    lpart[h] = rescale ? fmaf(lpart[h], alpha_s[h], pr) : lpart[h] + pr;
+                    const __nv_bfloat16 hi = __float2bfloat16_rn(pr);
+                    *reinterpret_cast<__nv_bfloat16 *>(pb + swz(h, t & 63)) = hi;
+                    if (precise)
+                        *reinterpret_cast<__nv_bfloat16 *>(pb + 4096 + swz(h, t & 63)) =
+                            __float2bfloat16_rn(pr - __bfloat162float(hi));
                 }
-                asm volatile("bar.sync 1, 128;" ::: "memory");  // red is reused
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(&p_full[sb]);
+                // ---- O^T of the previous tile, then rescale to this tile's max
+                if (i > lt0)
+                    accumulate_o(i_g - 1);
+                if (rescale) {
+#pragma unroll
+                    for (int h = 0; h < GP; ++h)
+#pragma unroll
+                        for (int hv = 0; hv < HALVES; ++hv)
+                            oacc[hv][h] *= alpha_s[h];
+                }
             }
-            // ---- probabilities, running sums, P^T (bf16, K-major, swizzled)
-            uint8_t *pb = ps + sb * 8192 + (t >> 6) * 2048;
+            if (lt1 > lt0)
+                accumulate_o(i_g - 1);
+
+            // ---- sums over the 128 keys of each head, then this item's result
 #pragma unroll
             for (int h = 0; h < GP; ++h) {
-                const float pr = sc[h] == -INFINITY ? 0.f : fast_exp2(sc[h] - m_run[h]);
-                lpart[h] = fmaf(lpart[h], alpha[h], pr);
-                const __nv_bfloat16 hi = __float2bfloat16_rn(pr);
-                *reinterpret_cast<__nv_bfloat16 *>(pb + swz(h, t & 63)) = hi;
-                if (precise)
-                    *reinterpret_cast<__nv_bfloat16 *>(pb + 4096 + swz(h, t & 63)) =
-                        __float2bfloat16_rn(pr - __bfloat162float(hi));
+                float v = lpart[h];
+#pragma unroll
+                for (int off = 16; off > 0; off >>= 1)
+                    v += __shfl_xor_sync(FULL_MASK, v, off);
+                lpart[h] = v;
             }
-            fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0)
-                mbar_arrive(&p_full[sb]);
-            // ---- O^T of the previous tile, then rescale to this tile's max
-            if (i >= 1)
-                accumulate_o(i - 1);
-            if (rescale) {
+            if (lane == 0) {
 #pragma unroll
                 for (int h = 0; h < GP; ++h)
-#pragma unroll
-                    for (int hv = 0; hv < HALVES; ++hv)
-                        oacc[hv][h] *= alpha[h];
+                    red[warp * 16 + h] = lpart[h];
             }
-        }
-        if (T > 0)
-            accumulate_o(T - 1);
-
-        // ---- final sums over the 128 keys of each head, then the output
+            asm volatile("bar.sync 1, 128;" ::: "memory");
+            // whole item: the output when the sequence has one split, else the
+            // split's partial; a piece of an item: this CTA's partial state.
+            // The G x D results are staged in the P^T buffers (idle between an
+            // item's last P.V and the next item's first P) and leave in TMA
+            // bulk stores: plain stores of 128 lines per item queue behind the
+            // ring's HBM traffic for several microseconds.
+            const bool single = whole && it.nsplit == 1;
+            const bool f32 = !single || p.out_f32;
+            const int slot = lt0 > 0 ? 0 : 1;  // cut at its start: this CTA's first item
 #pragma unroll
-        for (int h = 0; h < GP; ++h) {
-            float v = lpart[h];
+            for (int h = 0; h < GP; ++h) {
+                if (h >= G)
+                    continue;
+                const float L = (red[h] + red[16 + h]) + (red[32 + h] + red[48 + h]);
+                const float inv = L > 0.f ? 1.f / L : 0.f;
 #pragma unroll
-            for (int off = 16; off > 0; off >>= 1)
-                v += __shfl_xor_sync(FULL_MASK, v, off);
-            lpart[h] = v;
-        }
-        if (lane == 0) {
-#pragma unroll
-            for (int h = 0; h < GP; ++h)
-                red[warp * 16 + h] = lpart[h];
-        }
-        asm volatile("bar.sync 1, 128;" ::: "memory");
-        const bool single = nsplit == 1;
-#pragma unroll
-        for (int h = 0; h < GP; ++h) {
-            if (h >= G)
-                continue;
-            const float L = (red[h] + red[16 + h]) + (red[32 + h] + red[48 + h]);
-            const float inv = L > 0.f ? 1.f / L : 0.f;
-            const size_t orow = static_cast<size_t>(b) * p.num_q_heads + g * G + h;
-#pragma unroll
-            for (int hv = 0; hv < HALVES; ++hv) {
-                const int d = hv * 128 + t;
-                const float y = oacc[hv][h] * inv;
-                if (single) {
-                    if (p.out_f32)
-                        reinterpret_cast<float *>(p.out)[orow * D + d] = y;
+                for (int hv = 0; hv < HALVES; ++hv) {
+                    const int d = hv * 128 + t;
+                    const float y = oacc[hv][h] * inv;
+                    if (f32)
+                        reinterpret_cast<float *>(ps)[h * D + d] = y;
                     else
-                        reinterpret_cast<__nv_bfloat16 *>(p.out)[orow * D + d] = __float2bfloat16_rn(y);
-                } else {
-                    p.part_o[(orow * p.num_splits + split) * D + d] = y;
+                        reinterpret_cast<__nv_bfloat16 *>(ps)[h * D + d] = __float2bfloat16_rn(y);
                 }
+                if (t == h)
+                    lse_s[h] = L > 0.f ? (mrun_s[h] + log2f(L)) * LN2 : -INFINITY;
             }
-            if (!single && t == 0)
-                p.part_lse[orow * p.num_splits + split] =
-                    L > 0.f ? (m_run[h] + log2f(L)) * LN2 : -INFINITY;
+            fence_proxy_async_smem();
+            asm volatile("bar.sync 1, 128;" ::: "memory");
+            // a whole split's partial with a group that is not a multiple of
+            // four heads: its log-sum-exps are not a 16-byte run
+            const bool lse_scalar = whole && !single && (G & 3) != 0;
+            if (lse_scalar && t < G) {
+                const size_t prow = (static_cast<size_t>(it.b) * p.num_splits + it.s) * p.num_q_heads;
+                p.part_lse[prow + it.g * G + t] = lse_s[t];
+            }
+            if (t == 0) {
+                if (single) {
+                    const size_t row0 = static_cast<size_t>(it.b) * p.num_q_heads + it.g * G;
+                    const uint32_t es = p.out_f32 ? 4u : 2u;
+                    bulk_store(static_cast<uint8_t *>(p.out) + row0 * D * es, ps, G * D * es);
+                } else if (!whole) {
+                    const size_t srow = (static_cast<size_t>(c) * 2 + slot) * NPAD;
+                    bulk_store(p.sub_o + srow * D, ps, G * D * 4u);
+                    bulk_store(p.sub_lse + srow, lse_s, NPAD * 4u);
+                } else {
+                    // split-major partials: the group's G rows of split s are one run
+                    const size_t prow =
+                        (static_cast<size_t>(it.b) * p.num_splits + it.s) * p.num_q_heads + it.g * G;
+                    bulk_store(p.part_o + prow * D, ps, G * D * 4u);
+                    if (!lse_scalar)
+                        bulk_store(p.part_lse + prow, lse_s, G * 4u);
+                }
+                bulk_commit();
+                bulk_wait_read();
+            }
+            asm volatile("bar.sync 1, 128;" ::: "memory");  // staging read; red reusable
+            if constexpr (GP < 16) {
+                // P^T rows past the padded group must read as zero again
+                for (int idx = t; idx < PBYTES / 16; idx += 128)
+                    reinterpret_cast<uint4 *>(ps)[idx] = make_uint4(0u, 0u, 0u, 0u);
+            }
         }
+        if (t == 0)
+            bulk_wait_all();  // no bulk store outlives the kernel
     }
 
     __syncthreads();
     if (warp == MMA_WARP) {
         tc_fence_after();
         tmem_dealloc(tmem, TMEM_COLS);
+    }
+}
+
+// ------------------------------------------------------------------ fix-up
+// For each CTA boundary c that cuts an item and is that item's last cut, the
+// item's partial states (CTA ca's second slot, CTAs ca+1..c's first slot)
+// are merged by log-sum-exp into its result: the output, or the split's
+// partial state for the split-KV combine.
+constexpr int FIXUP_THREADS = 1024;
+
+__global__ void __launch_bounds__(FIXUP_THREADS) tc_fixup_kernel(const DecodeParams p)
+{
+    __shared__ float w_s[NPAD][kTcMaxGrid];  // weight of part k for head h
+    __shared__ float inv_s[NPAD], lse_s[NPAD];
+    const int4 hdr = p.tc_plan[0];
+    const int W = hdr.x, C = hdr.y;
+    const int c = blockIdx.x;
+    if (c == 0 || c >= C)
+        return;
+    const int t0 = tile_bound(c, W, C), t1 = tile_bound(c + 1, W, C);
+    const Item it = item_at(p, p.tc_plan[1 + c]);
+    if (it.b >= p.batch || !(it.start < t0 && t0 < it.start + it.T))
+        return;  // no item's real tiles are cut at this boundary
+    if (c < C - 1 && it.start + it.T > t1)
+        return;  // a later boundary cuts it too and merges it
+    int ca = c - 1;  // the CTA holding the item's first tile
+    while (ca > 0 && tile_bound(ca, W, C) > it.start)
+        --ca;
+    const int nparts = c - ca + 1;
+    const int D = p.head_dim, G = p.group;
+    // part k = CTA ca + k: its second slot for k = 0 (the item ends its
+    // range), its first slot otherwise (the item starts its range)
+    auto part = [&](int k) { return (static_cast<size_t>(ca + k) * 2 + (k == 0 ? 1 : 0)) * NPAD; };
+    if (threadIdx.x < G) {
+        const int h = threadIdx.x;
+        float M = -INFINITY;
+        for (int k = 0; k < nparts; ++k)
+            M = fmaxf(M, p.sub_lse[part(k) + h]);
+        float Z = 0.f;
+        for (int k = 0; k < nparts; ++k) {
+            const float l = p.sub_lse[part(k) + h];
+            const float w = (M == -INFINITY || l == -INFINITY) ? 0.f : expf(l - M);
+            w_s[h][k] = w;
+            Z += w;
+        }
+        inv_s[h] = Z > 0.f ? 1.f / Z : 0.f;
+        lse_s[h] = Z > 0.f ? M + logf(Z) : -INFINITY;
+    }
+    __syncthreads();
+    const bool single = it.nsplit == 1;
+    for (int idx = threadIdx.x; idx < G * D; idx += blockDim.x) {
+        const int h = idx / D, d = idx - h * D;
+        float acc = 0.f;
+        for (int k0 = 0; k0 < nparts; k0 += 8) {
+            // eight independent loads in flight, then their weighted sum
+            float v[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+                v[j] = k0 + j < nparts ? p.sub_o[(part(k0 + j) + h) * D + d] : 0.f;
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+                if (k0 + j < nparts && w_s[h][k0 + j] != 0.f)
+                    acc = fmaf(w_s[h][k0 + j], v[j], acc);
+        }
+        const float y = acc * inv_s[h];
+        const size_t orow = static_cast<size_t>(it.b) * p.num_q_heads + it.g * G + h;
+        if (single) {
+            if (p.out_f32)
+                reinterpret_cast<float *>(p.out)[orow * D + d] = y;
+            else
+                reinterpret_cast<__nv_bfloat16 *>(p.out)[orow * D + d] = __float2bfloat16_rn(y);
+        } else {
+            const size_t prow =
+                (static_cast<size_t>(it.b) * p.num_splits + it.s) * p.num_q_heads + it.g * G + h;
+            p.part_o[prow * D + d] = y;
+            if (d == 0)
+                p.part_lse[prow] = lse_s[h];
+        }
     }
 }
 
@@ -583,47 +955,94 @@ int decode_tc_group_pad(int group)
     return group <= 2 ? 2 : group <= 4 ? 4 : group <= 8 ? 8 : group <= 16 ? 16 : 0;
 }
 
+size_t decode_tc_scratch_bytes(int batch, int head_dim)
+{
+    auto up = [](size_t x) { return (x + 255) / 256 * 256; };
+    return up(sizeof(int4) * (2 + kTcMaxGrid)) + up(sizeof(int) * (static_cast<size_t>(batch) + 1)) +
+           up(sizeof(float) * kTcMaxGrid * 2 * NPAD) +
+           sizeof(float) * kTcMaxGrid * 2 * NPAD * static_cast<size_t>(head_dim);
+}
+
+void decode_tc_bind_scratch(DecodeParams &p, void *scratch, int batch)
+{
+    auto up = [](size_t x) { return (x + 255) / 256 * 256; };
+    char *s = static_cast<char *>(scratch);
+    p.tc_plan = reinterpret_cast<int4 *>(s);
+    s += up(sizeof(int4) * (2 + kTcMaxGrid));
+    p.tc_seqoff = reinterpret_cast<int *>(s);
+    s += up(sizeof(int) * (static_cast<size_t>(batch) + 1));
+    p.sub_lse = reinterpret_cast<float *>(s);
+    s += up(sizeof(float) * kTcMaxGrid * 2 * NPAD);
+    p.sub_o = reinterpret_cast<float *>(s);
+}
+
+int decode_tc_grid()
+{
+    static std::atomic<int> cached{0};
+    int v = cached.load(std::memory_order_relaxed);
+    if (v)
+        return v;
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0)
+        sms = 1;
+    v = sms < kTcMaxGrid ? sms : kTcMaxGrid;
+    cached.store(v, std::memory_order_relaxed);
+    return v;
+}
+
 template <int D, int GP>
 static cudaError_t launch_tc_one(const DecodeParams &p, const CUtensorMap &tmk,
-                                 const CUtensorMap &tmv, cudaStream_t s)
+                                 const CUtensorMap &tmv, const CUtensorMap &tmq, int grid,
+                                 cudaStream_t s)
 {
     const size_t smem = decode_tc_smem_bytes(p.num_stages);
     auto kern = decode_tc_kernel<D, GP>;
-    static int configured = 0;
-    if (static_cast<int>(smem) > configured) {
+    static std::atomic<int> configured{0};
+    if (static_cast<int>(smem) > configured.load(std::memory_order_relaxed)) {
         cudaError_t e =
             cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess)
             return e;
-        configured = static_cast<int>(smem);
+        configured.store(static_cast<int>(smem), std::memory_order_relaxed);
     }
-    dim3 grid(p.num_splits, p.num_kv_heads, p.batch);
-    kern<<<grid, TC_THREADS, smem, s>>>(p, tmk, tmv);
+    kern<<<grid, TC_THREADS, smem, s>>>(p, tmk, tmv, tmq);
     return cudaGetLastError();
 }
 
 template <int D>
 static cudaError_t launch_tc_d(const DecodeParams &p, const CUtensorMap &tmk,
-                               const CUtensorMap &tmv, int gp, cudaStream_t s)
+                               const CUtensorMap &tmv, const CUtensorMap &tmq, int gp, int grid,
+                               cudaStream_t s)
 {
     switch (gp) {
-    case 2: return launch_tc_one<D, 2>(p, tmk, tmv, s);
-    case 4: return launch_tc_one<D, 4>(p, tmk, tmv, s);
-    case 8: return launch_tc_one<D, 8>(p, tmk, tmv, s);
-    case 16: return launch_tc_one<D, 16>(p, tmk, tmv, s);
+    case 2: return launch_tc_one<D, 2>(p, tmk, tmv, tmq, grid, s);
+    case 4: return launch_tc_one<D, 4>(p, tmk, tmv, tmq, grid, s);
+    case 8: return launch_tc_one<D, 8>(p, tmk, tmv, tmq, grid, s);
+    case 16: return launch_tc_one<D, 16>(p, tmk, tmv, tmq, grid, s);
     default: return cudaErrorInvalidValue;
     }
 }
 
-cudaError_t launch_decode_tc(const DecodeParams &p, const CUtensorMap &tmk,
-                             const CUtensorMap &tmv, int head_dim, cudaStream_t s)
+cudaError_t launch_decode_tc(const DecodeParams &p, const CUtensorMap &tmk, const CUtensorMap &tmv,
+                             const CUtensorMap &tmq, int head_dim, cudaStream_t s)
 {
     const int gp = decode_tc_group_pad(p.group);
+    const int grid = decode_tc_grid();
+    tc_plan_kernel<<<1, 1024, 0, s>>>(p, grid);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess)
+        return e;
     if (head_dim == 128)
-        return launch_tc_d<128>(p, tmk, tmv, gp, s);
-    if (head_dim == 256)
-        return launch_tc_d<256>(p, tmk, tmv, gp, s);
-    return cudaErrorInvalidValue;
+        e = launch_tc_d<128>(p, tmk, tmv, tmq, gp, grid, s);
+    else if (head_dim == 256)
+        e = launch_tc_d<256>(p, tmk, tmv, tmq, gp, grid, s);
+    else
+        e = cudaErrorInvalidValue;
+    if (e != cudaSuccess)
+        return e;
+    tc_fixup_kernel<<<grid, FIXUP_THREADS, 0, s>>>(p);
+    return cudaGetLastError();
 }
 
 }  // namespace pkv

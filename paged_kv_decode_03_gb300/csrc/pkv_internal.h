@@ -19,8 +19,8 @@ struct DecodeParams {
     const int32_t *seq_lens;
     const float *k_scale;
     const float *v_scale;
-    float *part_lse;          // [B][H_q][num_splits]
-    float *part_o;            // [B][H_q][num_splits][D]
+    float *part_lse;          // [B][num_splits][H_q]
+    float *part_o;            // [B][num_splits][H_q][D]
     void *out;                // [B][H_q][D]
     int32_t max_blocks;       // block_table row length
     int32_t scale_mode;
@@ -39,6 +39,12 @@ struct DecodeParams {
     int32_t num_stages;       // smem ring depth
     float qk_scale_log2;      // softmax_scale * log2(e)
     unsigned int *err;        // device error word
+    int32_t head_dim;
+    // tensor-core kernel only (workspace): stream-K plan and partial states
+    int4 *tc_plan;            // [0] = {W, C}; [1 + c] = CTA c's first item; [1 + C] = end
+    int32_t *tc_seqoff;       // [batch + 1] first tile of each sequence
+    float *sub_lse;           // [grid][2][16] partial states of items cut at CTA boundaries
+    float *sub_o;             // [grid][2][16][head_dim]
 };
 
 struct AppendParams {
@@ -59,8 +65,8 @@ struct AppendParams {
 };
 
 struct CombineParams {
-    const float *part_lse;
-    const float *part_o;
+    const float *part_lse;    // [B][num_splits][H_q]
+    const float *part_o;      // [B][num_splits][H_q][D]
     const int32_t *seq_lens;
     void *out;
     int32_t batch;
@@ -83,11 +89,19 @@ cudaError_t launch_decode(const DecodeParams &p, const CUtensorMap &tmk, const C
 cudaError_t launch_combine(const CombineParams &p, cudaStream_t s);
 
 // Tensor-core decode kernel (bf16 pools, head_dim 128/256, group <= 16):
-// one CTA per (split, kv head, sequence); num_stages = ring units of 32 KB.
+// persistent stream-K over the 128-key tiles of all (sequence, kv head,
+// split) items, one CTA per SM (at most kTcMaxGrid); num_stages = ring units
+// of 32 KB.  Launches the plan, decode and fix-up kernels; needs
+// decode_tc_scratch_bytes of workspace bound with decode_tc_bind_scratch.
+constexpr int kTcMaxGrid = 256;
 int decode_tc_group_pad(int group);  // 0 if the group is too large
 size_t decode_tc_smem_bytes(int num_units);
+size_t decode_tc_scratch_bytes(int batch, int head_dim);
+void decode_tc_bind_scratch(DecodeParams &p, void *scratch, int batch);
+int decode_tc_grid();
 cudaError_t launch_decode_tc(const DecodeParams &p, const CUtensorMap &tmk,
-                             const CUtensorMap &tmv, int head_dim, cudaStream_t s);
+                             const CUtensorMap &tmv, const CUtensorMap &tmq, int head_dim,
+                             cudaStream_t s);
 cudaError_t launch_append(const AppendParams &p, int int8, cudaStream_t s);
 
 }  // namespace pkv

@@ -122,10 +122,23 @@ def test_split_geometry(lib):
 
 def test_workspace_bytes(lib):
     wb = lib.paged_decode_workspace_bytes
-    assert wb(32, 16, 1, 256, 16, 32768, 0, 0) == 0
+    pwb = lib.paged_decode_partial_workspace_bytes
+    up = lambda x: (x + 255) // 256 * 256
+    # CUDA-core shapes (group < 8): split partials only
+    assert wb(32, 16, 8, 256, 16, 32768, 0, 0) == 0
+    assert pwb(32, 16, 8, 256) == 0
     rows = 32 * 16 * 32
-    lse = (rows * 4 + 255) // 256 * 256
-    assert wb(32, 16, 1, 256, 16, 32768, 0, 1024) == lse + rows * 256 * 4
+    split_bytes = up(rows * 4) + rows * 256 * 4
+    assert wb(32, 16, 8, 256, 16, 32768, 0, 1024) == split_bytes
+    # tensor-core shapes (group 8..16, head_dim 128/256): the stream-K scratch
+    # (plan of up to 256 CTAs, per-sequence prefix, two partial states per CTA)
+    grid, npad = 256, 16
+    tc = up(16 * (2 + grid)) + up(4 * (32 + 1)) + up(4 * grid * 2 * npad) + 4 * grid * 2 * npad * 256
+    assert pwb(32, 16, 1, 256) == tc
+    assert wb(32, 16, 1, 256, 16, 32768, 0, 0) == tc
+    assert wb(32, 16, 1, 256, 16, 32768, 0, 1024) == max(split_bytes, tc)
+    assert pwb(32, 16, 1, 64) == 0      # head_dim 64 runs on CUDA cores
+    assert pwb(32, 64, 1, 128) == 0     # groups above 16 too
 
 
 def test_binding_refuses_host_tensors():

@@ -146,8 +146,8 @@ def test_split_partial_matches_oracle_partials():
     split = 256
     ns = pkv.paged_decode_num_splits(step.max_seq_len, spec.window, split)
     B, Hq, D = w.q.shape
-    lse = torch.full((B, Hq, ns), float("nan"), device="cuda")
-    po = torch.full((B, Hq, ns, D), float("nan"), device="cuda")
+    lse = torch.full((B, ns, Hq), float("nan"), device="cuda")      # split-major
+    po = torch.full((B, ns, Hq, D), float("nan"), device="cuda")
     out = torch.zeros((B, Hq, D), dtype=torch.float32, device="cuda")
     pkv.paged_decode_split_partial(step.q, gp, step.block_table, step.seq_lens, spec.window,
                                    np.float32(spec.softmax_scale), split, lse, po, out,
@@ -170,13 +170,118 @@ def test_split_partial_matches_oracle_partials():
             ol, oo = oracle.partial(w.q, op, w.block_table, w.seq_lens, Hq, spec.window,
                                     np.float32(spec.softmax_scale),
                                     np.full(B, kb), np.full(B, ke))
-            np.testing.assert_allclose(lse_h[b, :, s], ol[b], rtol=0, atol=2e-5)
-            assert _gpu.max_row_rel_err(po_h[b, :, s].astype(np.float64), oo[b]) <= F32_REL_TOL
+            np.testing.assert_allclose(lse_h[b, s], ol[b], rtol=0, atol=2e-5)
+            assert _gpu.max_row_rel_err(po_h[b, s].astype(np.float64), oo[b]) <= F32_REL_TOL
     # the combine step on these partials gives the full decode
     out2 = out.clone()
     pkv.paged_decode_lse_combine(lse, po, step.seq_lens, spec.window, split, out2)
     torch.cuda.synchronize()
     assert _gpu.max_row_rel_err(out2.cpu().numpy().astype(np.float64), full) <= F32_REL_TOL
+
+
+@pytest.mark.parametrize("hq,hkv,D,alias", [(16, 1, 256, True), (16, 2, 128, False)])
+def test_tc_split_partial_matches_oracle_partials(hq, hkv, D, alias):
+    """On the tensor-core kernel the split partials come from the stream-K
+    walk: splits cut between SMs are merged by the fix-up kernel before they
+    are written.  Each split's log-sum-exp and normalised output must match
+    the oracle's partial of the same keys."""
+    spec = synth.Spec(f"tc_split_{hq}_{hkv}_{D}", batch=7, num_q_heads=hq, num_kv_heads=hkv,
+                      head_dim=D, lens=("fixed", (0, 5, 300, 2100, 4500, 64, 9000)), alias=alias,
+                      seed=21 + D)
+    w = synth.make_workload(spec)
+    gp = _gpu.device_pool(w)
+    _gpu.append_all(w, gp)
+    op = _util.oracle_pool(w)
+    step = _gpu.DeviceStep(w)
+    split = 512
+    ns = pkv.paged_decode_num_splits(step.max_seq_len, spec.window, split)
+    B, Hq, _ = w.q.shape
+    lse = torch.full((B, ns, Hq), float("nan"), device="cuda")      # split-major
+    po = torch.full((B, ns, Hq, D), float("nan"), device="cuda")
+    out = torch.zeros((B, Hq, D), dtype=torch.float32, device="cuda")
+    pkv.paged_decode_split_partial(step.q, gp, step.block_table, step.seq_lens, spec.window,
+                                   np.float32(spec.softmax_scale), split, lse, po, out,
+                                   step.max_seq_len)
+    torch.cuda.synchronize()
+    lse_h, po_h, out_h = lse.cpu().numpy(), po.cpu().numpy(), out.cpu().numpy()
+    full = _util.oracle_decode(w, op)
+    for b in range(B):
+        L = int(w.seq_lens[b])
+        nblk = (L - 1) // 16 + 1 if L > 0 else 0
+        nsb = max(1, -(-nblk // (split // 16)))
+        if nsb == 1:
+            assert _gpu.max_row_rel_err(out_h[b].astype(np.float64), full[b]) <= F32_REL_TOL
+            continue
+        for s_ in range(nsb):
+            kb = s_ * split
+            ol, oo = oracle.partial(w.q, op, w.block_table, w.seq_lens, Hq, spec.window,
+                                    np.float32(spec.softmax_scale),
+                                    np.full(B, kb), np.full(B, kb + split))
+            np.testing.assert_allclose(lse_h[b, s_], ol[b], rtol=0, atol=2e-5)
+            assert _gpu.max_row_rel_err(po_h[b, s_].astype(np.float64), oo[b]) <= F32_REL_TOL
+    out2 = out.clone()
+    pkv.paged_decode_lse_combine(lse, po, step.seq_lens, spec.window, split, out2)
+    torch.cuda.synchronize()
+    assert _gpu.max_row_rel_err(out2.cpu().numpy().astype(np.float64), full) <= F32_REL_TOL
+    assert pkv.device_status(clear=True) == 0
+
+
+@pytest.mark.parametrize("lens", [
+    (0, 1, 20000, 0, 3, 129, 128),        # one range cut by many SM boundaries, empty rows
+    (1, 17, 130),                          # fewer tiles than SMs: one tile per CTA
+    (0, 0, 0),                             # nothing to read at all
+    tuple(range(1, 4000, 97)),             # many short ranges, some cut
+])
+def test_tc_stream_k_partition(lens):
+    """The stream-K walk of the tensor-core kernel: any mix of lengths splits
+    into equal tile shares per SM; ranges cut between SMs are merged by the
+    fix-up kernel."""
+    spec = synth.Spec(f"tc_sk_{len(lens)}_{max(lens)}", batch=len(lens), num_q_heads=16,
+                      num_kv_heads=1, head_dim=256, lens=("fixed", lens), alias=True,
+                      seed=5 + len(lens))
+    _run_case(spec, splits=(0,))
+
+
+def test_tc_stream_k_gqa8_window():
+    spec = synth.Spec("tc_sk_gqa8", batch=11, num_q_heads=32, num_kv_heads=4, head_dim=128,
+                      lens=("fixed", (3000, 1, 0, 700, 1025, 1026, 2048, 16, 5000, 333, 64)),
+                      window=1024, seed=44)
+    _run_case(spec, splits=(0,))
+
+
+def test_tc_graph_capture():
+    """The tensor-core path (plan, persistent decode and fix-up kernels)
+    captures into a CUDA graph and replays."""
+    spec = synth.shrink(synth.C3, batch=5, lens=("uniform", 1, 6000))
+    w = synth.make_workload(spec)
+    gp = _gpu.device_pool(w)
+    _gpu.append_all(w, gp, new=False)
+    op = _util.oracle_pool(w)
+    step = _gpu.DeviceStep(w)
+    k_new, slots = _gpu.to_dev_bits(w.new_k), _gpu.to_dev(w.new_slots)
+    B, Hq, D = w.q.shape
+    out = torch.empty((B, Hq, D), dtype=torch.bfloat16, device="cuda")
+    ws = torch.empty(max(1, pkv.paged_decode_workspace_bytes(B, Hq, spec.num_kv_heads, D,
+                                                             step.max_seq_len, spec.window)),
+                     dtype=torch.uint8, device="cuda")
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        pkv.paged_kv_append(k_new, None, slots, gp)
+        pkv.paged_decode_attention(step.q, gp, step.block_table, step.seq_lens, spec.window,
+                                   spec.softmax_scale, out, step.max_seq_len, workspace=ws)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        pkv.paged_kv_append(k_new, None, slots, gp)
+        pkv.paged_decode_attention(step.q, gp, step.block_table, step.seq_lens, spec.window,
+                                   spec.softmax_scale, out, step.max_seq_len, workspace=ws)
+    out.zero_()
+    g.replay()
+    torch.cuda.synchronize()
+    oracle.append(w.new_k, None, w.new_slots, op)
+    ref = _util.oracle_decode(w, op)
+    assert _gpu.max_abs_err(_gpu.out_to_f64(out), ref) <= BF16_TOL
+    assert pkv.device_status(clear=True) == 0
 
 
 def test_lse_combine_on_given_partials():
@@ -188,7 +293,10 @@ def test_lse_combine_on_given_partials():
     po = rng.normal(size=(B, Hq, ns, D)).astype(np.float32)
     lse[0, :, 3] = np.nan  # beyond sequence 0's splits: must be ignored
     out = torch.zeros((B, Hq, D), dtype=torch.float32, device="cuda")
-    pkv.paged_decode_lse_combine(_gpu.to_dev(lse), _gpu.to_dev(po), _gpu.to_dev(lens), 0, 64, out)
+    # the library's partials are split-major: [B][splits][H_q](, D)
+    lse_d = _gpu.to_dev(np.ascontiguousarray(lse.transpose(0, 2, 1)))
+    po_d = _gpu.to_dev(np.ascontiguousarray(po.transpose(0, 2, 1, 3)))
+    pkv.paged_decode_lse_combine(lse_d, po_d, _gpu.to_dev(lens), 0, 64, out)
     torch.cuda.synchronize()
     got = out.cpu().numpy()
     for b, nsb in enumerate((3, 4, 2)):
