@@ -217,10 +217,16 @@ __device__ __forceinline__ int tile_bound(int c, int W, int C)
 // first item it processes: the first item whose real tiles reach into its
 // units, or an empty item starting in them.  plan[0] = {W, C}; plan[1 + c] =
 // {b, g, s, first unit of that item}; plan[1 + C] = {batch, 0, 0, W}.
+constexpr int PLAN_SMEM_SEQS = 8192;  // prefix sums kept in shared memory up to this batch
+
 __global__ void __launch_bounds__(1024) tc_plan_kernel(const DecodeParams p, int grid)
 {
     __shared__ int wsum[32];
     __shared__ int carry_s;
+    __shared__ int soff_s[PLAN_SMEM_SEQS + 1];
+    const bool in_smem = p.batch <= PLAN_SMEM_SEQS;
+    int *soff = in_smem ? soff_s : p.tc_seqoff;
+    pdl_launch_dependents();  // the decode kernel's prologue may start now
     const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
     const int sb = p.split_blocks;
     const int F = sb > 0 ? (sb + 7) / 8 : 0;  // tiles of a whole split
@@ -278,7 +284,7 @@ __global__ void __launch_bounds__(1024) tc_plan_kernel(const DecodeParams p, int
         const int incl = x + (wid > 0 ? wsum[wid - 1] : 0);
         const int carry = carry_s;
         if (b < p.batch)
-            p.tc_seqoff[b] = carry + incl - v;
+            soff[b] = carry + incl - v;
         __syncthreads();
         if (tid == 1023)
             carry_s = carry + incl;
@@ -286,7 +292,7 @@ __global__ void __launch_bounds__(1024) tc_plan_kernel(const DecodeParams p, int
     }
     const int W = carry_s;  // >= KAPPA: every sequence has an item per kv head
     if (tid == 0)
-        p.tc_seqoff[p.batch] = W;
+        soff[p.batch] = W;
     __syncthreads();
     const int C = min(grid, W);
     if (tid == 0)
@@ -302,7 +308,7 @@ __global__ void __launch_bounds__(1024) tc_plan_kernel(const DecodeParams p, int
             int lo_b = 0, hi_b = p.batch;
             while (lo_b < hi_b) {
                 const int mid = (lo_b + hi_b) >> 1;
-                if (p.tc_seqoff[mid + 1] > x)
+                if (soff[mid + 1] > x)
                     hi_b = mid;
                 else
                     lo_b = mid + 1;
@@ -311,9 +317,9 @@ __global__ void __launch_bounds__(1024) tc_plan_kernel(const DecodeParams p, int
             it.b = lo_b;
             it.g = 0;
             it.s = 0;
-            it.start = p.tc_seqoff[lo_b];
+            it.start = soff[lo_b];
             item_geom(p, it);
-            const int Eg = (p.tc_seqoff[lo_b + 1] - it.start) / H;  // units per kv head
+            const int Eg = (soff[lo_b + 1] - it.start) / H;  // units per kv head
             const int rel = x - it.start;
             if (rel > 0) {
                 it.g = rel / Eg;
@@ -342,14 +348,6 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     constexpr uint32_t QB = NPAD * D * 2;  // Q^T bytes of one item
     static_assert(D == 128 || D == 256, "head_dim");
     static_assert(GP == 2 || GP == 4 || GP == 8 || GP == 16, "padded group");
-
-    const int4 hdr = p.tc_plan[0];
-    const int W = hdr.x, C = hdr.y;
-    const int c = blockIdx.x;
-    if (c >= C)
-        return;  // the whole CTA: no barrier below is reached
-    const int t0 = tile_bound(c, W, C), t1 = tile_bound(c + 1, W, C);
-    const int4 first = p.tc_plan[1 + c];
 
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
@@ -409,6 +407,17 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+
+    // The set-up above overlaps the plan kernel (programmatic dependent
+    // launch); the plan is read once that kernel has completed.
+    pdl_wait();
+    pdl_launch_dependents();  // the fix-up kernel may be scheduled as SMs free up
+    const int4 hdr = p.tc_plan[0];
+    const int W = hdr.x, C = hdr.y;
+    const int c = blockIdx.x;
+    const bool active = c < C;  // CTAs past C only release their TMEM
+    const int t0 = active ? tile_bound(c, W, C) : 0, t1 = active ? tile_bound(c + 1, W, C) : 0;
+    const int4 first = active ? p.tc_plan[1 + c] : make_int4(p.batch, 0, 0, 0);
 
     constexpr int GL = GP < 16 ? GP : 16;  // TMEM columns read per result
     // Unit j (a 128-dim half of a 128-key tile, counted over the CTA's whole
@@ -875,11 +884,13 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
 // are merged by log-sum-exp into its result: the output, or the split's
 // partial state for the split-KV combine.
 constexpr int FIXUP_THREADS = 1024;
+constexpr int FIXUP_CTAS = (NPAD * 256) / FIXUP_THREADS;  // CTAs per boundary: G*D <= 16*256
 
 __global__ void __launch_bounds__(FIXUP_THREADS) tc_fixup_kernel(const DecodeParams p)
 {
-    __shared__ float w_s[NPAD][kTcMaxGrid];  // weight of part k for head h
+    __shared__ float w_s[NPAD][kTcMaxGrid];  // log-sum-exp, then weight, of part k for head h
     __shared__ float inv_s[NPAD], lse_s[NPAD];
+    pdl_wait();  // the decode kernel's partial states are complete and visible
     const int4 hdr = p.tc_plan[0];
     const int W = hdr.x, C = hdr.y;
     const int c = blockIdx.x;
@@ -899,14 +910,21 @@ __global__ void __launch_bounds__(FIXUP_THREADS) tc_fixup_kernel(const DecodePar
     // part k = CTA ca + k: its second slot for k = 0 (the item ends its
     // range), its first slot otherwise (the item starts its range)
     auto part = [&](int k) { return (static_cast<size_t>(ca + k) * 2 + (k == 0 ? 1 : 0)) * NPAD; };
+    // every part's log-sum-exp loaded at once (one thread each), then the
+    // weights per head from shared memory
+    for (int idx = threadIdx.x; idx < nparts * NPAD; idx += blockDim.x) {
+        const int k = idx / NPAD, h = idx - k * NPAD;
+        w_s[h][k] = h < G ? p.sub_lse[part(k) + h] : -INFINITY;
+    }
+    __syncthreads();
     if (threadIdx.x < G) {
         const int h = threadIdx.x;
         float M = -INFINITY;
         for (int k = 0; k < nparts; ++k)
-            M = fmaxf(M, p.sub_lse[part(k) + h]);
+            M = fmaxf(M, w_s[h][k]);
         float Z = 0.f;
         for (int k = 0; k < nparts; ++k) {
-            const float l = p.sub_lse[part(k) + h];
+            const float l = w_s[h][k];
             const float w = (M == -INFINITY || l == -INFINITY) ? 0.f : expf(l - M);
             w_s[h][k] = w;
             Z += w;
@@ -916,34 +934,37 @@ __global__ void __launch_bounds__(FIXUP_THREADS) tc_fixup_kernel(const DecodePar
     }
     __syncthreads();
     const bool single = it.nsplit == 1;
-    for (int idx = threadIdx.x; idx < G * D; idx += blockDim.x) {
-        const int h = idx / D, d = idx - h * D;
-        float acc = 0.f;
-        for (int k0 = 0; k0 < nparts; k0 += 8) {
-            // eight independent loads in flight, then their weighted sum
-            float v[8];
+    // one output (h, d) per thread: CTA y of the boundary takes outputs
+    // [y*FIXUP_THREADS, (y+1)*FIXUP_THREADS) of the G*D; eight parts' loads
+    // are in flight at once
+    const int idx = blockIdx.y * FIXUP_THREADS + threadIdx.x;
+    if (idx >= G * D)
+        return;
+    const int h = idx / D, d = idx - h * D;
+    float acc = 0.f;
+    for (int k0 = 0; k0 < nparts; k0 += 8) {
+        float v[8];
 #pragma unroll
-            for (int j = 0; j < 8; ++j)
-                v[j] = k0 + j < nparts ? p.sub_o[(part(k0 + j) + h) * D + d] : 0.f;
+        for (int kk = 0; kk < 8; ++kk)
+            v[kk] = k0 + kk < nparts ? p.sub_o[(part(k0 + kk) + h) * D + d] : 0.f;
 #pragma unroll
-            for (int j = 0; j < 8; ++j)
-                if (k0 + j < nparts && w_s[h][k0 + j] != 0.f)
-                    acc = fmaf(w_s[h][k0 + j], v[j], acc);
-        }
-        const float y = acc * inv_s[h];
-        const size_t orow = static_cast<size_t>(it.b) * p.num_q_heads + it.g * G + h;
-        if (single) {
-            if (p.out_f32)
-                reinterpret_cast<float *>(p.out)[orow * D + d] = y;
-            else
-                reinterpret_cast<__nv_bfloat16 *>(p.out)[orow * D + d] = __float2bfloat16_rn(y);
-        } else {
-            const size_t prow =
-                (static_cast<size_t>(it.b) * p.num_splits + it.s) * p.num_q_heads + it.g * G + h;
-            p.part_o[prow * D + d] = y;
-            if (d == 0)
-                p.part_lse[prow] = lse_s[h];
-        }
+        for (int kk = 0; kk < 8; ++kk)
+            if (k0 + kk < nparts && w_s[h][k0 + kk] != 0.f)
+                acc = fmaf(w_s[h][k0 + kk], v[kk], acc);
+    }
+    const float y = acc * inv_s[h];
+    const size_t orow = static_cast<size_t>(it.b) * p.num_q_heads + it.g * G + h;
+    if (single) {
+        if (p.out_f32)
+            reinterpret_cast<float *>(p.out)[orow * D + d] = y;
+        else
+            reinterpret_cast<__nv_bfloat16 *>(p.out)[orow * D + d] = __float2bfloat16_rn(y);
+    } else {
+        const size_t prow =
+            (static_cast<size_t>(it.b) * p.num_splits + it.s) * p.num_q_heads + it.g * G + h;
+        p.part_o[prow * D + d] = y;
+        if (d == 0)
+            p.part_lse[prow] = lse_s[h];
     }
 }
 
@@ -1006,8 +1027,17 @@ static cudaError_t launch_tc_one(const DecodeParams &p, const CUtensorMap &tmk,
             return e;
         configured.store(static_cast<int>(smem), std::memory_order_relaxed);
     }
-    kern<<<grid, TC_THREADS, smem, s>>>(p, tmk, tmv, tmq);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(TC_THREADS);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, p, tmk, tmv, tmq);
 }
 
 template <int D>
@@ -1041,8 +1071,16 @@ cudaError_t launch_decode_tc(const DecodeParams &p, const CUtensorMap &tmk, cons
         e = cudaErrorInvalidValue;
     if (e != cudaSuccess)
         return e;
-    tc_fixup_kernel<<<grid, FIXUP_THREADS, 0, s>>>(p);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.gridDim = dim3(grid, FIXUP_CTAS);
+    cfg.blockDim = dim3(FIXUP_THREADS);
+    cfg.stream = s;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, tc_fixup_kernel, p);
 }
 
 }  // namespace pkv
