@@ -337,7 +337,8 @@ def run_ours(args, rank, world, local_rank):
     status = pkv.device_status(clear=True)
     app_us = statistics.mean(e[0].elapsed_time(e[1]) for e in evs) * 1e3
     dec_us = statistics.mean(e[1].elapsed_time(e[2]) for e in evs) * 1e3
-    cmb_us = statistics.mean(e[2].elapsed_time(e[3]) for e in evs) * 1e3
+    cmb_us = (statistics.mean(e[2].elapsed_time(e[3]) for e in evs) * 1e3
+              if parts[2] is not None else 0.0)
     ms_per_step = elapsed_ms / args.steps
     value = world * step_bytes / (ms_per_step * 1e-3) / 1e9
 
