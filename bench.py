@@ -258,10 +258,10 @@ def run_ours(args, rank, world, local_rank):
         if ev is not None:
             ev[3].record()
 
-    # kernels per step: append; decode (tensor cores: plan + stream-K decode +
-    # fix-up; CUDA cores: decode [+ combine when split])
+    # kernels per step: append; decode (tensor cores: plan + stream-K decode;
+    # CUDA cores: decode [+ combine when split])
     if tc:
-        launches_per_step = 1 + 3 + (1 if split_api else 0)
+        launches_per_step = 1 + 2 + (1 if split_api else 0)
     else:
         launches_per_step = 1 + 1 + (1 if st > 0 else 0)
     dbytes = bytes_model.decode_bytes(spec, w.seq_lens, w.block_table)
@@ -437,7 +437,7 @@ def run_ours(args, rank, world, local_rank):
         "kernels_us": {"append": round(app_us, 3), "decode": round(dec_us, 3),
                        "combine": round(cmb_us, 3)},
         "roofline": {"bound": "hbm",
-                     "kernel": ("decode_tc_kernel (+ plan, fix-up)" if tc else "decode_kernel")
+                     "kernel": ("decode_tc_kernel (+ plan)" if tc else "decode_kernel")
                      + (" split partial" if split_api else ""),
                      "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "peak_source": peak_kind,

@@ -24,8 +24,9 @@
 // tiles there (or an empty item starting there).  A CTA walks its items in order with one pipeline that never
 // drains between them; an item it covers entirely is finished in place (the
 // output, or that split's partial state), an item cut at a CTA boundary
-// leaves one partial state per CTA (log-sum-exp and normalised o), which
-// tc_fixup_kernel merges.  Every SM gets the same number of tiles within
+// leaves one partial state per CTA (log-sum-exp and normalised o), which the
+// CTA holding its last part merges once the others have published theirs
+// (merge_cut_item).  Every SM gets the same number of tiles within
 // one, whatever the mix of lengths, and the per-CTA start-up and drain
 // (TMEM allocation, first loads, last softmax and P.V) are paid once per SM
 // instead of once per item.
@@ -227,6 +228,8 @@ __global__ void __launch_bounds__(1024) tc_plan_kernel(const DecodeParams p, int
     const bool in_smem = p.batch <= PLAN_SMEM_SEQS;
     int *soff = in_smem ? soff_s : p.tc_seqoff;
     pdl_launch_dependents();  // the decode kernel's prologue may start now
+    for (int i = threadIdx.x; i < 2 * kTcMaxGrid; i += 1024)
+        p.tc_flags[i] = 0;
     const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
     const int sb = p.split_blocks;
     const int F = sb > 0 ? (sb + 7) / 8 : 0;  // tiles of a whole split
@@ -337,6 +340,123 @@ __global__ void __launch_bounds__(1024) tc_plan_kernel(const DecodeParams p, int
     }
 }
 
+// ------------------------------------------------------------------ merge
+// An item cut at CTA boundaries is merged by the CTA holding its last part:
+// the CTA whose first item started before its units and ends within them.
+// Its parts are CTA ca's second slot (the item ends ca's range) and the first
+// slots of CTAs ca+1 .. c (the item starts theirs); each is published with a
+// release flag once its bulk stores are complete.  The launch is cooperative
+// (all CTAs resident), so the waits end; they are bounded all the same.
+// Weights exp(lse_k - max), then the normalised sum, written as the output
+// (one split) or as the split's partial state.  scratch: the idle ring.
+template <int D>
+__device__ __noinline__ void merge_cut_item(const DecodeParams &p, int4 first, int c, int W, int C, int t0,
+                               int t1, float *scratch)
+{
+    __shared__ int bad;
+    const Item it = item_at(p, first);
+    if (!(it.b < p.batch && it.start < t0 && t0 < it.start + it.T &&
+          (c == C - 1 || it.start + it.T <= t1)))
+        return;  // uniform over the CTA
+    int ca = c - 1;
+    while (ca > 0 && tile_bound(ca, W, C) > it.start)
+        --ca;
+    const int nparts = c - ca + 1;
+    auto part = [&](int k) { return (static_cast<size_t>(ca + k) * 2 + (k == 0 ? 1 : 0)) * NPAD; };
+    if (threadIdx.x == 0) {
+        bad = 0;
+        for (int k = 0; k < nparts - 1; ++k) {
+            const int *f = &p.tc_flags[(ca + k) * 2 + (k == 0 ? 1 : 0)];
+            if (ld_acquire_gpu(f))
+                continue;
+            const uint64_t t_start = global_timer_ns();
+            while (!ld_acquire_gpu(f)) {
+                if (global_timer_ns() - t_start > 2000000000ull) {
+                    record_error(p.err, PKV_DEV_TIMEOUT);
+                    bad = 1;
+                    break;
+                }
+            }
+            if (bad)
+                break;
+        }
+    }
+    __syncthreads();
+    if (bad)
+        return;
+    const int G = p.group;
+    float *w_s = scratch;                  // [16][kTcMaxGrid]
+    float *inv_s = w_s + NPAD * kTcMaxGrid;  // [16]
+    float *lse_s = inv_s + NPAD;             // [16]
+    for (int idx = threadIdx.x; idx < nparts * NPAD; idx += blockDim.x) {
+        const int k = idx / NPAD, h = idx - k * NPAD;
+        w_s[h * kTcMaxGrid + k] = h < G ? p.sub_lse[part(k) + h] : -INFINITY;
+    }
+    __syncthreads();
+    if (threadIdx.x < G) {
+        const int h = threadIdx.x;
+        float *w = w_s + h * kTcMaxGrid;
+        float M = -INFINITY;
+        for (int k = 0; k < nparts; ++k)
+            M = fmaxf(M, w[k]);
+        float Z = 0.f;
+        for (int k = 0; k < nparts; ++k) {
+            const float e = (M == -INFINITY || w[k] == -INFINITY) ? 0.f : expf(w[k] - M);
+            w[k] = e;
+            Z += e;
+        }
+        inv_s[h] = Z > 0.f ? 1.f / Z : 0.f;
+        lse_s[h] = Z > 0.f ? M + logf(Z) : -INFINITY;
+    }
+    __syncthreads();
+    const bool single = it.nsplit == 1;
+    // four outputs (one float4) per step, four parts' loads in flight
+    for (int q = threadIdx.x; q < G * D / 4; q += blockDim.x) {
+        const int h = (q * 4) / D, d = q * 4 - h * D;
+        const float *w = w_s + h * kTcMaxGrid;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int k0 = 0; k0 < nparts; k0 += 4) {
+            float4 v[4];
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+                v[kk] = k0 + kk < nparts
+                            ? *reinterpret_cast<const float4 *>(&p.sub_o[(part(k0 + kk) + h) * D + d])
+                            : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+                const float wk = k0 + kk < nparts ? w[k0 + kk] : 0.f;
+                if (wk != 0.f) {
+                    acc.x = fmaf(wk, v[kk].x, acc.x);
+                    acc.y = fmaf(wk, v[kk].y, acc.y);
+                    acc.z = fmaf(wk, v[kk].z, acc.z);
+                    acc.w = fmaf(wk, v[kk].w, acc.w);
+                }
+            }
+        }
+        const float inv = inv_s[h];
+        const float4 y = make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+        if (single) {
+            const size_t o = (static_cast<size_t>(it.b) * p.num_q_heads + it.g * G + h) * D + d;
+            if (p.out_f32) {
+                *reinterpret_cast<float4 *>(reinterpret_cast<float *>(p.out) + o) = y;
+            } else {
+                __nv_bfloat162 lo2 = __floats2bfloat162_rn(y.x, y.y);
+                __nv_bfloat162 hi2 = __floats2bfloat162_rn(y.z, y.w);
+                uint2 u;
+                u.x = *reinterpret_cast<uint32_t *>(&lo2);
+                u.y = *reinterpret_cast<uint32_t *>(&hi2);
+                *reinterpret_cast<uint2 *>(reinterpret_cast<__nv_bfloat16 *>(p.out) + o) = u;
+            }
+        } else {
+            const size_t prow =
+                (static_cast<size_t>(it.b) * p.num_splits + it.s) * p.num_q_heads + it.g * G + h;
+            *reinterpret_cast<float4 *>(&p.part_o[prow * D + d]) = y;
+            if (d == 0)
+                p.part_lse[prow] = lse_s[h];
+        }
+    }
+}
+
 // ------------------------------------------------------------------ decode
 template <int D, int GP>
 __global__ void __launch_bounds__(TC_THREADS, 1)
@@ -411,7 +531,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     // The set-up above overlaps the plan kernel (programmatic dependent
     // launch); the plan is read once that kernel has completed.
     pdl_wait();
-    pdl_launch_dependents();  // the fix-up kernel may be scheduled as SMs free up
+    pdl_launch_dependents();  // a dependent kernel may be scheduled as SMs free up
     const int4 hdr = p.tc_plan[0];
     const int W = hdr.x, C = hdr.y;
     const int c = blockIdx.x;
@@ -867,8 +987,16 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                     reinterpret_cast<uint4 *>(ps)[idx] = make_uint4(0u, 0u, 0u, 0u);
             }
         }
-        if (t == 0)
-            bulk_wait_all();  // no bulk store outlives the kernel
+        if (t == 0) {
+            // publish this CTA's partial states: every bulk store (this thread
+            // issued them all) complete, then the flags
+            bulk_wait_all();
+            fence_proxy_async_global();
+            if (active) {
+                st_release_gpu(&p.tc_flags[c * 2 + 0], 1);
+                st_release_gpu(&p.tc_flags[c * 2 + 1], 1);
+            }
+        }
     }
 
     __syncthreads();
@@ -876,96 +1004,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         tc_fence_after();
         tmem_dealloc(tmem, TMEM_COLS);
     }
-}
-
-// ------------------------------------------------------------------ fix-up
-// For each CTA boundary c that cuts an item and is that item's last cut, the
-// item's partial states (CTA ca's second slot, CTAs ca+1..c's first slot)
-// are merged by log-sum-exp into its result: the output, or the split's
-// partial state for the split-KV combine.
-constexpr int FIXUP_THREADS = 1024;
-constexpr int FIXUP_CTAS = (NPAD * 256) / FIXUP_THREADS;  // CTAs per boundary: G*D <= 16*256
-
-__global__ void __launch_bounds__(FIXUP_THREADS) tc_fixup_kernel(const DecodeParams p)
-{
-    __shared__ float w_s[NPAD][kTcMaxGrid];  // log-sum-exp, then weight, of part k for head h
-    __shared__ float inv_s[NPAD], lse_s[NPAD];
-    pdl_wait();  // the decode kernel's partial states are complete and visible
-    const int4 hdr = p.tc_plan[0];
-    const int W = hdr.x, C = hdr.y;
-    const int c = blockIdx.x;
-    if (c == 0 || c >= C)
-        return;
-    const int t0 = tile_bound(c, W, C), t1 = tile_bound(c + 1, W, C);
-    const Item it = item_at(p, p.tc_plan[1 + c]);
-    if (it.b >= p.batch || !(it.start < t0 && t0 < it.start + it.T))
-        return;  // no item's real tiles are cut at this boundary
-    if (c < C - 1 && it.start + it.T > t1)
-        return;  // a later boundary cuts it too and merges it
-    int ca = c - 1;  // the CTA holding the item's first tile
-    while (ca > 0 && tile_bound(ca, W, C) > it.start)
-        --ca;
-    const int nparts = c - ca + 1;
-    const int D = p.head_dim, G = p.group;
-    // part k = CTA ca + k: its second slot for k = 0 (the item ends its
-    // range), its first slot otherwise (the item starts its range)
-    auto part = [&](int k) { return (static_cast<size_t>(ca + k) * 2 + (k == 0 ? 1 : 0)) * NPAD; };
-    // every part's log-sum-exp loaded at once (one thread each), then the
-    // weights per head from shared memory
-    for (int idx = threadIdx.x; idx < nparts * NPAD; idx += blockDim.x) {
-        const int k = idx / NPAD, h = idx - k * NPAD;
-        w_s[h][k] = h < G ? p.sub_lse[part(k) + h] : -INFINITY;
-    }
-    __syncthreads();
-    if (threadIdx.x < G) {
-        const int h = threadIdx.x;
-        float M = -INFINITY;
-        for (int k = 0; k < nparts; ++k)
-            M = fmaxf(M, w_s[h][k]);
-        float Z = 0.f;
-        for (int k = 0; k < nparts; ++k) {
-            const float l = w_s[h][k];
-            const float w = (M == -INFINITY || l == -INFINITY) ? 0.f : expf(l - M);
-            w_s[h][k] = w;
-            Z += w;
-        }
-        inv_s[h] = Z > 0.f ? 1.f / Z : 0.f;
-        lse_s[h] = Z > 0.f ? M + logf(Z) : -INFINITY;
-    }
-    __syncthreads();
-    const bool single = it.nsplit == 1;
-    // one output (h, d) per thread: CTA y of the boundary takes outputs
-    // [y*FIXUP_THREADS, (y+1)*FIXUP_THREADS) of the G*D; eight parts' loads
-    // are in flight at once
-    const int idx = blockIdx.y * FIXUP_THREADS + threadIdx.x;
-    if (idx >= G * D)
-        return;
-    const int h = idx / D, d = idx - h * D;
-    float acc = 0.f;
-    for (int k0 = 0; k0 < nparts; k0 += 8) {
-        float v[8];
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-            v[kk] = k0 + kk < nparts ? p.sub_o[(part(k0 + kk) + h) * D + d] : 0.f;
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-            if (k0 + kk < nparts && w_s[h][k0 + kk] != 0.f)
-                acc = fmaf(w_s[h][k0 + kk], v[kk], acc);
-    }
-    const float y = acc * inv_s[h];
-    const size_t orow = static_cast<size_t>(it.b) * p.num_q_heads + it.g * G + h;
-    if (single) {
-        if (p.out_f32)
-            reinterpret_cast<float *>(p.out)[orow * D + d] = y;
-        else
-            reinterpret_cast<__nv_bfloat16 *>(p.out)[orow * D + d] = __float2bfloat16_rn(y);
-    } else {
-        const size_t prow =
-            (static_cast<size_t>(it.b) * p.num_splits + it.s) * p.num_q_heads + it.g * G + h;
-        p.part_o[prow * D + d] = y;
-        if (d == 0)
-            p.part_lse[prow] = lse_s[h];
-    }
+    if (active)
+        merge_cut_item<D>(p, first, c, W, C, t0, t1, reinterpret_cast<float *>(units));
 }
 
 // ------------------------------------------------------------ host side
@@ -979,7 +1019,8 @@ int decode_tc_group_pad(int group)
 size_t decode_tc_scratch_bytes(int batch, int head_dim)
 {
     auto up = [](size_t x) { return (x + 255) / 256 * 256; };
-    return up(sizeof(int4) * (2 + kTcMaxGrid)) + up(sizeof(int) * (static_cast<size_t>(batch) + 1)) +
+    return up(sizeof(int4) * (2 + kTcMaxGrid)) + up(sizeof(int) * 2 * kTcMaxGrid) +
+           up(sizeof(int) * (static_cast<size_t>(batch) + 1)) +
            up(sizeof(float) * kTcMaxGrid * 2 * NPAD) +
            sizeof(float) * kTcMaxGrid * 2 * NPAD * static_cast<size_t>(head_dim);
 }
@@ -990,6 +1031,8 @@ void decode_tc_bind_scratch(DecodeParams &p, void *scratch, int batch)
     char *s = static_cast<char *>(scratch);
     p.tc_plan = reinterpret_cast<int4 *>(s);
     s += up(sizeof(int4) * (2 + kTcMaxGrid));
+    p.tc_flags = reinterpret_cast<int *>(s);
+    s += up(sizeof(int) * 2 * kTcMaxGrid);
     p.tc_seqoff = reinterpret_cast<int *>(s);
     s += up(sizeof(int) * (static_cast<size_t>(batch) + 1));
     p.sub_lse = reinterpret_cast<float *>(s);
@@ -1027,16 +1070,19 @@ static cudaError_t launch_tc_one(const DecodeParams &p, const CUtensorMap &tmk,
             return e;
         configured.store(static_cast<int>(smem), std::memory_order_relaxed);
     }
+    // cooperative: every CTA resident, so the merge's waits on other CTAs end
     cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeCooperative;
+    attr[1].val.cooperative = 1;
     cfg.gridDim = dim3(grid);
     cfg.blockDim = dim3(TC_THREADS);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     return cudaLaunchKernelEx(&cfg, kern, p, tmk, tmv, tmq);
 }
 
@@ -1069,18 +1115,7 @@ cudaError_t launch_decode_tc(const DecodeParams &p, const CUtensorMap &tmk, cons
         e = launch_tc_d<256>(p, tmk, tmv, tmq, gp, grid, s);
     else
         e = cudaErrorInvalidValue;
-    if (e != cudaSuccess)
-        return e;
-    cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.gridDim = dim3(grid, FIXUP_CTAS);
-    cfg.blockDim = dim3(FIXUP_THREADS);
-    cfg.stream = s;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, tc_fixup_kernel, p);
+    return e;
 }
 
 }  // namespace pkv

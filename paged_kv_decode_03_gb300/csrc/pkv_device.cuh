@@ -114,6 +114,26 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, unsign
     }
 }
 
+// ------------------------------------------------ flags between CTAs
+__device__ __forceinline__ void st_release_gpu(int *addr, int v)
+{
+    asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(addr), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ int ld_acquire_gpu(const int *addr)
+{
+    int v;
+    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(addr) : "memory");
+    return v;
+}
+
+// Order this thread's completed async-proxy (bulk copy) global writes before
+// its later generic accesses.
+__device__ __forceinline__ void fence_proxy_async_global()
+{
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
 // ------------------------------------------- programmatic dependent launch
 // Let the next kernel in the stream (launched with programmatic stream
 // serialisation) start its prologue now.

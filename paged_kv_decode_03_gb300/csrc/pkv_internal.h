@@ -45,6 +45,7 @@ struct DecodeParams {
     int32_t *tc_seqoff;       // [batch + 1] first tile of each sequence
     float *sub_lse;           // [grid][2][16] partial states of items cut at CTA boundaries
     float *sub_o;             // [grid][2][16][head_dim]
+    int32_t *tc_flags;        // [grid][2] partial state published (cleared by the plan)
 };
 
 struct AppendParams {
@@ -91,7 +92,7 @@ cudaError_t launch_combine(const CombineParams &p, cudaStream_t s);
 // Tensor-core decode kernel (bf16 pools, head_dim 128/256, group <= 16):
 // persistent stream-K over the 128-key tiles of all (sequence, kv head,
 // split) items, one CTA per SM (at most kTcMaxGrid); num_stages = ring units
-// of 32 KB.  Launches the plan, decode and fix-up kernels; needs
+// of 32 KB.  Launches the plan and the (cooperative) decode kernel; needs
 // decode_tc_scratch_bytes of workspace bound with decode_tc_bind_scratch.
 constexpr int kTcMaxGrid = 256;
 int decode_tc_group_pad(int group);  // 0 if the group is too large

@@ -131,9 +131,11 @@ def test_workspace_bytes(lib):
     split_bytes = up(rows * 4) + rows * 256 * 4
     assert wb(32, 16, 8, 256, 16, 32768, 0, 1024) == split_bytes
     # tensor-core shapes (group 8..16, head_dim 128/256): the stream-K scratch
-    # (plan of up to 256 CTAs, per-sequence prefix, two partial states per CTA)
+    # (plan of up to 256 CTAs, their publish flags, per-sequence prefix, two
+    # partial states per CTA)
     grid, npad = 256, 16
-    tc = up(16 * (2 + grid)) + up(4 * (32 + 1)) + up(4 * grid * 2 * npad) + 4 * grid * 2 * npad * 256
+    tc = (up(16 * (2 + grid)) + up(4 * 2 * grid) + up(4 * (32 + 1)) + up(4 * grid * 2 * npad)
+          + 4 * grid * 2 * npad * 256)
     assert pwb(32, 16, 1, 256) == tc
     assert wb(32, 16, 1, 256, 16, 32768, 0, 0) == tc
     assert wb(32, 16, 1, 256, 16, 32768, 0, 1024) == max(split_bytes, tc)
