@@ -182,9 +182,9 @@ def test_split_partial_matches_oracle_partials():
 @pytest.mark.parametrize("hq,hkv,D,alias", [(16, 1, 256, True), (16, 2, 128, False)])
 def test_tc_split_partial_matches_oracle_partials(hq, hkv, D, alias):
     """On the tensor-core kernel the split partials come from the stream-K
-    walk: splits cut between SMs are merged by the fix-up kernel before they
-    are written.  Each split's log-sum-exp and normalised output must match
-    the oracle's partial of the same keys."""
+    walk: splits cut between SMs are merged by the CTA holding their last part
+    before they are written.  Each split's log-sum-exp and normalised output
+    must match the oracle's partial of the same keys."""
     spec = synth.Spec(f"tc_split_{hq}_{hkv}_{D}", batch=7, num_q_heads=hq, num_kv_heads=hkv,
                       head_dim=D, lens=("fixed", (0, 5, 300, 2100, 4500, 64, 9000)), alias=alias,
                       seed=21 + D)
@@ -235,7 +235,7 @@ def test_tc_split_partial_matches_oracle_partials(hq, hkv, D, alias):
 def test_tc_stream_k_partition(lens):
     """The stream-K walk of the tensor-core kernel: any mix of lengths splits
     into equal tile shares per SM; ranges cut between SMs are merged by the
-    fix-up kernel."""
+    CTA holding their last part."""
     spec = synth.Spec(f"tc_sk_{len(lens)}_{max(lens)}", batch=len(lens), num_q_heads=16,
                       num_kv_heads=1, head_dim=256, lens=("fixed", lens), alias=True,
                       seed=5 + len(lens))
@@ -250,7 +250,7 @@ def test_tc_stream_k_gqa8_window():
 
 
 def test_tc_graph_capture():
-    """The tensor-core path (plan, persistent decode and fix-up kernels)
+    """The tensor-core path (plan and persistent cooperative decode kernels)
     captures into a CUDA graph and replays."""
     spec = synth.shrink(synth.C3, batch=5, lens=("uniform", 1, 6000))
     w = synth.make_workload(spec)
