@@ -258,12 +258,20 @@ def run_ours(args, rank, world, local_rank):
         if ev is not None:
             ev[3].record()
 
-    # kernels per step: append; decode (tensor cores: plan + stream-K decode;
-    # CUDA cores: decode [+ combine when split])
-    if tc:
-        launches_per_step = 1 + 2 + (1 if split_api else 0)
+    # kernels per step, as the library reports them for each call
+    launches_per_step = 0
+    pkv.paged_kv_append(k_new, v_new, slots, pool)
+    launches_per_step += pkv.last_launch_count()
+    if split_api:
+        pkv.paged_decode_split_partial(q, pool, bt, sl, spec.window, scale, st, lse, po, out,
+                                       max_len, workspace=pws)
+        launches_per_step += pkv.last_launch_count()
+        pkv.paged_decode_lse_combine(lse, po, sl, spec.window, st, out)
+        launches_per_step += pkv.last_launch_count()
     else:
-        launches_per_step = 1 + 1 + (1 if st > 0 else 0)
+        pkv.paged_decode_attention(q, pool, bt, sl, spec.window, scale, out, max_len,
+                                   split_tokens=st, workspace=ws)
+        launches_per_step += pkv.last_launch_count()
     dbytes = bytes_model.decode_bytes(spec, w.seq_lens, w.block_table)
     abytes = bytes_model.append_bytes(spec, int((w.new_slots >= 0).sum()))
     step_bytes = dbytes["kv"] + dbytes["q"] + dbytes["out"] + abytes

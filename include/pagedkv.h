@@ -149,13 +149,15 @@ PKV_API int32_t paged_decode_num_splits(int32_t block_size, int32_t max_seq_len,
                                         int32_t split_tokens);
 
 /*
- * paged_decode_workspace_bytes -- device scratch paged_decode_attention needs
- * for these sizes: the larger of the split partials (when the key ranges
- * are split: partial log-sum-exp [batch][num_splits][num_q_heads] fp32,
- * then, 256-byte aligned, partial outputs
- * [batch][num_splits][num_q_heads][head_dim] fp32) and the tensor-core
- * kernel's scratch (paged_decode_partial_workspace_bytes).  0 when neither
- * is needed.
+ * paged_decode_workspace_bytes -- device scratch paged_decode_attention
+ * uses for these sizes: the largest of the split partials (when the key
+ * ranges are split: partial log-sum-exp [batch][num_splits][num_q_heads]
+ * fp32, then, 256-byte aligned, partial outputs
+ * [batch][num_splits][num_q_heads][head_dim] fp32), the tensor-core kernel's
+ * scratch (paged_decode_partial_workspace_bytes) and, for a single pass on
+ * CUDA cores, (sequence, length) int32 pairs of the batch longest first (used
+ * when the grid exceeds one wave; a single pass given no workspace runs in
+ * batch order).  0 only for batch 0.
  */
 PKV_API size_t paged_decode_workspace_bytes(int32_t batch, int32_t num_q_heads,
                                             int32_t num_kv_heads, int32_t head_dim,
@@ -289,6 +291,9 @@ PKV_API int paged_decode_attention_noalloc(const void *q, const pkv_pool *pool,
  * kernel, or a negative PKV_E_* code for an invalid pool.  Host only.
  */
 PKV_API int32_t paged_decode_uses_tensor_cores(const pkv_pool *pool, int32_t num_q_heads);
+
+/* Number of kernels the calling thread's last call of this library launched. */
+PKV_API int32_t pkv_last_launch_count(void);
 
 /* Message of the last host-side error on this thread ("" if none). */
 PKV_API const char *pkv_last_error(void);

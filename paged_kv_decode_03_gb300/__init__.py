@@ -12,7 +12,7 @@ from .binding import (  # noqa: F401
     PagedKVPool, paged_kv_append, paged_decode_attention, paged_decode_split_partial,
     paged_decode_lse_combine, paged_decode_workspace_bytes, paged_decode_num_splits,
     paged_decode_split_tokens, PagedKVError, paged_decode_attention_noalloc,
-    paged_decode_partial_workspace_bytes, uses_tensor_cores,
+    paged_decode_partial_workspace_bytes, uses_tensor_cores, last_launch_count,
     STATIC_SCRATCH_BYTES,
     library_path, load_library, device_status, exported_symbols,
 )

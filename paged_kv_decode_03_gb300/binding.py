@@ -80,6 +80,8 @@ def load_library():
     lib.paged_decode_attention_noalloc.restype = ctypes.c_int
     lib.paged_decode_uses_tensor_cores.argtypes = [p, i32]
     lib.paged_decode_uses_tensor_cores.restype = i32
+    lib.pkv_last_launch_count.argtypes = []
+    lib.pkv_last_launch_count.restype = i32
     lib.pkv_last_error.argtypes = []
     lib.pkv_last_error.restype = ctypes.c_char_p
     lib.pkv_device_status.argtypes = [i32]
@@ -231,6 +233,11 @@ def paged_decode_attention(q, pool: PagedKVPool, block_table, seq_lens, window: 
                                       int(split_tokens), ws_ptr, ws_bytes, _dev_ptr(out, "out"),
                                       out_dtype, _stream(stream)), "paged_decode_attention")
     return out
+
+
+def last_launch_count() -> int:
+    """Kernels launched by this thread's last call into the library."""
+    return int(load_library().pkv_last_launch_count())
 
 
 def uses_tensor_cores(pool: PagedKVPool, num_q_heads: int) -> bool:

@@ -40,6 +40,9 @@ static unsigned int *error_word_ptr()
 }
 
 static thread_local std::string t_last_error;
+static thread_local int t_launches = 0;  // kernels launched by this thread's last call
+
+void note_launch() { ++t_launches; }
 
 static int fail(int code, const char *fmt, ...)
 {
@@ -239,6 +242,8 @@ extern "C" {
 
 PKV_API const char *pkv_last_error(void) { return t_last_error.c_str(); }
 
+PKV_API int32_t pkv_last_launch_count(void) { return t_launches; }
+
 PKV_API int pkv_device_status(int32_t clear)
 {
     unsigned int w = 0;
@@ -257,6 +262,7 @@ PKV_API int pkv_device_status(int32_t clear)
 PKV_API int32_t paged_decode_uses_tensor_cores(const pkv_pool *pool, int32_t num_q_heads)
 {
     t_last_error.clear();
+    t_launches = 0;
     if (int rc = check_pool(pool))
         return rc;
     if (num_q_heads <= 0 || num_q_heads % pool->num_kv_heads)
@@ -269,6 +275,7 @@ PKV_API int paged_kv_append(const void *k, const void *v, const int64_t *slot_ma
                             int32_t num_tokens, const pkv_pool *pool, void *stream)
 {
     t_last_error.clear();
+    t_launches = 0;
     if (int rc = check_pool(pool))
         return rc;
     if (num_tokens < 0)
@@ -357,7 +364,10 @@ PKV_API size_t paged_decode_workspace_bytes(int32_t batch, int32_t num_q_heads,
     }
     const size_t tc = paged_decode_partial_workspace_bytes(batch, num_q_heads, num_kv_heads,
                                                            head_dim);
-    return need > tc ? need : tc;
+    // a single pass on CUDA cores orders the sequences longest first in here
+    const size_t order = batch > 0 ? (2 * sizeof(int32_t) * (size_t)batch + 255) / 256 * 256 : 0;
+    need = need > tc ? need : tc;
+    return need > order ? need : order;
 }
 
 PKV_API size_t paged_decode_partial_workspace_bytes(int32_t batch, int32_t num_q_heads,
@@ -465,6 +475,11 @@ static int run_decode(const void *q, const pkv_pool *pool, const int32_t *block_
     }
     p.qk_scale_log2 = softmax_scale * LOG2E;
     p.head_dim = pool->head_dim;
+    // a single pass on CUDA cores may order the sequences longest first in
+    // the caller's workspace
+    if (!tc && split_tokens == 0 && workspace && aligned(workspace, 8) &&
+        workspace_bytes >= 2 * sizeof(int32_t) * static_cast<size_t>(batch))
+        p.order_ws = static_cast<int32_t *>(workspace);
     p.err = error_word_ptr();
     if (!p.err)
         return fail(PKV_E_DRIVER, "cannot resolve the device error word");
@@ -501,6 +516,7 @@ PKV_API int paged_decode_split_partial(const void *q, const pkv_pool *pool,
                                        void *stream)
 {
     t_last_error.clear();
+    t_launches = 0;
     if (int rc = check_decode_args(q, pool, block_table, max_blocks_per_seq, seq_lens, batch,
                                    num_q_heads, max_seq_len, window, out, out_dtype))
         return rc;
@@ -530,6 +546,7 @@ PKV_API int paged_decode_lse_combine(const float *partial_lse, const float *part
                                      int32_t out_dtype, void *stream)
 {
     t_last_error.clear();
+    t_launches = 0;
     if (!partial_lse || !partial_o || !seq_lens || !out)
         return fail(PKV_E_NULL, "NULL argument");
     if (block_size != kBlock)
@@ -569,6 +586,7 @@ PKV_API int paged_decode_attention(const void *q, const pkv_pool *pool, const in
                                    int32_t out_dtype, void *stream)
 {
     t_last_error.clear();
+    t_launches = 0;
     if (int rc = check_decode_args(q, pool, block_table, max_blocks_per_seq, seq_lens, batch,
                                    num_q_heads, max_seq_len, window, out, out_dtype))
         return rc;
@@ -674,6 +692,7 @@ extern "C" PKV_API int paged_decode_attention_noalloc(
     void *stream)
 {
     t_last_error.clear();
+    t_launches = 0;
     if (int rc = check_decode_args(q, pool, block_table, max_blocks_per_seq, seq_lens, batch,
                                    num_q_heads, max_seq_len, window, out, out_dtype))
         return rc;

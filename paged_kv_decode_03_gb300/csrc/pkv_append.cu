@@ -126,6 +126,7 @@ cudaError_t launch_append(const AppendParams &p, int int8, cudaStream_t s)
         append_kernel<true><<<p.num_tokens, APPEND_THREADS, 0, s>>>(p);
     else
         append_kernel<false><<<p.num_tokens, APPEND_THREADS, 0, s>>>(p);
+    note_launch();
     return cudaGetLastError();
 }
 

@@ -184,9 +184,8 @@ __device__ __forceinline__ void load_chunk(const uint8_t *p, float2 (&f)[INT8 ? 
 }
 
 template <int D, int GT, bool INT8>
-__global__ void __launch_bounds__(THREADS) decode_kernel(const DecodeParams p,
-                                                         const __grid_constant__ CUtensorMap tmk,
-                                                         const __grid_constant__ CUtensorMap tmv)
+__device__ __forceinline__ void decode_body(const DecodeParams &p, const CUtensorMap *tmk,
+                                            const CUtensorMap *tmv)
 {
     using C = Cfg<D, GT, INT8>;
     constexpr int BPS = C::BPS;
@@ -202,7 +201,17 @@ __global__ void __launch_bounds__(THREADS) decode_kernel(const DecodeParams p,
     const int split = blockIdx.x;
     const int g = blockIdx.y / p.head_chunks;
     const int chunk = blockIdx.y - g * p.head_chunks;
-    const int b = blockIdx.z;
+    // in order, or the order kernel's (sequence, length) pair: one load either way
+    int b, len;
+    if (p.seq_order) {
+        pdl_wait();  // the order kernel has completed
+        const int2 e = reinterpret_cast<const int2 *>(p.seq_order)[blockIdx.z];
+        b = e.x;
+        len = e.y;
+    } else {
+        b = blockIdx.z;
+        len = p.seq_lens[b];
+    }
     const int NS = p.num_stages;
     const bool alias = p.alias != 0;
     const bool per_token = INT8 && p.scale_mode == PKV_SCALE_PER_TOKEN;
@@ -210,7 +219,6 @@ __global__ void __launch_bounds__(THREADS) decode_kernel(const DecodeParams p,
     const int KS = slot_bytes(C::TILE, BPS, per_token);
     const int SB = alias ? KS : 2 * KS;  // one stage: K slot [+ V slot]
 
-    int len = p.seq_lens[b];
     const bool reporter = threadIdx.x == 0 && split == 0 && blockIdx.y == 0;
     if (len > p.max_blocks * C::P) {
         if (reporter)
@@ -249,9 +257,9 @@ __global__ void __launch_bounds__(THREADS) decode_kernel(const DecodeParams p,
         // stage hold data; the other lanes only help read the block table.
         if (nst > 0) {
             if (lane == 0) {
-                prefetch_tensormap(&tmk);
+                prefetch_tensormap(tmk);
                 if (!alias)
-                    prefetch_tensormap(&tmv);
+                    prefetch_tensormap(tmv);
             }
             const uint64_t pol = policy_evict_first();
             TableCursor tc;
@@ -292,7 +300,7 @@ __global__ void __launch_bounds__(THREADS) decode_kernel(const DecodeParams p,
                         smask[st] = vm;  // released by the arrive below
                     mbar_arrive_expect_tx(&fullb[st], tx);
                     uint8_t *dst = ring + st * SB + which * KS;
-                    const CUtensorMap *map = which == 0 ? &tmk : &tmv;
+                    const CUtensorMap *map = which == 0 ? tmk : tmv;
                     const float *scales = which == 0 ? p.k_scale : p.v_scale;
 #pragma unroll
                     for (int t = 0; t < BPS; ++t) {
@@ -597,6 +605,101 @@ __global__ void __launch_bounds__(THREADS) decode_kernel(const DecodeParams p,
     }
 }
 
+// The kernels.  One query head per CTA has its own entry with at most 80
+// registers, so that five CTAs fit an SM (left to itself the compiler takes
+// 81 for the int8 head_dim-128 instance, which then runs four CTAs per SM and
+// measured 6% slower); the other instances keep the compiler's choice (an
+// explicit bound of one CTA makes it take more registers than without).
+template <int D, int GT, bool INT8>
+__global__ void __launch_bounds__(THREADS) decode_kernel(const DecodeParams p,
+                                                         const __grid_constant__ CUtensorMap tmk,
+                                                         const __grid_constant__ CUtensorMap tmv)
+{
+    decode_body<D, GT, INT8>(p, &tmk, &tmv);
+}
+
+template <int D, bool INT8>
+__global__ void __launch_bounds__(THREADS, 5) decode_kernel_1h(const DecodeParams p,
+                                                               const __grid_constant__ CUtensorMap tmk,
+                                                               const __grid_constant__ CUtensorMap tmv)
+{
+    decode_body<D, 1, INT8>(p, &tmk, &tmv);
+}
+
+template <int D, int GT, bool INT8>
+constexpr auto decode_entry()
+{
+    if constexpr (GT == 1)
+        return decode_kernel_1h<D, INT8>;
+    else
+        return decode_kernel<D, GT, INT8>;
+}
+
+// Sequences ordered by decreasing number of paged blocks in their key range
+// (counting sort, one CTA): CTAs are dispatched in grid order, so with more
+// CTAs than fit at once the longest ranges start first and the short ones
+// fill the last wave.  Ties come out in any order (the results do not depend
+// on the order in which CTAs run).
+constexpr int ORDER_BINS = 4096;
+
+__global__ void __launch_bounds__(1024) seq_order_kernel(const int32_t *seq_lens, int batch,
+                                                         int window, int max_blocks,
+                                                         int2 *order)
+{
+    __shared__ int hist[ORDER_BINS];
+    __shared__ int wsum[32];
+    pdl_launch_dependents();
+    auto key = [&](int b) {
+        const int len = min(seq_lens[b], max_blocks * kBlock);
+        const KeyRange kr = key_range(len, window, 0);
+        return ORDER_BINS - 1 - min(kr.nblk, ORDER_BINS - 1);  // longest first
+    };
+    for (int i = threadIdx.x; i < ORDER_BINS; i += 1024)
+        hist[i] = 0;
+    __syncthreads();
+    for (int b = threadIdx.x; b < batch; b += 1024)
+        atomicAdd(&hist[key(b)], 1);
+    __syncthreads();
+    // exclusive prefix over the bins: 4 per thread, warp shuffles, then warps
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+    int v[4], sum = 0;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        v[j] = hist[threadIdx.x * 4 + j];
+        sum += v[j];
+    }
+    int x = sum;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const int y = __shfl_up_sync(FULL_MASK, x, off);
+        if (lane >= off)
+            x += y;
+    }
+    if (lane == 31)
+        wsum[wid] = x;
+    __syncthreads();
+    if (wid == 0) {
+        int w = wsum[lane];
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int y = __shfl_up_sync(FULL_MASK, w, off);
+            if (lane >= off)
+                w += y;
+        }
+        wsum[lane] = w;
+    }
+    __syncthreads();
+    int run = x - sum + (wid > 0 ? wsum[wid - 1] : 0);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        hist[threadIdx.x * 4 + j] = run;
+        run += v[j];
+    }
+    __syncthreads();
+    for (int b = threadIdx.x; b < batch; b += 1024)
+        order[atomicAdd(&hist[key(b)], 1)] = make_int2(b, seq_lens[b]);
+}
+
 // One CTA per (query head, sequence) with more than one split.
 __global__ void __launch_bounds__(128) combine_kernel(const CombineParams p)
 {
@@ -669,7 +772,7 @@ static cudaError_t configure_smem()
     if (e == cudaSuccess)
         e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
     if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(decode_kernel<D, GT, INT8>,
+        e = cudaFuncSetAttribute(decode_entry<D, GT, INT8>(),
                                  cudaFuncAttributeMaxDynamicSharedMemorySize, optin);
     if (e == cudaSuccess)
         done.store(1, std::memory_order_release);
@@ -692,7 +795,7 @@ static int ring_stages_one(int alias, int per_token)
     for (int ns = 2; ns <= 8; ++ns) {
         const size_t smem = decode_smem_bytes(D, INT8, alias, per_token, GT, ns);
         int occ = 0;
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, decode_kernel<D, GT, INT8>,
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, decode_entry<D, GT, INT8>(),
                                                           THREADS, smem) != cudaSuccess ||
             occ < 1)
             break;
@@ -741,8 +844,41 @@ static cudaError_t launch_one(const DecodeParams &p, const CUtensorMap &tmk,
     if (e != cudaSuccess)
         return e;
     dim3 grid(p.num_splits, p.num_kv_heads * p.head_chunks, p.batch);
-    decode_kernel<D, GT, INT8><<<grid, THREADS, smem, s>>>(p, tmk, tmv);
-    return cudaGetLastError();
+    // More CTAs than fit at once (a single pass with ragged lengths is what
+    // gains): order the sequences longest first, if the caller gave room.
+    bool order = false;
+    if (p.order_ws && p.split_blocks == 0 && p.batch > 1) {
+        int occ = 0, dev = 0, sms = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, decode_entry<D, GT, INT8>(),
+                                                          THREADS, smem) == cudaSuccess &&
+            cudaGetDevice(&dev) == cudaSuccess &&
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess)
+            order = static_cast<int64_t>(grid.x) * grid.y * grid.z > static_cast<int64_t>(occ) * sms;
+    }
+    if (!order) {
+        decode_entry<D, GT, INT8>()<<<grid, THREADS, smem, s>>>(p, tmk, tmv);
+        note_launch();
+        return cudaGetLastError();
+    }
+    seq_order_kernel<<<1, 1024, 0, s>>>(p.seq_lens, p.batch, p.window, p.max_blocks,
+                                        reinterpret_cast<int2 *>(p.order_ws));
+    note_launch();
+    if ((e = cudaGetLastError()) != cudaSuccess)
+        return e;
+    note_launch();
+    DecodeParams q = p;
+    q.seq_order = p.order_ws;
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(THREADS);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, decode_entry<D, GT, INT8>(), q, tmk, tmv);
 }
 
 template <int D>
@@ -774,6 +910,7 @@ cudaError_t launch_combine(const CombineParams &p, cudaStream_t s)
 {
     dim3 grid(p.num_q_heads, p.batch);
     combine_kernel<<<grid, 128, 0, s>>>(p);
+    note_launch();
     return cudaGetLastError();
 }
 

@@ -1083,6 +1083,7 @@ static cudaError_t launch_tc_one(const DecodeParams &p, const CUtensorMap &tmk,
     cfg.stream = s;
     cfg.attrs = attr;
     cfg.numAttrs = 2;
+    note_launch();
     return cudaLaunchKernelEx(&cfg, kern, p, tmk, tmv, tmq);
 }
 
@@ -1106,6 +1107,7 @@ cudaError_t launch_decode_tc(const DecodeParams &p, const CUtensorMap &tmk, cons
     const int gp = decode_tc_group_pad(p.group);
     const int grid = decode_tc_grid();
     tc_plan_kernel<<<1, 1024, 0, s>>>(p, grid);
+    note_launch();
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess)
         return e;

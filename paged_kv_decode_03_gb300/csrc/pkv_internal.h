@@ -46,6 +46,10 @@ struct DecodeParams {
     float *sub_lse;           // [grid][2][16] partial states of items cut at CTA boundaries
     float *sub_o;             // [grid][2][16][head_dim]
     int32_t *tc_flags;        // [grid][2] partial state published (cleared by the plan)
+    // CUDA-core kernel: (sequence, length) pairs longest first (NULL = in
+    // order), and the workspace that may hold them ([batch] int2; NULL = none)
+    const int32_t *seq_order;
+    int32_t *order_ws;
 };
 
 struct AppendParams {
@@ -104,5 +108,8 @@ cudaError_t launch_decode_tc(const DecodeParams &p, const CUtensorMap &tmk,
                              const CUtensorMap &tmv, const CUtensorMap &tmq, int head_dim,
                              cudaStream_t s);
 cudaError_t launch_append(const AppendParams &p, int int8, cudaStream_t s);
+
+// Count one kernel launch of the current API call (pkv_last_launch_count).
+void note_launch();
 
 }  // namespace pkv

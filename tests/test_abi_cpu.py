@@ -124,8 +124,11 @@ def test_workspace_bytes(lib):
     wb = lib.paged_decode_workspace_bytes
     pwb = lib.paged_decode_partial_workspace_bytes
     up = lambda x: (x + 255) // 256 * 256
-    # CUDA-core shapes (group < 8): split partials only
-    assert wb(32, 16, 8, 256, 16, 32768, 0, 0) == 0
+    # CUDA-core shapes (group < 8): split partials, or for a single pass the
+    # (sequence, length) order of the batch (256-byte rounded)
+    assert wb(32, 16, 8, 256, 16, 32768, 0, 0) == 256
+    assert wb(1000, 16, 8, 256, 16, 32768, 0, 0) == up(8 * 1000)
+    assert wb(0, 16, 8, 256, 16, 32768, 0, 0) == 0
     assert pwb(32, 16, 8, 256) == 0
     rows = 32 * 16 * 32
     split_bytes = up(rows * 4) + rows * 256 * 4
