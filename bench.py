@@ -78,10 +78,18 @@ def peaks():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def csrc_sha() -> str:
+# Sources each decode kernel is compiled from: a recorded DRAM-traffic figure
+# stays valid while these files are unchanged.
+KERNEL_SOURCES = {
+    "cuda_core": ("pkv_decode.cu", "pkv_device.cuh", "pkv_internal.h"),
+    "tensor_core": ("pkv_decode_tc.cu", "pkv_device.cuh", "pkv_internal.h"),
+}
+
+
+def csrc_sha(names=None) -> str:
     h = hashlib.sha256()
     base = os.path.join(ROOT, "paged_kv_decode_03_gb300", "csrc")
-    for name in sorted(os.listdir(base)):
+    for name in sorted(names if names is not None else os.listdir(base)):
         with open(os.path.join(base, name), "rb") as f:
             h.update(name.encode())
             h.update(f.read())
@@ -90,13 +98,13 @@ def csrc_sha() -> str:
 
 def recorded_traffic(config: str):
     """DRAM bytes per launch of the decode kernel from the committed ncu
-    summary, if it was taken on the current kernel sources."""
+    summary, if it was taken on the current sources of that kernel."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as f:
             d = json.load(f)
         e = d.get(config)
-        if e and e.get("csrc_sha") == csrc_sha():
+        if e and e.get("sources_sha") == csrc_sha(KERNEL_SOURCES[e["kernel_family"]]):
             return e.get("bytes_per_launch")
     except Exception:
         pass

@@ -1,5 +1,4 @@
-// pkv_decode.cu -- CUDA-core decode attention over a paged KV pool, and the
-// log-sum-exp combine of split-KV partials.
+// pkv_decode.cu -- CUDA-core decode attention over a paged KV pool.
 //
 // What is computed (sources by page title and section):
 //   "CS336 · 第 10 课", KV-cache section: y = softmax(q K^T * scale) V over
@@ -68,7 +67,7 @@ struct KeyRange {
 };
 
 // Keys a decode at position len-1 may attend to, and the block-aligned
-// split of that range.  Shared by the decode and the combine kernels.
+// split of that range.
 __device__ __forceinline__ KeyRange key_range(int len, int window, int split_blocks)
 {
     KeyRange r;
@@ -700,48 +699,6 @@ __global__ void __launch_bounds__(1024) seq_order_kernel(const int32_t *seq_lens
         order[atomicAdd(&hist[key(b)], 1)] = make_int2(b, seq_lens[b]);
 }
 
-// One CTA per (query head, sequence) with more than one split.
-__global__ void __launch_bounds__(128) combine_kernel(const CombineParams p)
-{
-    __shared__ float w_s[1024];
-    __shared__ float red[2];
-    const int hq = blockIdx.x, b = blockIdx.y;
-    const KeyRange kr = key_range(p.seq_lens[b], p.window, p.split_blocks);
-    const int ns = min(kr.nsplit, p.num_splits);
-    if (ns <= 1)
-        return;
-    const size_t row = static_cast<size_t>(b) * p.num_q_heads + hq;
-    // split s of this row: lse at [(b*S + s)*H_q + hq], o at that index * D
-    const size_t stride = static_cast<size_t>(p.num_q_heads);
-    const float *lse = p.part_lse + static_cast<size_t>(b) * p.num_splits * stride + hq;
-    if (threadIdx.x == 0) {
-        float M = -INFINITY;
-        for (int s = 0; s < ns; ++s)
-            M = fmaxf(M, lse[s * stride]);
-        float Z = 0.f;
-        for (int s = 0; s < ns && s < 1024; ++s) {
-            const float l = lse[s * stride];
-            const float w = (M == -INFINITY || l == -INFINITY) ? 0.f : expf(l - M);
-            w_s[s] = w;
-            Z += w;
-        }
-        red[0] = Z;
-    }
-    __syncthreads();
-    const float Z = red[0];
-    const float *po = p.part_o + (static_cast<size_t>(b) * p.num_splits * stride + hq) * p.head_dim;
-    for (int d = threadIdx.x; d < p.head_dim; d += blockDim.x) {
-        float acc = 0.f;
-        for (int s = 0; s < ns && s < 1024; ++s)
-            acc = fmaf(w_s[s], po[s * stride * p.head_dim + d], acc);
-        const float y = Z > 0.f ? acc / Z : 0.f;
-        if (p.out_f32)
-            reinterpret_cast<float *>(p.out)[row * p.head_dim + d] = y;
-        else
-            reinterpret_cast<__nv_bfloat16 *>(p.out)[row * p.head_dim + d] = __float2bfloat16_rn(y);
-    }
-}
-
 // ------------------------------------------------------------ host side
 int decode_group_tile(int group)
 {
@@ -904,14 +861,6 @@ cudaError_t launch_decode(const DecodeParams &p, const CUtensorMap &tmk, const C
     case 256: return launch_d<256>(p, tmk, tmv, int8, group_tile, s);
     default: return cudaErrorInvalidValue;
     }
-}
-
-cudaError_t launch_combine(const CombineParams &p, cudaStream_t s)
-{
-    dim3 grid(p.num_q_heads, p.batch);
-    combine_kernel<<<grid, 128, 0, s>>>(p);
-    note_launch();
-    return cudaGetLastError();
 }
 
 }  // namespace pkv

@@ -306,6 +306,48 @@ def test_lse_combine_on_given_partials():
             np.testing.assert_allclose(got[b, h], y, rtol=2e-5, atol=2e-6)
 
 
+@pytest.mark.parametrize("D,max_splits,f32,offset", [
+    (256, 40, False, 0),    # 16-byte columns, two split subsets per column
+    (256, 31, True, 0),
+    (100, 300, False, 1),   # scalar columns (head_dim % 4 != 0), misaligned out
+    (64, 300, True, 1),     # misaligned fp32 out: scalar stores
+    (512, 9, False, 0),     # as many columns as threads
+    (1024, 5, True, 0),     # more columns than threads: two passes
+])
+def test_lse_combine_shapes(D, max_splits, f32, offset):
+    """The combine on oracle partials over its column and split layouts:
+    more splits than threads, rows with fewer or more 16-byte columns than
+    threads, head_dim not a multiple of four, and an output that is not
+    16-byte aligned (element offset)."""
+    rng = np.random.default_rng(D + max_splits)
+    B, Hq, split_tokens = 5, 3, 16
+    nsb = np.array([max_splits, 1, 2, max_splits - 1, 7], np.int64)
+    nsb = np.minimum(nsb, max_splits)
+    lens = (nsb * split_tokens).astype(np.int32)
+    lse = rng.normal(size=(B, Hq, max_splits)).astype(np.float32) * 4
+    po = rng.normal(size=(B, Hq, max_splits, D)).astype(np.float32)
+    dt = torch.float32 if f32 else torch.bfloat16
+    base = torch.zeros(B * Hq * D + offset, dtype=dt, device="cuda")
+    out = base[offset:].view(B, Hq, D)
+    lse_d = _gpu.to_dev(np.ascontiguousarray(lse.transpose(0, 2, 1)))
+    po_d = _gpu.to_dev(np.ascontiguousarray(po.transpose(0, 2, 1, 3)))
+    pkv.paged_decode_lse_combine(lse_d, po_d, _gpu.to_dev(lens), 0, split_tokens, out)
+    torch.cuda.synchronize()
+    got = out.float().cpu().numpy().astype(np.float64)
+    for b in range(B):
+        for h in range(Hq):
+            if nsb[b] <= 1:
+                assert np.all(got[b, h] == 0)  # single-split rows are left untouched
+                continue
+            y, _ = oracle.lse_combine(lse[b, h, :nsb[b]].astype(np.float64),
+                                      po[b, h, :nsb[b]].astype(np.float64))
+            if f32:
+                np.testing.assert_allclose(got[b, h], y, rtol=2e-5, atol=2e-6)
+            else:
+                np.testing.assert_allclose(got[b, h], y, rtol=1 / 128, atol=1e-3)
+    assert base[:offset].float().abs().sum().item() == 0  # nothing written before out
+
+
 def test_bad_block_id_is_reported_not_faulted():
     spec = synth.Spec("badblk", batch=3, num_q_heads=4, num_kv_heads=2, head_dim=64,
                       lens=("fixed", (40, 40, 40)), seed=8)
