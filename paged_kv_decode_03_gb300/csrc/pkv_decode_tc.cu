@@ -35,9 +35,11 @@
 //   warps 4-9 (producers): TMA loads of 128-key tiles into a ring of six
 //     32 KB units.  With K and V separate the ring is split into a K ring
 //     (read only by the score warp) and a V ring (read only by the P.V
-//     warp); with K == V one ring is read by both in the same order.  Each
-//     consumer thus waits on every phase of the slots it reads, which is
-//     what makes parity waits sound.  Producer warp w owns slot w and
+//     warp); with K == V one ring is read by both in the same order, and
+//     only the score warp waits for the loads (the P.V warp reads a unit
+//     after the softmax published P for it, which follows the score MMAs
+//     on it).  Each waiter thus waits on every phase of the slots it reads,
+//     which is what makes parity waits sound.  Producer warp w owns slot w and
 //     issues its uses in order; several issuing warps are needed because
 //     the rate of 2 KB TMA boxes scales with the number of issuing warps.
 //     Producer 0 also loads each item's Q^T (TMA, 128-byte swizzle) into one
@@ -731,10 +733,17 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                 }
                 for (int h = 0; h < HALVES; ++h, ++j) {
                     const int slot = VBASE + j % NVU;
-                    ok = wait_or_abort(&unit_full[slot], (j / NVU) & 1, flags, p.err);
-                    if (!__all_sync(FULL_MASK, ok)) {
-                        ok = false;
-                        break;
+                    // A separate V stream is waited for here.  With K == V the
+                    // score warp waited for the unit, and its MMAs on it came
+                    // before S, P and p_full.  Each half is issued on its own:
+                    // one burst of 16 P.V MMAs delays the next tile's score
+                    // MMAs queued behind it in the tensor pipe.
+                    if (!alias) {
+                        ok = wait_or_abort(&unit_full[slot], (j / NVU) & 1, flags, p.err);
+                        if (!__all_sync(FULL_MASK, ok)) {
+                            ok = false;
+                            break;
+                        }
                     }
                     if (z0b > z0a || z1b > z1a) {
                         uint8_t *ub = units + slot * UNIT;
