@@ -491,6 +491,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     float *mrun_s = reinterpret_cast<float *>(sm + 768);     // [16]
     float *alpha_s = reinterpret_cast<float *>(sm + 832);    // [16]
     float *lse_s = reinterpret_cast<float *>(sm + 896);      // [16] an item's log-sum-exps
+    float *inv_s = reinterpret_cast<float *>(sm + 960);      // [16] an item's 1 / L
     uint8_t *qs = sm + CTRL;
     uint8_t *ps = sm + CTRL + QBYTES;
     uint8_t *units = sm + RING_OFF;
@@ -942,23 +943,45 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             const bool single = whole && it.nsplit == 1;
             const bool f32 = !single || p.out_f32;
             const int slot = lt0 > 0 ? 0 : 1;  // cut at its start: this CTA's first item
+            // per head once: the normaliser 1/L and the log-sum-exp; every
+            // thread then reads the normalisers in four vector loads before
+            // its stores (reading them per head between stores costs one
+            // shared-memory round trip per head, which under the ring's
+            // traffic is several microseconds per item)
+            if (t < NPAD) {
+                const float L = (red[t] + red[16 + t]) + (red[32 + t] + red[48 + t]);
+                inv_s[t] = L > 0.f ? 1.f / L : 0.f;
+                lse_s[t] = L > 0.f ? (mrun_s[t] + log2f(L)) * LN2 : -INFINITY;
+            }
+            asm volatile("bar.sync 1, 128;" ::: "memory");
+            float inv[GP];
+            if constexpr (GP >= 4) {
+#pragma unroll
+                for (int h4 = 0; h4 < GP / 4; ++h4) {
+                    const float4 v = reinterpret_cast<const float4 *>(inv_s)[h4];
+                    inv[4 * h4] = v.x;
+                    inv[4 * h4 + 1] = v.y;
+                    inv[4 * h4 + 2] = v.z;
+                    inv[4 * h4 + 3] = v.w;
+                }
+            } else {
+                const float2 v = *reinterpret_cast<const float2 *>(inv_s);
+                inv[0] = v.x;
+                inv[1] = v.y;
+            }
 #pragma unroll
             for (int h = 0; h < GP; ++h) {
                 if (h >= G)
                     continue;
-                const float L = (red[h] + red[16 + h]) + (red[32 + h] + red[48 + h]);
-                const float inv = L > 0.f ? 1.f / L : 0.f;
 #pragma unroll
                 for (int hv = 0; hv < HALVES; ++hv) {
                     const int d = hv * 128 + t;
-                    const float y = oacc[hv][h] * inv;
+                    const float y = oacc[hv][h] * inv[h];
                     if (f32)
                         reinterpret_cast<float *>(ps)[h * D + d] = y;
                     else
                         reinterpret_cast<__nv_bfloat16 *>(ps)[h * D + d] = __float2bfloat16_rn(y);
                 }
-                if (t == h)
-                    lse_s[h] = L > 0.f ? (mrun_s[h] + log2f(L)) * LN2 : -INFINITY;
             }
             fence_proxy_async_smem();
             asm volatile("bar.sync 1, 128;" ::: "memory");
