@@ -141,6 +141,41 @@ __device__ __forceinline__ bool softmax_any(bool pred)
     return r != 0;
 }
 
+// Sums over the 32 lanes of N values (N = 2..16) by halving exchanges: a
+// lane keeps one half of its values and sends the other, so the whole
+// reduction takes N - 1 + 5 - log2(N) shuffles instead of 5N.  Returns the
+// full sum of value `head`, a function of the lane: lanes that differ only
+// in their low 5 - log2(N) bits hold the same head.
+template <int N>
+__device__ __forceinline__ float warp_sum_scatter(const float (&in)[N], int lane, int &head)
+{
+    static_assert(N == 2 || N == 4 || N == 8 || N == 16, "N");
+    constexpr int STEPS = N == 2 ? 1 : N == 4 ? 2 : N == 8 ? 3 : 4;
+    float v[N];
+#pragma unroll
+    for (int i = 0; i < N; ++i)
+        v[i] = in[i];
+    head = 0;
+#pragma unroll
+    for (int k = 0; k < STEPS; ++k) {
+        const int o = 16 >> k;
+        const bool up = (lane & o) != 0;
+        const int half = N >> (k + 1);
+#pragma unroll
+        for (int i = 0; i < half; ++i) {
+            const float send = up ? v[i] : v[i + half];
+            const float keep = up ? v[i + half] : v[i];
+            v[i] = keep + __shfl_xor_sync(FULL_MASK, send, o);
+        }
+        head = (head << 1) | (up ? 1 : 0);
+    }
+    float r = v[0];
+#pragma unroll
+    for (int o = 16 >> STEPS; o > 0; o >>= 1)
+        r += __shfl_xor_sync(FULL_MASK, r, o);
+    return r;
+}
+
 // Virtual tiles charged per item for its fixed cost (about two tiles of
 // streaming: the wait for the last P.V and the write of the result).
 constexpr int KAPPA = 2;
@@ -526,6 +561,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         for (int idx = threadIdx.x; idx < PBYTES / 16; idx += 128)
             reinterpret_cast<uint4 *>(ps)[idx] = make_uint4(0u, 0u, 0u, 0u);
         fence_proxy_async_smem();
+        if (threadIdx.x < NPAD)
+            mrun_s[threadIdx.x] = -INFINITY;  // the first item's running max
     }
     __syncthreads();
     tc_fence_after();
@@ -821,9 +858,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                 for (int hv = 0; hv < HALVES; ++hv)
                     oacc[hv][h] = 0.f;
             }
-            if (t < 16)
-                mrun_s[t] = -INFINITY;
-            asm volatile("bar.sync 1, 128;" ::: "memory");
+            // mrun_s was reset by the previous item's epilogue (or the set-up)
             const int32_t *bt_row = p.block_table + static_cast<size_t>(it.b) * p.max_blocks + it.ub0;
             int phys_next = (lt0 * 8 + (t >> 4)) < it.n ? __ldg(bt_row + lt0 * 8 + (t >> 4)) : -1;
             for (int i = lt0; i < lt1; ++i, ++i_g) {
@@ -916,24 +951,25 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                             oacc[hv][h] *= alpha_s[h];
                 }
             }
-            if (lt1 > lt0)
-                accumulate_o(i_g - 1);
-
-            // ---- sums over the 128 keys of each head, then this item's result
-#pragma unroll
-            for (int h = 0; h < GP; ++h) {
-                float v = lpart[h];
-#pragma unroll
-                for (int off = 16; off > 0; off >>= 1)
-                    v += __shfl_xor_sync(FULL_MASK, v, off);
-                lpart[h] = v;
-            }
-            if (lane == 0) {
-#pragma unroll
-                for (int h = 0; h < GP; ++h)
-                    red[warp * 16 + h] = lpart[h];
+            // ---- sums over the 128 keys of each head, 1/L and the
+            // log-sum-exp: lpart and the running max are final once the last
+            // tile's P is formed, so this overlaps that tile's P.V
+            {
+                int hh;
+                const float v = warp_sum_scatter<GP>(lpart, lane, hh);
+                if ((lane & (32 / GP - 1)) == 0)
+                    red[warp * 16 + hh] = v;
             }
             asm volatile("bar.sync 1, 128;" ::: "memory");
+            if (t < GP) {
+                const float L = (red[t] + red[16 + t]) + (red[32 + t] + red[48 + t]);
+                inv_s[t] = L > 0.f ? 1.f / L : 0.f;
+                lse_s[t] = L > 0.f ? (mrun_s[t] + log2f(L)) * LN2 : -INFINITY;
+                mrun_s[t] = -INFINITY;  // the next item's running max
+            }
+            asm volatile("bar.sync 1, 128;" ::: "memory");
+            if (lt1 > lt0)
+                accumulate_o(i_g - 1);
             // whole item: the output when the sequence has one split, else the
             // split's partial; a piece of an item: this CTA's partial state.
             // The G x D results are staged in the P^T buffers (idle between an
@@ -943,17 +979,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             const bool single = whole && it.nsplit == 1;
             const bool f32 = !single || p.out_f32;
             const int slot = lt0 > 0 ? 0 : 1;  // cut at its start: this CTA's first item
-            // per head once: the normaliser 1/L and the log-sum-exp; every
-            // thread then reads the normalisers in four vector loads before
-            // its stores (reading them per head between stores costs one
+            // every thread reads the normalisers in vector loads before its
+            // stores (reading them per head between stores costs one
             // shared-memory round trip per head, which under the ring's
             // traffic is several microseconds per item)
-            if (t < NPAD) {
-                const float L = (red[t] + red[16 + t]) + (red[32 + t] + red[48 + t]);
-                inv_s[t] = L > 0.f ? 1.f / L : 0.f;
-                lse_s[t] = L > 0.f ? (mrun_s[t] + log2f(L)) * LN2 : -INFINITY;
-            }
-            asm volatile("bar.sync 1, 128;" ::: "memory");
             float inv[GP];
             if constexpr (GP >= 4) {
 #pragma unroll
