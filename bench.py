@@ -386,8 +386,13 @@ def run_ours(args, rank, world, local_rank):
             bt.copy_(pin["bt"], non_blocking=True)
             sl.copy_(pin["sl"], non_blocking=True)
             pkv.paged_kv_append(k_new, v_new, slots, pool)
-            pkv.paged_decode_attention(q, pool, bt, sl, spec.window, scale, out, max_len,
-                                       split_tokens=st, workspace=ws)
+            if split_api:  # the same calls as the device-timed step
+                pkv.paged_decode_split_partial(q, pool, bt, sl, spec.window, scale, st, lse, po,
+                                               out, max_len, workspace=pws)
+                pkv.paged_decode_lse_combine(lse, po, sl, spec.window, st, out)
+            else:
+                pkv.paged_decode_attention(q, pool, bt, sl, spec.window, scale, out, max_len,
+                                           split_tokens=st, workspace=ws)
             out_h.copy_(out, non_blocking=True)
 
         for _ in range(max(3, args.warmup)):
@@ -410,7 +415,9 @@ def run_ours(args, rank, world, local_rank):
         e2e = {"value": world * step_bytes / (e2e_ms / args.steps * 1e-3) / 1e9, "unit": "GB/s",
                "ms_per_step": e2e_ms / args.steps, "h2d_bytes_per_step": int(h2d),
                "d2h_bytes_per_step": int(d2h),
-               "api": "paged_kv_append + paged_decode_attention (C ABI), pinned host buffers"}
+               "api": ("paged_kv_append + paged_decode_split_partial + paged_decode_lse_combine"
+                       if split_api else "paged_kv_append + paged_decode_attention")
+                      + " (C ABI), pinned host buffers"}
 
     if rank != 0:
         return None
