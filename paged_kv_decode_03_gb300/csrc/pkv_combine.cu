@@ -13,7 +13,9 @@
 // subsets of the splits, with eight loads in flight per thread; the subsets
 // are summed through shared memory.  The work is a few hundred kilobytes
 // per sequence, so the kernel is latency-bound: what matters is how many
-// dependent memory round trips a CTA makes (two).
+// dependent memory round trips a CTA makes.  The first batch of partial
+// loads is issued before the weights are formed, so rows of up to 8 x
+// (threads / columns) splits (16 at head_dim 256) take one.
 #include <cuda_bf16.h>
 #include <math.h>
 #include <stdint.h>
@@ -85,6 +87,36 @@ __global__ void __launch_bounds__(CT) combine_kernel(const CombineParams p)
     const float *po = p.part_o + (static_cast<size_t>(b) * p.num_splits * stride + hq) * D;
     const size_t sstride = stride * D;  // floats between splits of one row
 
+    // column layout: 16-byte columns when the row and the pointers allow
+    const uintptr_t oa = reinterpret_cast<uintptr_t>(p.out);
+    const bool vec = (D & 3) == 0 && (reinterpret_cast<uintptr_t>(p.part_o) & 15) == 0 &&
+                     (oa & (p.out_f32 ? 15 : 7)) == 0;
+    const int nq = vec ? D / 4 : D;              // columns: float4 or scalar
+    const int groups = nq >= CT ? 1 : CT / nq;   // interleaved split subsets
+    const int g = tid / (nq >= CT ? CT : nq);
+    const size_t row = static_cast<size_t>(b) * p.num_q_heads + hq;
+    // INFLIGHT partial values of column c from splits s0, s0 + groups, ...
+    auto load_batch = [&](int c, int s0, float4 (&v)[INFLIGHT]) {
+#pragma unroll
+        for (int k = 0; k < INFLIGHT; ++k) {
+            const int s = s0 + k * groups;
+            if (s < ns) {
+                if (vec)
+                    v[k] = *reinterpret_cast<const float4 *>(po + s * sstride + c * 4);
+                else
+                    v[k] = make_float4(po[s * sstride + c], 0.f, 0.f, 0.f);
+            } else {
+                v[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+        }
+    };
+    // the first batch is in flight while the weights are formed: one memory
+    // round trip fewer for rows of up to INFLIGHT x groups splits
+    const bool mine = g < groups;
+    float4 first[INFLIGHT];
+    if (mine && (nq >= CT ? tid : tid % nq) < nq)
+        load_batch(nq >= CT ? tid : tid % nq, g, first);
+
     // ---- weights: L = max lse, w_s = exp(lse_s - L), Z = sum w_s
     float m = -INFINITY;
     for (int s = tid; s < ns; s += CT) {
@@ -103,31 +135,18 @@ __global__ void __launch_bounds__(CT) combine_kernel(const CombineParams p)
     const float Z = block_reduce<false>(z, red);  // its barriers publish w_s
 
     // ---- weighted sum of the normalised partials
-    const uintptr_t oa = reinterpret_cast<uintptr_t>(p.out);
-    const bool vec = (D & 3) == 0 && (reinterpret_cast<uintptr_t>(p.part_o) & 15) == 0 &&
-                     (oa & (p.out_f32 ? 15 : 7)) == 0;
-    const int nq = vec ? D / 4 : D;              // columns: float4 or scalar
-    const int groups = nq >= CT ? 1 : CT / nq;   // interleaved split subsets
-    const int g = tid / (nq >= CT ? CT : nq);
-    const size_t row = static_cast<size_t>(b) * p.num_q_heads + hq;
     for (int c0 = 0; c0 < nq; c0 += CT) {
         const int c = c0 + (nq >= CT ? tid : tid % nq);
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (g < groups && c < nq) {
+        if (mine && c < nq) {
             for (int s0 = g; s0 < ns; s0 += INFLIGHT * groups) {
                 float4 v[INFLIGHT];
+                if (c0 == 0 && s0 == g) {
 #pragma unroll
-                for (int k = 0; k < INFLIGHT; ++k) {
-                    const int s = s0 + k * groups;
-                    if (s < ns) {
-                        if (vec) {
-                            v[k] = *reinterpret_cast<const float4 *>(po + s * sstride + c * 4);
-                        } else {
-                            v[k] = make_float4(po[s * sstride + c], 0.f, 0.f, 0.f);
-                        }
-                    } else {
-                        v[k] = make_float4(0.f, 0.f, 0.f, 0.f);
-                    }
+                    for (int k = 0; k < INFLIGHT; ++k)
+                        v[k] = first[k];
+                } else {
+                    load_batch(c, s0, v);
                 }
 #pragma unroll
                 for (int k = 0; k < INFLIGHT; ++k) {
