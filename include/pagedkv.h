@@ -32,9 +32,14 @@
  *    pkv_last_error()); a positive cudaError_t when a launch fails.
  *  - Errors the host cannot see (a block id outside the pool, a length
  *    beyond the block table or beyond max_seq_len, a slot outside the pool)
- *    are detected in the kernels: the offending keys or tokens are skipped
- *    and a bit is set in the device error word, read with
- *    pkv_device_status() after the stream has been synchronised.
+ *    are detected in the kernels and set a bit in the device error word,
+ *    read with pkv_device_status() after the stream has been synchronised.
+ *    Nothing outside the pool or the block table is read or written: keys
+ *    past the block table and tokens with a slot outside the pool are
+ *    skipped; a block id outside the pool is never dereferenced (the
+ *    CUDA-core kernel skips its keys, the tensor-core kernel reads them as
+ *    zero vectors), so the output of a sequence that names one is
+ *    unspecified.  Other sequences are unaffected.
  */
 #ifndef PAGEDKV_H
 #define PAGEDKV_H

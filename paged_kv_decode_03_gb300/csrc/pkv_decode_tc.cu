@@ -859,18 +859,14 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                     oacc[hv][h] = 0.f;
             }
             // mrun_s was reset by the previous item's epilogue (or the set-up)
-            const int32_t *bt_row = p.block_table + static_cast<size_t>(it.b) * p.max_blocks + it.ub0;
-            int phys_next = (lt0 * 8 + (t >> 4)) < it.n ? __ldg(bt_row + lt0 * 8 + (t >> 4)) : -1;
             for (int i = lt0; i < lt1; ++i, ++i_g) {
                 const int sb = i_g & 1;
-                const int blk = i * 8 + (t >> 4);
-                const int phys = phys_next;
-                {
-                    const int nb = (i + 1) * 8 + (t >> 4);
-                    phys_next = (i + 1 < lt1 && nb < it.n) ? __ldg(bt_row + nb) : -1;
-                }
-                const bool loaded =
-                    blk < it.n && static_cast<unsigned>(phys) < static_cast<unsigned>(p.num_blocks);
+                // key t of the tile: inside the item's blocks and in [lo, pos].
+                // A block id outside the pool is not read here: the producer
+                // reports it and its box arrives as zeros (keys of score 0,
+                // V rows 0), so only that sequence's output is affected; no
+                // global load stands in the softmax's path.
+                const bool loaded = i * 8 + (t >> 4) < it.n;
                 const int jk = (it.ub0 + i * 8) * kBlock + t;
                 const bool ok = loaded && jk >= it.lo && jk <= it.pos;
                 // ---- scores

@@ -368,6 +368,49 @@ def test_bad_block_id_is_reported_not_faulted():
     assert _gpu.max_abs_err(got[[0, 2]], ref[[0, 2]]) <= BF16_TOL
 
 
+@pytest.mark.parametrize("alias", [True, False])
+def test_bad_block_id_tensor_core_path(alias):
+    """A block id outside the pool on the tensor-core path: reported, never
+    dereferenced (its box reads as zeros), the sequence's own output finite
+    but unspecified, the other sequences exact; single pass and splits."""
+    spec = synth.Spec("badblk_tc", batch=3, num_q_heads=16, num_kv_heads=1, head_dim=128,
+                      lens=("fixed", (700, 700, 700)), alias=alias, seed=18)
+    w = synth.make_workload(spec)
+    gp = _gpu.device_pool(w)
+    assert pkv.uses_tensor_cores(gp, spec.num_q_heads)
+    _gpu.append_all(w, gp)
+    op = _util.oracle_pool(w)
+    ref = _util.oracle_decode(w, op)
+    step = _gpu.DeviceStep(w)
+    bt = w.block_table.copy()
+    bt[1, 20] = w.layout.num_blocks + 1000
+    step.block_table = _gpu.to_dev(bt)
+    # single pass
+    pkv.device_status(clear=True)
+    got = _gpu.out_to_f64(step.decode(gp, split_tokens=0))
+    torch.cuda.synchronize()
+    assert pkv.device_status(clear=True) & 1  # PKV_DEV_BAD_BLOCK
+    assert np.isfinite(got[1]).all()
+    assert _gpu.max_abs_err(got[[0, 2]], ref[[0, 2]]) <= BF16_TOL
+    # split partials and the combine
+    split = 256
+    ns = pkv.paged_decode_num_splits(step.max_seq_len, spec.window, split)
+    B, Hq, D = w.q.shape
+    lse = torch.empty((B, ns, Hq), device="cuda")
+    po = torch.empty((B, ns, Hq, D), device="cuda")
+    out = torch.zeros((B, Hq, D), dtype=torch.bfloat16, device="cuda")
+    pkv.device_status(clear=True)
+    pkv.paged_decode_split_partial(step.q, gp, step.block_table, step.seq_lens, spec.window,
+                                   np.float32(spec.softmax_scale), split, lse, po, out,
+                                   step.max_seq_len)
+    pkv.paged_decode_lse_combine(lse, po, step.seq_lens, spec.window, split, out)
+    torch.cuda.synchronize()
+    assert pkv.device_status(clear=True) & 1
+    got = _gpu.out_to_f64(out)
+    assert np.isfinite(got[1]).all()
+    assert _gpu.max_abs_err(got[[0, 2]], ref[[0, 2]]) <= BF16_TOL
+
+
 def test_bad_slot_is_reported_not_faulted():
     spec = synth.Spec("badslot", batch=2, num_q_heads=2, num_kv_heads=2, head_dim=64,
                       lens=("fixed", (5, 5)), seed=9)
