@@ -6,8 +6,9 @@
 // over the keys [lo, pos] of each sequence ("CS336 · 第 10 课", KV-cache
 // section; "实验五：Gemma4 端到端推理优化", sliding-window, GQA and Flash
 // Attention sections: online softmax with running max/sum in fp32, blocks
-// outside the window never read; the split-KV log-sum-exp merge of the
-// flash-decoding design those pages describe).
+// outside the window never read).  Partial states of one key range, cut
+// between CTAs or split by the caller, merge by the same max/sum recurrence
+// ("LLM推理优化底层原理" §3.1 step 2) in log-sum-exp form.
 //
 // Why tensor cores here: at head_dim 256 the bf16 inner products of 8-16
 // query heads cost the CUDA cores more issue slots than HBM needs time to
@@ -21,15 +22,15 @@
 // the result is written), form one sequence of W units.
 // tc_plan_kernel (one CTA) scans the lengths and gives CTA c the units
 // [c*W/C, (c+1)*W/C), C = min(grid, W): it records the first item with real
-// tiles there (or an empty item starting there).  A CTA walks its items in order with one pipeline that never
-// drains between them; an item it covers entirely is finished in place (the
-// output, or that split's partial state), an item cut at a CTA boundary
-// leaves one partial state per CTA (log-sum-exp and normalised o), which the
-// CTA holding its last part merges once the others have published theirs
-// (merge_cut_item).  Every SM gets the same number of tiles within
-// one, whatever the mix of lengths, and the per-CTA start-up and drain
-// (TMEM allocation, first loads, last softmax and P.V) are paid once per SM
-// instead of once per item.
+// tiles there (or an empty item starting there).  A CTA walks its items in
+// order with one pipeline that never drains between them; an item it covers
+// entirely is finished in place (the output, or that split's partial state),
+// an item cut at a CTA boundary leaves one partial state per CTA
+// (log-sum-exp and normalised o), which the CTA holding its last part merges
+// once the others have published theirs (merge_cut_item).  Every SM gets the
+// same number of tiles within one, whatever the mix of lengths, and the
+// per-CTA start-up and drain (TMEM allocation, first loads, last softmax and
+// P.V) are paid once per SM instead of once per item.
 //
 // One CTA per SM, 12 warps:
 //   warps 4-9 (producers): TMA loads of 128-key tiles into a ring of six
@@ -50,7 +51,8 @@
 //     tcgen05.commit signals the mbarriers that free ring units, Q buffers
 //     and hand results on.
 //   warps 0-3 (softmax): thread t owns key t of the tile (TMEM lane t):
-//     loads its 16 scores, masks keys outside [lo, pos], forms the tile max
+//     loads its 16 scores, masks keys outside [lo, pos] (from the item's
+//     geometry alone: the softmax reads no block table), forms the tile max
 //     per head (warp shuffles + one exchange through shared memory), keeps
 //     running max / sums in fp32, writes P^T in bf16 (K-major, swizzled)
 //     for the P.V MMA -- for fp32 output also the bf16 residual p - bf16(p),
