@@ -177,6 +177,24 @@ class ClockSampler:
 
 
 # ------------------------------------------------------------- our arm
+def max_over_ranks(x: float, world: int, device) -> float:
+    """The largest value of x over all ranks (the job's time is its slowest
+    rank's); x itself on one rank."""
+    if world <= 1:
+        return x
+    import torch
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_gbs(bytes_per_rank_step: float, ms_per_step: float, world: int) -> float:
+    """Whole-job throughput: every rank moves bytes_per_rank_step per step
+    (weak scaling, one independent batch per GPU) and a step takes the slowest
+    rank's ms_per_step."""
+    return world * bytes_per_rank_step / (ms_per_step * 1e-3) / 1e9
+
+
 def run_ours(args, rank, world, local_rank):
     import torch
     import paged_kv_decode_03_gb300 as pkv
@@ -345,18 +363,14 @@ def run_ours(args, rank, world, local_rank):
     if world > 1:
         torch.distributed.barrier()
     clocks = sampler.stop(t0, t1) if sampler else None
-    elapsed_ms = start.elapsed_time(end)
-    if world > 1:
-        tm = torch.tensor([elapsed_ms], device=dev)
-        torch.distributed.all_reduce(tm, op=torch.distributed.ReduceOp.MAX)
-        elapsed_ms = float(tm.item())
+    elapsed_ms = max_over_ranks(start.elapsed_time(end), world, dev)
     status = pkv.device_status(clear=True)
     app_us = statistics.mean(e[0].elapsed_time(e[1]) for e in evs) * 1e3
     dec_us = statistics.mean(e[1].elapsed_time(e[2]) for e in evs) * 1e3
     cmb_us = (statistics.mean(e[2].elapsed_time(e[3]) for e in evs) * 1e3
               if parts[2] is not None else 0.0)
     ms_per_step = elapsed_ms / args.steps
-    value = world * step_bytes / (ms_per_step * 1e-3) / 1e9
+    value = whole_job_gbs(step_bytes, ms_per_step, world)
 
     # ---- end to end through the C ABI with host buffers
     e2e = None
@@ -407,12 +421,8 @@ def run_ours(args, rank, world, local_rank):
             e2e_step()
         e2.record()
         torch.cuda.synchronize()
-        e2e_ms = s2.elapsed_time(e2)
-        if world > 1:
-            tm = torch.tensor([e2e_ms], device=dev)
-            torch.distributed.all_reduce(tm, op=torch.distributed.ReduceOp.MAX)
-            e2e_ms = float(tm.item())
-        e2e = {"value": world * step_bytes / (e2e_ms / args.steps * 1e-3) / 1e9, "unit": "GB/s",
+        e2e_ms = max_over_ranks(s2.elapsed_time(e2), world, dev)
+        e2e = {"value": whole_job_gbs(step_bytes, e2e_ms / args.steps, world), "unit": "GB/s",
                "ms_per_step": e2e_ms / args.steps, "h2d_bytes_per_step": int(h2d),
                "d2h_bytes_per_step": int(d2h),
                "api": ("paged_kv_append + paged_decode_split_partial + paged_decode_lse_combine"
