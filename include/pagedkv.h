@@ -206,7 +206,13 @@ PKV_API size_t paged_decode_partial_workspace_bytes(int32_t batch, int32_t num_q
  *                 across SMs itself and ignores it (same result up to
  *                 rounding).
  *   workspace:    device scratch of paged_decode_workspace_bytes(...) bytes,
- *                 256-byte aligned (NULL allowed when that is 0).
+ *                 256-byte aligned.  Required (PKV_E_WORKSPACE without it)
+ *                 when the call splits the key ranges or runs on the
+ *                 tensor-core kernel (paged_decode_uses_tensor_cores);
+ *                 optional for a single pass on the CUDA-core kernel, which
+ *                 then takes the sequences in batch order instead of longest
+ *                 first.  Calls on one stream may share it; concurrent calls
+ *                 may not.
  *   out:          [batch][num_q_heads][head_dim], bf16 (out_dtype
  *                 PKV_OUT_BF16) or fp32 (PKV_OUT_F32), 16-byte aligned.
  */
