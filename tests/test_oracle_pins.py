@@ -433,3 +433,20 @@ def test_decode_bytes_counts_window_keys_once():
     wg = synth.make_workload(g)
     dg = bm.decode_bytes(g, wg.seq_lens, wg.block_table)
     assert dg["keys"] - dg["unique_keys"] == 3 * 8 * 16
+
+
+def test_bytes_per_key_of_the_workloads():
+    """Per-key algorithmic bytes: K and V rows of every kv head (one tensor
+    when K == V), plus the int8 per-token scales; per-head scales count once
+    per launch."""
+    from paged_kv_decode_03_gb300 import bytes_model as bm
+    assert bm.bytes_per_key(8, 256, "bf16", False) == 8192        # Gemma4 sliding layer
+    assert bm.bytes_per_key(1, 256, "bf16", True) == 512          # Gemma4 global, K == V
+    assert bm.bytes_per_key(40, 128, "int8_token", False) == 10240 + 8  # Llama-2-13B-like
+    assert bm.bytes_per_key(8, 256, "int8_head", False) == 4096
+    spec = synth.shrink(synth.C5_SLIDING, batch=2, lens=("fixed", (20, 40)),
+                        shared_prefix_seqs=0)
+    w = synth.make_workload(spec)
+    d = bm.decode_bytes(spec, w.seq_lens, w.block_table)
+    assert d["kv"] == d["unique_keys"] * 4096 + 2 * spec.num_kv_heads * 4
+    assert d["q"] == 2 * spec.num_q_heads * spec.head_dim * 2
