@@ -127,8 +127,11 @@ typedef struct pkv_pool {
  *   bf16 pool: bit copy.  int8 per token: scale = max|x| / 127 over the
  *   token's num_kv_heads*head_dim values (fp32, IEEE division), stored at
  *   scale[slot]; q = clamp(round_half_even(x / scale), -127, 127); a zero
- *   scale stores zeros.  int8 per head: the same rounding with the caller's
- *   static scale[h].  K and V are quantised separately.
+ *   scale stores zeros.  Non-finite inputs: NaN is ignored by max|x| and
+ *   stored as code 0; +-inf makes the token's scale inf (every code of that
+ *   token 0) or, under a per-head scale, saturates to +-127.  int8 per
+ *   head: the same rounding with the caller's static scale[h].  K and V are
+ *   quantised separately.
  *   Tokens that map to the same slot race (the last writer is unspecified).
  */
 PKV_API int paged_kv_append(const void *k, const void *v, const int64_t *slot_mapping,
@@ -279,7 +282,11 @@ PKV_API int paged_decode_lse_combine(const float *partial_lse, const float *part
  *   Nothing here calls cudaMalloc, cudaFree or any allocating routine.
  *   The first call on a device looks the array's address up on that device
  *   (cudaGetSymbolAddress, the device current); make that first call before
- *   any stream capture.  All calls share the one array and it keeps the
+ *   any stream capture.  The address is kept for the life of the process:
+ *   after cudaDeviceReset (or any reset of the device's primary context) the
+ *   array is gone and this entry point must not be called again.  The same
+ *   holds for every call of this library, which caches the address of its
+ *   device error word the same way.  All calls share the one array and it keeps the
  *   previous call's contents (no part of it needs to start at zero: every
  *   partial is written before it is read), so calls that overlap on the GPU
  *   -- on two streams, or from two threads -- race and must be serialised by

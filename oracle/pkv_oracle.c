@@ -73,13 +73,17 @@ static float bf16_bits_to_float(uint16_t b)
 /* Quantiser ([CS336-L10] quantisation: scale = max(abs(x))/127,            */
 /* x_q = round(x/scale)).  Readings: round = IEEE round-half-to-even; the   */
 /* result is saturated to [-127, 127] (a static per-head scale can be       */
-/* exceeded); a zero scale quantises everything to 0.                       */
+/* exceeded); a zero scale quantises everything to 0; a quotient that is    */
+/* not a number (a NaN input, or inf/inf under an infinite per-token scale) */
+/* has no code and is stored as 0 (the pages are silent on non-finite x).   */
 /* ------------------------------------------------------------------------ */
 static int8_t quantize_one(float x, float scale)
 {
     if (scale == 0.0f)
         return 0;
     float y = x / scale;     /* one IEEE fp32 division */
+    if (isnan(y))
+        return 0;
     float r = nearbyintf(y); /* default rounding mode: half to even */
     if (r > 127.0f)
         r = 127.0f;

@@ -701,9 +701,19 @@ extern "C" PKV_API int paged_decode_attention_noalloc(
                                                  split_tokens);
     if (st < 0)
         return st;
-    const size_t need = paged_decode_workspace_bytes(batch, num_q_heads, pool->num_kv_heads,
-                                                     pool->head_dim, pool->block_size,
-                                                     max_seq_len, window, st);
+    // The scratch paged_decode_attention itself needs on the path it takes:
+    // the tensor-core kernel's scratch (it balances the key ranges itself
+    // and ignores the split length), the split partials on the CUDA-core
+    // kernel, or the optional length order of a CUDA-core single pass.
+    size_t need;
+    if (use_tc(pool, num_q_heads / pool->num_kv_heads))
+        need = decode_tc_scratch_bytes(batch, pool->head_dim);
+    else if (st > 0)
+        need = paged_decode_workspace_bytes(batch, num_q_heads, pool->num_kv_heads,
+                                            pool->head_dim, pool->block_size, max_seq_len,
+                                            window, st);
+    else
+        need = batch > 0 ? (2 * sizeof(int32_t) * (size_t)batch + 255) / 256 * 256 : 0;
     if (need > kStaticScratchBytes)
         return fail(PKV_E_WORKSPACE,
                     "these sizes need %zu bytes of scratch but the static scratch holds %zu "
@@ -713,6 +723,8 @@ extern "C" PKV_API int paged_decode_attention_noalloc(
     void *ws = nullptr;
     if (need > 0 && !(ws = static_scratch_ptr()))
         return PKV_E_DRIVER;
+    // The whole array is offered: on each path paged_decode_attention
+    // checks the workspace against the same figure as `need` above.
     return paged_decode_attention(q, pool, block_table, max_blocks_per_seq, seq_lens, batch,
                                   num_q_heads, max_seq_len, window, softmax_scale, st, ws,
                                   need > 0 ? kStaticScratchBytes : 0, out, out_dtype, stream);

@@ -21,11 +21,17 @@ namespace pkv {
 
 constexpr int APPEND_THREADS = 128;
 
+// Code of x under scale: round half to even, saturated to [-127, 127]; a
+// zero scale gives 0, and so does a quotient that is not a number (a NaN
+// input, or inf / inf when the token's scale is infinite).
 __device__ __forceinline__ int8_t quantize_one(float x, float scale)
 {
     if (scale == 0.f)
         return 0;
-    int r = __float2int_rn(__fdiv_rn(x, scale));
+    const float y = __fdiv_rn(x, scale);
+    if (y != y)
+        return 0;
+    int r = __float2int_rn(y);
     r = max(-127, min(127, r));
     return static_cast<int8_t>(r);
 }

@@ -18,22 +18,21 @@
 // Work decomposition (stream-K).  An item is one (sequence, kv head, split)
 // key range (one split when the caller does not split); the 128-key tiles of
 // all items, in (sequence, kv head, split, tile) order, each item followed by
-// KAPPA virtual tiles that stand for its fixed cost (the last P.V drains and
-// the result is written), form one sequence of W units.
-// tc_plan_kernel (one CTA) scans the lengths and gives CTA c the units
-// [c*W/C, (c+1)*W/C), C = min(grid, W): it records the first item with real
-// tiles there (or an empty item starting there).  A CTA walks its items in
-// order with one pipeline that never drains between them; an item it covers
-// entirely is finished in place (the output, or that split's partial state),
-// an item cut at a CTA boundary leaves one partial state per CTA
-// (log-sum-exp and normalised o), which the CTA holding its last part merges
-// once the others have published theirs (merge_cut_item).  Every SM gets the
-// same number of tiles within one, whatever the mix of lengths, and the
-// per-CTA start-up and drain (TMEM allocation, first loads, last softmax and
-// P.V) are paid once per SM instead of once per item.
+// KAPPA virtual tiles that stand for its fixed cost, form one sequence of W
+// units.  tc_plan_kernel (one CTA) scans the lengths and gives CTA c the
+// units [c*W/C, (c+1)*W/C), C = min(grid, W): it records the first item with
+// real tiles there (or an empty item starting there).  A CTA walks its items
+// in order with one pipeline that never drains between them; an item it
+// covers entirely is finished in place (the output, or that split's partial
+// state), an item cut at CTA boundaries leaves one partial state per CTA
+// (log-sum-exp and normalised o) and a ticket: the part that finishes last
+// merges them.  No CTA waits for another.  Every SM gets the same number of
+// units within one, whatever the mix of lengths, and the per-CTA start-up
+// (TMEM allocation, first loads) is paid once per SM instead of once per
+// item.
 //
-// One CTA per SM, 12 warps:
-//   warps 4-9 (producers): TMA loads of 128-key tiles into a ring of six
+// One CTA per SM, 16 warps:
+//   warps 8-13 (producers): TMA loads of 128-key tiles into a ring of six
 //     32 KB units.  With K and V separate the ring is split into a K ring
 //     (read only by the score warp) and a V ring (read only by the P.V
 //     warp); with K == V one ring is read by both in the same order, and
@@ -45,23 +44,30 @@
 //     the rate of 2 KB TMA boxes scales with the number of issuing warps.
 //     Producer 0 also loads each item's Q^T (TMA, 128-byte swizzle) into one
 //     of two buffers.
-//   warp 10 (one thread): S^T[128 keys x 16] = K Q^T (M=128, N=16 query
+//   warp 14 (one thread): S^T[128 keys x 16] = K Q^T (M=128, N=16 query
 //     heads padded, K=16 per instruction) into TMEM;
-//   warp 11 (one thread): O^T[128 dims x 16] = V^T P^T per 128-dim half.
-//     tcgen05.commit signals the mbarriers that free ring units, Q buffers
-//     and hand results on.
+//   warp 15 (one thread): O^T[128 dims x 16] += V^T P^T per 128-dim half,
+//     accumulated in TMEM over all tiles of an item (two O buffers, one per
+//     item in flight).  tcgen05.commit signals the mbarriers that free ring
+//     units, Q and P buffers and hand a finished item to the epilogue.
 //   warps 0-3 (softmax): thread t owns key t of the tile (TMEM lane t):
 //     loads its 16 scores, masks keys outside [lo, pos] (from the item's
-//     geometry alone: the softmax reads no block table), forms the tile max
-//     per head (warp shuffles + one exchange through shared memory), keeps
-//     running max / sums in fp32, writes P^T in bf16 (K-major, swizzled)
-//     for the P.V MMA -- for fp32 output also the bf16 residual p - bf16(p),
-//     multiplied in a second pass, which keeps the error near 2^-17 -- and
-//     accumulates the per-tile O^T (thread t owns output dims t and 128+t)
-//     with the rescale alpha = 2^(m_old - m_new).
-//     The P.V warp zeroes the V rows of masked keys inside loaded blocks
-//     (stale slots past pos, keys before the window start) before its MMAs
-//     read them, so no stale value (not even a NaN) reaches the output.
+//     geometry alone: the softmax reads no block table), keeps running max /
+//     sums in fp32 and writes P^T in bf16 (K-major, swizzled) for the P.V
+//     MMA -- for fp32 output also the bf16 residual p - bf16(p), multiplied
+//     in a second pass, which keeps the error near 2^-17.  The running max
+//     changes only when a score exceeds it by more than 2^8 (any reference
+//     at least the true maximum minus 8 gives the same result and keeps
+//     p <= 256); when it changes after an item's first tile, the softmax
+//     scales the item's O in TMEM by 2^(m_old - m_new) once the previous
+//     tile's P.V is done, before it publishes the new P.
+//   warps 4-7 (epilogue): per item, once its last P.V is done, read O^T from
+//     TMEM (thread t owns output dims t and 128+t), divide by the sum, and
+//     store the output row, the split's partial state, or this CTA's part of
+//     a cut item -- off the softmax's path, while the next item streams.
+//   The P.V warp zeroes the V rows of masked keys inside loaded blocks
+//   (stale slots past pos, keys before the window start) before its MMAs
+//   read them, so no stale value (not even a NaN) reaches the output.
 //   Q^T rows past the group hold other heads' queries (or zeros past the
 //   end of q); their score columns are masked and their P^T rows stay zero.
 #include <cuda_bf16.h>
@@ -76,8 +82,10 @@ namespace pkv {
 
 namespace {
 
+constexpr int SOFTMAX_WARPS = 4;   // warps 0-3; TMEM lanes 0-127
+constexpr int EPI_WARP = 4;        // warps 4-7: the epilogue warpgroup
+constexpr int PRODUCER_WARP = 8;   // first producer warp
 constexpr int PRODUCER_WARPS = 6;  // one per ring unit; TMA issue rate scales with issuing warps
-constexpr int PRODUCER_WARP = 4;   // first producer warp
 constexpr int MMA_WARP = PRODUCER_WARP + PRODUCER_WARPS;  // issues the score MMAs, owns TMEM
 constexpr int PV_WARP = MMA_WARP + 1;                     // issues the P.V MMAs
 constexpr int TC_WARPS = PV_WARP + 1;
@@ -92,8 +100,9 @@ constexpr int PBYTES = 16384;     // P^T: 2 buffers x (hi, lo) x 2 columns x 16 
 constexpr int RING_OFF = CTRL + QBYTES + PBYTES;
 constexpr uint32_t TMEM_COLS = 128;
 
+// TMEM columns: S^T of tile parity sb, O^T half `half` of item parity ob.
 __device__ __forceinline__ uint32_t s_col(int sb) { return sb * 16; }
-__device__ __forceinline__ uint32_t o_col(int sb, int half) { return 32 + sb * 32 + half * 16; }
+__device__ __forceinline__ uint32_t o_col(int ob, int half) { return 32 + ob * 32 + half * 16; }
 
 // Byte offset of element (row, col) of a [rows][64] bf16 column stored with
 // the 128-byte swizzle (16-byte chunk index XOR row % 8).
@@ -106,12 +115,18 @@ struct Flags {
     volatile int *abort;
 };
 
+// Bounded wait on an mbarrier phase; false (and the CTA's pipeline aborted)
+// if it ran past its limit or another role aborted.  SPIN: the roles on the
+// per-tile critical path poll; the epilogue, which waits most of the time,
+// sleeps between polls.
+template <bool SPIN>
 __device__ __forceinline__ bool wait_or_abort(uint64_t *bar, uint32_t parity, const Flags &f,
                                               unsigned int *err)
 {
     if (*f.abort)
         return false;
-    if (!mbar_wait(bar, parity, err)) {
+    const bool ok = SPIN ? mbar_wait_spin(bar, parity, err) : mbar_wait(bar, parity, err);
+    if (!ok) {
         *f.abort = 1;
         return false;
     }
@@ -128,19 +143,45 @@ __device__ __forceinline__ void ld_cols(uint32_t taddr, float (&v)[N])
         tmem_ld<N>(taddr, v);
 }
 
-// OR of a predicate over the 128 softmax threads (named barrier 1).
-__device__ __forceinline__ bool softmax_any(bool pred)
+// OR of a predicate over the 128 threads of named barrier `id`.
+template <int ID>
+__device__ __forceinline__ bool group_any(bool pred)
 {
     uint32_t r;
     asm volatile(
         "{\n\t.reg .pred p, q;\n\t"
         "setp.ne.u32 p, %1, 0;\n\t"
-        "bar.red.or.pred q, 1, 128, p;\n\t"
+        "bar.red.or.pred q, %2, 128, p;\n\t"
         "selp.u32 %0, 1, 0, q;\n\t}"
         : "=r"(r)
-        : "r"(pred ? 1u : 0u)
+        : "r"(pred ? 1u : 0u), "n"(ID)
         : "memory");
     return r != 0;
+}
+
+// AND of a predicate over the 128 threads of named barrier `id`.
+template <int ID>
+__device__ __forceinline__ bool group_all(bool pred)
+{
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 p, %1, 0;\n\t"
+        "bar.red.and.pred q, %2, 128, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"(pred ? 1u : 0u), "n"(ID)
+        : "memory");
+    return r != 0;
+}
+
+constexpr int BAR_SOFTMAX = 1;  // named barrier of warps 0-3
+constexpr int BAR_EPI = 2;      // named barrier of warps 4-7
+
+template <int ID>
+__device__ __forceinline__ void group_sync()
+{
+    asm volatile("bar.sync %0, 128;" ::"n"(ID) : "memory");
 }
 
 // Sums over the 32 lanes of N values (N = 2..16) by halving exchanges: a
@@ -178,9 +219,11 @@ __device__ __forceinline__ float warp_sum_scatter(const float (&in)[N], int lane
     return r;
 }
 
-// Virtual tiles charged per item for its fixed cost (about two tiles of
-// streaming: the wait for the last P.V and the write of the result).
-constexpr int KAPPA = 2;
+
+// Virtual tiles charged per item for its fixed cost on the CTA's pipeline
+// (the first tile's loads of the next item start behind the item's last
+// ones; the result is written by the epilogue warps, off that path).
+constexpr int KAPPA = 1;
 
 // One (sequence, kv head, split) item and its key range.
 struct Item {
@@ -379,120 +422,102 @@ __global__ void __launch_bounds__(1024) tc_plan_kernel(const DecodeParams p, int
     }
 }
 
-// ------------------------------------------------------------------ merge
-// An item cut at CTA boundaries is merged by the CTA holding its last part:
-// the CTA whose first item started before its units and ends within them.
-// Its parts are CTA ca's second slot (the item ends ca's range) and the first
-// slots of CTAs ca+1 .. c (the item starts theirs); each is published with a
-// release flag once its bulk stores are complete.  The launch is cooperative
-// (all CTAs resident), so the waits end; they are bounded all the same.
-// Weights exp(lse_k - max), then the normalised sum, written as the output
-// (one split) or as the split's partial state.  scratch: the idle ring.
-template <int D>
-__device__ __noinline__ void merge_cut_item(const DecodeParams &p, int4 first, int c, int W, int C, int t0,
-                               int t1, float *scratch)
+
+// ------------------------------------------------------------------ epilogue
+// Partial-state row of part k of a cut item: the CTA holding its first tile
+// (ca) has it as its last item (slot 1), the CTAs after it as their first
+// item (slot 0).
+__device__ __forceinline__ size_t part_row(int ca, int k)
 {
-    __shared__ int bad;
-    const Item it = item_at(p, first);
-    if (!(it.b < p.batch && it.start < t0 && t0 < it.start + it.T &&
-          (c == C - 1 || it.start + it.T <= t1)))
-        return;  // uniform over the CTA
-    int ca = c - 1;
-    while (ca > 0 && tile_bound(ca, W, C) > it.start)
-        --ca;
-    const int nparts = c - ca + 1;
-    auto part = [&](int k) { return (static_cast<size_t>(ca + k) * 2 + (k == 0 ? 1 : 0)) * NPAD; };
-    if (threadIdx.x == 0) {
-        bad = 0;
-        for (int k = 0; k < nparts - 1; ++k) {
-            const int *f = &p.tc_flags[(ca + k) * 2 + (k == 0 ? 1 : 0)];
-            if (ld_acquire_gpu(f))
-                continue;
-            const uint64_t t_start = global_timer_ns();
-            while (!ld_acquire_gpu(f)) {
-                if (global_timer_ns() - t_start > 2000000000ull) {
-                    record_error(p.err, PKV_DEV_TIMEOUT);
-                    bad = 1;
-                    break;
-                }
-            }
-            if (bad)
-                break;
-        }
-    }
-    __syncthreads();
-    if (bad)
-        return;
+    return (static_cast<size_t>(ca + k) * 2 + (k == 0 ? 1 : 0)) * NPAD;
+}
+
+// Merge of a cut item's parts by the epilogue warpgroup of the CTA whose
+// part finished last: per head the weights exp(lse_k - max) / sum over the
+// parts, then the weighted sum of the normalised partial outputs, written
+// as the output row (one split) or as the split's partial state.  Thread t
+// owns head t / 8 and every eighth 16-byte column of it; the parts'
+// log-sum-exps are reduced by the 8 threads of a head.
+template <int D>
+__device__ __forceinline__ void merge_parts(const DecodeParams &p, const Item &it, int ca,
+                                         int nparts, int t)
+{
+    constexpr int NV = D / 32;  // 16-byte columns per thread
     const int G = p.group;
-    float *w_s = scratch;                  // [16][kTcMaxGrid]
-    float *inv_s = w_s + NPAD * kTcMaxGrid;  // [16]
-    float *lse_s = inv_s + NPAD;             // [16]
-    for (int idx = threadIdx.x; idx < nparts * NPAD; idx += blockDim.x) {
-        const int k = idx / NPAD, h = idx - k * NPAD;
-        w_s[h * kTcMaxGrid + k] = h < G ? p.sub_lse[part(k) + h] : -INFINITY;
-    }
-    __syncthreads();
-    if (threadIdx.x < G) {
-        const int h = threadIdx.x;
-        float *w = w_s + h * kTcMaxGrid;
-        float M = -INFINITY;
-        for (int k = 0; k < nparts; ++k)
-            M = fmaxf(M, w[k]);
-        float Z = 0.f;
-        for (int k = 0; k < nparts; ++k) {
-            const float e = (M == -INFINITY || w[k] == -INFINITY) ? 0.f : expf(w[k] - M);
-            w[k] = e;
-            Z += e;
-        }
-        inv_s[h] = Z > 0.f ? 1.f / Z : 0.f;
-        lse_s[h] = Z > 0.f ? M + logf(Z) : -INFINITY;
-    }
-    __syncthreads();
-    const bool single = it.nsplit == 1;
-    // four outputs (one float4) per step, four parts' loads in flight
-    for (int q = threadIdx.x; q < G * D / 4; q += blockDim.x) {
-        const int h = (q * 4) / D, d = q * 4 - h * D;
-        const float *w = w_s + h * kTcMaxGrid;
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int k0 = 0; k0 < nparts; k0 += 4) {
-            float4 v[4];
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk)
-                v[kk] = k0 + kk < nparts
-                            ? *reinterpret_cast<const float4 *>(&p.sub_o[(part(k0 + kk) + h) * D + d])
-                            : make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk) {
-                const float wk = k0 + kk < nparts ? w[k0 + kk] : 0.f;
-                if (wk != 0.f) {
-                    acc.x = fmaf(wk, v[kk].x, acc.x);
-                    acc.y = fmaf(wk, v[kk].y, acc.y);
-                    acc.z = fmaf(wk, v[kk].z, acc.z);
-                    acc.w = fmaf(wk, v[kk].w, acc.w);
-                }
+    const int hh = t >> 3, grp = t & 7;
+    float M = -INFINITY, Z = 0.f;
+    if (hh < G) {
+        for (int k = grp; k < nparts; k += 8) {
+            const float l = __ldcg(&p.sub_lse[part_row(ca, k) + hh]);
+            if (l == -INFINITY)
+                continue;
+            if (l > M) {
+                Z = Z * expf(M - l) + 1.f;
+                M = l;
+            } else {
+                Z += expf(l - M);
             }
         }
-        const float inv = inv_s[h];
-        const float4 y = make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
-        if (single) {
-            const size_t o = (static_cast<size_t>(it.b) * p.num_q_heads + it.g * G + h) * D + d;
+    }
+#pragma unroll
+    for (int off = 1; off < 8; off <<= 1) {
+        const float M2 = __shfl_xor_sync(FULL_MASK, M, off);
+        const float Z2 = __shfl_xor_sync(FULL_MASK, Z, off);
+        const float Mn = fmaxf(M, M2);
+        Z = Mn == -INFINITY ? 0.f
+                            : (M == -INFINITY ? 0.f : Z * expf(M - Mn)) +
+                                  (M2 == -INFINITY ? 0.f : Z2 * expf(M2 - Mn));
+        M = Mn;
+    }
+    if (hh >= G)
+        return;
+    const float invZ = Z > 0.f ? 1.f / Z : 0.f;
+    float4 acc[NV];
+#pragma unroll
+    for (int i = 0; i < NV; ++i)
+        acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    // one part per step: NV independent 16-byte loads in flight per thread
+    for (int k = 0; k < nparts; ++k) {
+        const size_t r = part_row(ca, k) + hh;
+        const float l = __ldcg(&p.sub_lse[r]);
+        const float4 *src = reinterpret_cast<const float4 *>(p.sub_o + r * D);
+        float4 v[NV];
+#pragma unroll
+        for (int i = 0; i < NV; ++i)
+            v[i] = __ldcg(src + grp + 8 * i);
+        const float w = (l == -INFINITY || M == -INFINITY) ? 0.f : expf(l - M) * invZ;
+#pragma unroll
+        for (int i = 0; i < NV; ++i) {
+            acc[i].x = fmaf(w, v[i].x, acc[i].x);
+            acc[i].y = fmaf(w, v[i].y, acc[i].y);
+            acc[i].z = fmaf(w, v[i].z, acc[i].z);
+            acc[i].w = fmaf(w, v[i].w, acc[i].w);
+        }
+    }
+    if (it.nsplit == 1) {
+        const size_t o = (static_cast<size_t>(it.b) * p.num_q_heads + it.g * G + hh) * D;
+#pragma unroll
+        for (int i = 0; i < NV; ++i) {
+            const int d = (grp + 8 * i) * 4;
             if (p.out_f32) {
-                *reinterpret_cast<float4 *>(reinterpret_cast<float *>(p.out) + o) = y;
+                *reinterpret_cast<float4 *>(reinterpret_cast<float *>(p.out) + o + d) = acc[i];
             } else {
-                __nv_bfloat162 lo2 = __floats2bfloat162_rn(y.x, y.y);
-                __nv_bfloat162 hi2 = __floats2bfloat162_rn(y.z, y.w);
+                __nv_bfloat162 lo2 = __floats2bfloat162_rn(acc[i].x, acc[i].y);
+                __nv_bfloat162 hi2 = __floats2bfloat162_rn(acc[i].z, acc[i].w);
                 uint2 u;
                 u.x = *reinterpret_cast<uint32_t *>(&lo2);
                 u.y = *reinterpret_cast<uint32_t *>(&hi2);
-                *reinterpret_cast<uint2 *>(reinterpret_cast<__nv_bfloat16 *>(p.out) + o) = u;
+                *reinterpret_cast<uint2 *>(reinterpret_cast<__nv_bfloat16 *>(p.out) + o + d) = u;
             }
-        } else {
-            const size_t prow =
-                (static_cast<size_t>(it.b) * p.num_splits + it.s) * p.num_q_heads + it.g * G + h;
-            *reinterpret_cast<float4 *>(&p.part_o[prow * D + d]) = y;
-            if (d == 0)
-                p.part_lse[prow] = lse_s[h];
         }
+    } else {
+        const size_t prow =
+            (static_cast<size_t>(it.b) * p.num_splits + it.s) * p.num_q_heads + it.g * G + hh;
+#pragma unroll
+        for (int i = 0; i < NV; ++i)
+            *reinterpret_cast<float4 *>(&p.part_o[prow * D + (grp + 8 * i) * 4]) = acc[i];
+        if (grp == 0)
+            p.part_lse[prow] = Z > 0.f ? M + logf(Z) : -INFINITY;
     }
 }
 
@@ -513,22 +538,26 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     uint8_t *sm = smem_raw + (((raw + 1023u) & ~1023u) - raw);
     uint64_t *unit_full = reinterpret_cast<uint64_t *>(sm);  // [8]
     uint64_t *unit_empty = unit_full + 8;                    // [8]
-    uint64_t *s_full = unit_full + 16;                       // [2]
-    uint64_t *s_empty = s_full + 2;                          // [2]
-    uint64_t *p_full = s_full + 4;                           // [2]
-    uint64_t *o_full = s_full + 6;                           // [2]
-    uint64_t *o_empty = s_full + 8;                          // [2]
-    uint64_t *q_full = s_full + 10;                          // [2]
-    uint64_t *q_empty = s_full + 12;                         // [2]
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + 256);
-    Flags flags{reinterpret_cast<volatile int *>(sm + 260)};
-    float *red = reinterpret_cast<float *>(sm + 512);        // [4][16]
+    uint64_t *s_full = unit_full + 16;                       // [2] S^T of a tile in TMEM
+    uint64_t *s_empty = s_full + 2;                          // [2] S^T read by the softmax
+    uint64_t *p_full = s_full + 4;                           // [2] P^T of a tile written
+    uint64_t *pv_done = s_full + 6;                          // [2] a tile's P.V complete
+    uint64_t *o_full = s_full + 8;                           // [2] an item's O^T complete
+    uint64_t *o_free = s_full + 10;                          // [2] an item's O^T read
+    uint64_t *q_full = s_full + 12;                          // [2]
+    uint64_t *q_empty = s_full + 14;                         // [2]
+    uint64_t *epi_full = s_full + 16;                        // [2] an item's max and sums
+    uint64_t *epi_empty = s_full + 18;                       // [2] ... read by the epilogue
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + 288);
+    Flags flags{reinterpret_cast<volatile int *>(sm + 292)};
+    volatile int *ticket_s = reinterpret_cast<volatile int *>(sm + 296);
+    float *red = reinterpret_cast<float *>(sm + 320);        // [4][16] softmax exchange
     // running max per head and the last rescale factors: the same in every
     // softmax thread, so kept once in shared memory instead of in registers
-    float *mrun_s = reinterpret_cast<float *>(sm + 768);     // [16]
-    float *alpha_s = reinterpret_cast<float *>(sm + 832);    // [16]
-    float *lse_s = reinterpret_cast<float *>(sm + 896);      // [16] an item's log-sum-exps
-    float *inv_s = reinterpret_cast<float *>(sm + 960);      // [16] an item's 1 / L
+    float *mrun_s = reinterpret_cast<float *>(sm + 576);     // [16]
+    float *alpha_s = reinterpret_cast<float *>(sm + 640);    // [16]
+    float *epi_m = reinterpret_cast<float *>(sm + 704);      // [2][16] an item's max (log2)
+    float *epi_l = reinterpret_cast<float *>(sm + 832);      // [2][16] an item's sums
     uint8_t *qs = sm + CTRL;
     uint8_t *ps = sm + CTRL + QBYTES;
     uint8_t *units = sm + RING_OFF;
@@ -546,25 +575,26 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&s_full[i], 1);
-            mbar_init(&s_empty[i], 4);
-            mbar_init(&p_full[i], 4);
+            mbar_init(&s_empty[i], SOFTMAX_WARPS);
+            mbar_init(&p_full[i], SOFTMAX_WARPS);
+            mbar_init(&pv_done[i], 1);
             mbar_init(&o_full[i], 1);
-            mbar_init(&o_empty[i], 4);
+            mbar_init(&o_free[i], 4);
             mbar_init(&q_full[i], 1);
             mbar_init(&q_empty[i], 1);
+            mbar_init(&epi_full[i], 1);
+            mbar_init(&epi_empty[i], 4);
         }
         *flags.abort = 0;
         fence_barrier_init();
     }
     if (warp == MMA_WARP)
         tmem_alloc(tmem_slot, TMEM_COLS);
-    if (warp < 4) {
+    if (warp < SOFTMAX_WARPS) {
         // P^T buffers start at zero: padded heads stay zero for the whole kernel
         for (int idx = threadIdx.x; idx < PBYTES / 16; idx += 128)
             reinterpret_cast<uint4 *>(ps)[idx] = make_uint4(0u, 0u, 0u, 0u);
         fence_proxy_async_smem();
-        if (threadIdx.x < NPAD)
-            mrun_s[threadIdx.x] = -INFINITY;  // the first item's running max
     }
     __syncthreads();
     tc_fence_after();
@@ -581,7 +611,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     const int t0 = active ? tile_bound(c, W, C) : 0, t1 = active ? tile_bound(c + 1, W, C) : 0;
     const int4 first = active ? p.tc_plan[1 + c] : make_int4(p.batch, 0, 0, 0);
 
-    constexpr int GL = GP < 16 ? GP : 16;  // TMEM columns read per result
+    constexpr int GL = GP < 16 ? GP : 16;  // TMEM columns per S or O half
     // Unit j (a 128-dim half of a 128-key tile, counted over the CTA's whole
     // walk) of the K stream lives in slot j % NKU, use j / NKU; of the V
     // stream in slot VBASE + j % NVU, use j / NVU.
@@ -612,8 +642,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                 if (slot == 0) {
                     // Q^T of this item: 16 rows (heads g*G ...) x D dims
                     const int qb = kq & 1;
-                    const bool room = kq < 2 ||
-                                      wait_or_abort(&q_empty[qb], ((kq >> 1) - 1) & 1, flags, p.err);
+                    const bool room =
+                        kq < 2 || wait_or_abort<true>(&q_empty[qb], ((kq >> 1) - 1) & 1, flags, p.err);
                     if (!__all_sync(FULL_MASK, room))
                         break;
                     if (lane == 0) {
@@ -648,8 +678,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                         if (rbase + jj % ring != slot)
                             continue;
                         const int use = jj / ring;
-                        const bool room = use == 0 ||
-                                          wait_or_abort(&unit_empty[slot], (use - 1) & 1, flags, p.err);
+                        const bool room = use == 0 || wait_or_abort<true>(&unit_empty[slot], (use - 1) & 1,
+                                                                          flags, p.err);
                         if (!__all_sync(FULL_MASK, room)) {
                             stop = true;
                             break;
@@ -695,20 +725,21 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                 if (lt1 <= lt0)
                     continue;
                 const int qb = kq & 1;
-                ok = wait_or_abort(&q_full[qb], (kq >> 1) & 1, flags, p.err);
+                ok = wait_or_abort<true>(&q_full[qb], (kq >> 1) & 1, flags, p.err);
                 if (!ok)
                     break;
                 tc_fence_after();
                 const uint32_t q_base = smem_u32(qs + qb * QBUF);
                 for (int i = lt0; i < lt1 && ok; ++i, ++i_g) {
                     const int sb = i_g & 1;
-                    if (i_g >= 2 && !wait_or_abort(&s_empty[sb], ((i_g >> 1) - 1) & 1, flags, p.err)) {
+                    if (i_g >= 2 &&
+                        !wait_or_abort<true>(&s_empty[sb], ((i_g >> 1) - 1) & 1, flags, p.err)) {
                         ok = false;
                         break;
                     }
                     for (int h = 0; h < HALVES; ++h, ++j) {
                         const int slot = j % NKU;
-                        ok = wait_or_abort(&unit_full[slot], (j / NKU) & 1, flags, p.err);
+                        ok = wait_or_abort<true>(&unit_full[slot], (j / NKU) & 1, flags, p.err);
                         if (!ok)
                             break;
                         tc_fence_after();
@@ -735,25 +766,34 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         __syncwarp();
     } else if (warp == PV_WARP) {
         // ------------------------------------------------------ P.V MMAs
-        // tile i needs P^T, a free O buffer and its V units; the whole warp
-        // first zeroes V rows of masked keys inside loaded blocks (only the
-        // block holding the window start and the block holding pos can have
-        // them), lane 0 then issues the MMAs.
+        // tile i needs P^T and its V units; an item's first tile also needs
+        // its O buffer (free once the epilogue has read the item two back).
+        // The whole warp first zeroes V rows of masked keys inside loaded
+        // blocks (only the block holding the window start and the block
+        // holding pos can have them), lane 0 then issues the MMAs, which
+        // accumulate into the item's O^T from its second tile on.
         constexpr uint32_t IDESC_PV = umma_idesc_bf16(128, NPAD, true, false);
         const uint32_t p_base = smem_u32(ps), u_base = smem_u32(units);
-        int i_g = 0, j = 0;
+        int i_g = 0, j = 0, k = 0;
         bool ok = true;
         Item it = item_at(p, first);
         for (; ok && it.b < p.batch && it.start < t1; item_next(p, it)) {
             const int lt0 = max(0, t0 - it.start), lt1 = min(it.T, t1 - it.start);
             if (lt1 <= lt0)
                 continue;
+            const int ob = k & 1;
+            {
+                const bool go =
+                    k < 2 || wait_or_abort<true>(&o_free[ob], ((k >> 1) - 1) & 1, flags, p.err);
+                if (!__all_sync(FULL_MASK, go)) {
+                    ok = false;
+                    break;
+                }
+            }
             const int lo_blk = it.lo / kBlock, pos_blk = it.pos / kBlock;
             for (int i = lt0; i < lt1 && ok; ++i, ++i_g) {
                 const int sb = i_g & 1;
-                bool go = wait_or_abort(&p_full[sb], (i_g >> 1) & 1, flags, p.err);
-                go = go &&
-                     (i_g < 2 || wait_or_abort(&o_empty[sb], ((i_g >> 1) - 1) & 1, flags, p.err));
+                const bool go = wait_or_abort<true>(&p_full[sb], (i_g >> 1) & 1, flags, p.err);
                 if (!__all_sync(FULL_MASK, go)) {
                     ok = false;
                     break;
@@ -779,7 +819,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                     // one burst of 16 P.V MMAs delays the next tile's score
                     // MMAs queued behind it in the tensor pipe.
                     if (!alias) {
-                        ok = wait_or_abort(&unit_full[slot], (j / NVU) & 1, flags, p.err);
+                        ok = wait_or_abort<true>(&unit_full[slot], (j / NVU) & 1, flags, p.err);
                         if (!__all_sync(FULL_MASK, ok)) {
                             ok = false;
                             break;
@@ -808,7 +848,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                                 const uint64_t bd = umma_smem_desc(
                                     p_base + sb * 8192 + pass * 4096 + (kk >> 2) * 2048 + (kk & 3) * 32,
                                     16, 1024);
-                                umma_bf16(tmem + o_col(sb, h), a, bd, IDESC_PV, (pass | kk) != 0);
+                                umma_bf16(tmem + o_col(ob, h), a, bd, IDESC_PV,
+                                          i > lt0 || pass > 0 || kk > 0);
                             }
                         }
                         umma_commit(&unit_empty[slot]);  // V (or K = V) unit free once read
@@ -817,52 +858,34 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                 }
                 if (!ok)
                     break;
-                if (lane == 0)
-                    umma_commit(&o_full[sb]);
+                if (lane == 0) {
+                    umma_commit(&pv_done[sb]);  // P^T buffer sb free; O through this tile
+                    if (i == lt1 - 1)
+                        umma_commit(&o_full[ob]);  // the item's O^T is final
+                }
                 __syncwarp();
             }
+            ++k;
         }
-    } else {
+    } else if (warp < SOFTMAX_WARPS) {
         // ------------------------------------------------------ softmax
         const int t = threadIdx.x;  // key row of the tile == TMEM lane
         const uint32_t lane_base = tmem + (static_cast<uint32_t>(warp * 32) << 16);
         const float qk = p.qk_scale_log2;
-        float lpart[GP], m_run[GP];
-        float oacc[HALVES][GP];  // running O^T relative to the running max
-        auto accumulate_o = [&](int k) {
-            const int sb = k & 1;
-            const bool live = wait_or_abort(&o_full[sb], (k >> 1) & 1, flags, p.err);
-            tc_fence_after();
-#pragma unroll
-            for (int hv = 0; hv < HALVES; ++hv) {
-                float ot[GL];
-                if (live)
-                    ld_cols<GL>(lane_base + o_col(sb, hv), ot);
-#pragma unroll
-                for (int h = 0; h < GP; ++h)
-                    oacc[hv][h] += live ? ot[h] : 0.f;
-            }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0)
-                mbar_arrive(&o_empty[sb]);
-        };
-        int i_g = 0;
+        float lpart[GP];
+        int i_g = 0, k = 0;
         Item it = item_at(p, first);
         for (; it.b < p.batch && it.start < t1; item_next(p, it)) {
             const int lt0 = max(0, t0 - it.start), lt1 = min(it.T, t1 - it.start);
-            const bool whole = lt0 == 0 && lt1 == it.T;
+            if (lt1 <= lt0)
+                continue;
+            const int ob = k & 1;
 #pragma unroll
-            for (int h = 0; h < GP; ++h) {
+            for (int h = 0; h < GP; ++h)
                 lpart[h] = 0.f;
-                m_run[h] = -INFINITY;
-#pragma unroll
-                for (int hv = 0; hv < HALVES; ++hv)
-                    oacc[hv][h] = 0.f;
-            }
-            // mrun_s was reset by the previous item's epilogue (or the set-up)
             for (int i = lt0; i < lt1; ++i, ++i_g) {
                 const int sb = i_g & 1;
+                const bool first_tile = i == lt0;
                 // key t of the tile: inside the item's blocks and in [lo, pos].
                 // A block id outside the pool is not read here: the producer
                 // reports it and its box arrives as zeros (keys of score 0,
@@ -872,7 +895,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                 const int jk = (it.ub0 + i * 8) * kBlock + t;
                 const bool ok = loaded && jk >= it.lo && jk <= it.pos;
                 // ---- scores
-                const bool live = wait_or_abort(&s_full[sb], (i_g >> 1) & 1, flags, p.err);
+                bool live = wait_or_abort<true>(&s_full[sb], (i_g >> 1) & 1, flags, p.err);
                 tc_fence_after();
                 float s[GL];
                 if (live)
@@ -882,51 +905,69 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                 if (lane == 0)
                     mbar_arrive(&s_empty[sb]);
                 float sc[GP];
-                bool big = false;
+                // the item's first tile always sets the running max
+                bool big = first_tile;
 #pragma unroll
                 for (int h = 0; h < GP; ++h) {
                     sc[h] = (live && ok && h < G) ? s[h] * qk : -INFINITY;
-                    big |= sc[h] > m_run[h] + 8.f;
+                    big |= sc[h] > mrun_s[h] + 8.f;
                 }
-                // ---- running max: reduce only when some score exceeds it by more
-                // than 2^8 (any reference max >= the true one gives the same
-                // result; this one keeps every p <= 256).  softmax_any is also
-                // the barrier after which mrun_s / alpha_s may be rewritten.
-                const bool rescale = softmax_any(big);
+                // ---- running max: changed only when some score exceeds it by
+                // more than 2^8.  group_any is also the barrier after which
+                // red / mrun_s / alpha_s may be rewritten.
+                const bool rescale = group_any<BAR_SOFTMAX>(big);
                 if (rescale) {
-                    float mx[GP];
 #pragma unroll
                     for (int h = 0; h < GP; ++h) {
                         float v = sc[h];
 #pragma unroll
                         for (int off = 16; off > 0; off >>= 1)
                             v = fmaxf(v, __shfl_xor_sync(FULL_MASK, v, off));
-                        mx[h] = v;
+                        if (lane == 0)
+                            red[warp * 16 + h] = v;
                     }
-                    if (lane == 0) {
-#pragma unroll
-                        for (int h = 0; h < GP; ++h)
-                            red[warp * 16 + h] = mx[h];
-                    }
-                    asm volatile("bar.sync 1, 128;" ::: "memory");
+                    group_sync<BAR_SOFTMAX>();
                     if (t < GP) {
                         const float tm =
                             fmaxf(fmaxf(red[t], red[16 + t]), fmaxf(red[32 + t], red[48 + t]));
-                        const float mo = mrun_s[t];
+                        const float mo = first_tile ? -INFINITY : mrun_s[t];
                         const float mn = fmaxf(mo, tm);
                         alpha_s[t] = mn == -INFINITY ? 1.f : fast_exp2(mo - mn);
                         mrun_s[t] = mn;
                     }
-                    asm volatile("bar.sync 1, 128;" ::: "memory");  // red is reused
+                    group_sync<BAR_SOFTMAX>();  // red is reused
+                }
+                // ---- P^T buffer sb was last read by the P.V of tile i_g - 2
+                if (i_g >= 2)
+                    live &= wait_or_abort<true>(&pv_done[sb], ((i_g >> 1) - 1) & 1, flags, p.err);
+                if (rescale && !first_tile) {
+                    // O^T through the previous tile is relative to the old max:
+                    // scale it once that tile's P.V is done, before this P is
+                    // published (the P.V warp waits for it)
+                    live &= wait_or_abort<true>(&pv_done[sb ^ 1], ((i_g - 1) >> 1) & 1, flags, p.err);
+                    tc_fence_after();
+                    if (live) {
 #pragma unroll
-                    for (int h = 0; h < GP; ++h)
-                        m_run[h] = mrun_s[h];
+                        for (int hv = 0; hv < HALVES; ++hv) {
+                            constexpr int NC = GL < 8 ? GL : 8;  // columns per TMEM access
+#pragma unroll
+                            for (int c0 = 0; c0 < GL; c0 += NC) {
+                                float o[NC];
+                                ld_cols<NC>(lane_base + o_col(ob, hv) + c0, o);
+#pragma unroll
+                                for (int h = 0; h < NC; ++h)
+                                    o[h] *= alpha_s[c0 + h];
+                                tmem_st<NC>(lane_base + o_col(ob, hv) + c0, o);
+                            }
+                        }
+                    }
+                    tc_fence_before();
                 }
                 // ---- probabilities, running sums, P^T (bf16, K-major, swizzled)
                 uint8_t *pb = ps + sb * 8192 + (t >> 6) * 2048;
 #pragma unroll
                 for (int h = 0; h < GP; ++h) {
-                    const float pr = sc[h] == -INFINITY ? 0.f : fast_exp2(sc[h] - m_run[h]);
+                    const float pr = sc[h] == -INFINITY ? 0.f : fast_exp2(sc[h] - mrun_s[h]);
                     lpart[h] = rescale ? fmaf(lpart[h], alpha_s[h], pr) : lpart[h] + pr;
                     const __nv_bfloat16 hi = __float2bfloat16_rn(pr);
                     *reinterpret_cast<__nv_bfloat16 *>(pb + swz(h, t & 63)) = hi;
@@ -938,122 +979,145 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                 __syncwarp();
                 if (lane == 0)
                     mbar_arrive(&p_full[sb]);
-                // ---- O^T of the previous tile, then rescale to this tile's max
-                if (i > lt0)
-                    accumulate_o(i_g - 1);
-                if (rescale) {
-#pragma unroll
-                    for (int h = 0; h < GP; ++h)
-#pragma unroll
-                        for (int hv = 0; hv < HALVES; ++hv)
-                            oacc[hv][h] *= alpha_s[h];
-                }
             }
-            // ---- sums over the 128 keys of each head, 1/L and the
-            // log-sum-exp: lpart and the running max are final once the last
-            // tile's P is formed, so this overlaps that tile's P.V
+            // ---- the item's sums over its keys and its max go to the
+            // epilogue (slot ob, free once the epilogue has read item k - 2)
             {
                 int hh;
                 const float v = warp_sum_scatter<GP>(lpart, lane, hh);
                 if ((lane & (32 / GP - 1)) == 0)
                     red[warp * 16 + hh] = v;
             }
-            asm volatile("bar.sync 1, 128;" ::: "memory");
-            if (t < GP) {
-                const float L = (red[t] + red[16 + t]) + (red[32 + t] + red[48 + t]);
-                inv_s[t] = L > 0.f ? 1.f / L : 0.f;
-                lse_s[t] = L > 0.f ? (mrun_s[t] + log2f(L)) * LN2 : -INFINITY;
-                mrun_s[t] = -INFINITY;  // the next item's running max
-            }
-            asm volatile("bar.sync 1, 128;" ::: "memory");
-            if (lt1 > lt0)
-                accumulate_o(i_g - 1);
-            // whole item: the output when the sequence has one split, else the
-            // split's partial; a piece of an item: this CTA's partial state.
-            // The G x D results are staged in the P^T buffers (idle between an
-            // item's last P.V and the next item's first P) and leave in TMA
-            // bulk stores: plain stores of 128 lines per item queue behind the
-            // ring's HBM traffic for several microseconds.
-            const bool single = whole && it.nsplit == 1;
-            const bool f32 = !single || p.out_f32;
-            const int slot = lt0 > 0 ? 0 : 1;  // cut at its start: this CTA's first item
-            // every thread reads the normalisers in vector loads before its
-            // stores (reading them per head between stores costs one
-            // shared-memory round trip per head, which under the ring's
-            // traffic is several microseconds per item)
-            float inv[GP];
-            if constexpr (GP >= 4) {
-#pragma unroll
-                for (int h4 = 0; h4 < GP / 4; ++h4) {
-                    const float4 v = reinterpret_cast<const float4 *>(inv_s)[h4];
-                    inv[4 * h4] = v.x;
-                    inv[4 * h4 + 1] = v.y;
-                    inv[4 * h4 + 2] = v.z;
-                    inv[4 * h4 + 3] = v.w;
+            group_sync<BAR_SOFTMAX>();
+            if (warp == 0) {
+                if (t < GP) {
+                    if (k >= 2)
+                        wait_or_abort<true>(&epi_empty[ob], ((k >> 1) - 1) & 1, flags, p.err);
+                    epi_l[ob * 16 + t] = (red[t] + red[16 + t]) + (red[32 + t] + red[48 + t]);
+                    epi_m[ob * 16 + t] = mrun_s[t];
                 }
-            } else {
-                const float2 v = *reinterpret_cast<const float2 *>(inv_s);
-                inv[0] = v.x;
-                inv[1] = v.y;
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(&epi_full[ob]);
             }
+            ++k;
+        }
+    } else {
+        // ------------------------------------------------------ epilogue
+        const int t = threadIdx.x - EPI_WARP * 32;  // output dims t, 128 + t == TMEM lane t
+        const uint32_t lane_base = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
+        int k = 0;
+        Item it = item_at(p, first);
+        for (; it.b < p.batch && it.start < t1; item_next(p, it)) {
+            const int lt0 = max(0, t0 - it.start), lt1 = min(it.T, t1 - it.start);
+            if (it.T == 0) {
+                // no keys (length 0): a zero output row, written by the CTA
+                // whose units hold the item's start
+                if (it.start >= t0) {
+                    const size_t row0 = static_cast<size_t>(it.b) * p.num_q_heads + it.g * G;
+                    for (int idx = t; idx < G * D; idx += 128) {
+                        if (p.out_f32)
+                            reinterpret_cast<float *>(p.out)[row0 * D + idx] = 0.f;
+                        else
+                            reinterpret_cast<__nv_bfloat16 *>(p.out)[row0 * D + idx] =
+                                __float2bfloat16_rn(0.f);
+                    }
+                }
+                continue;
+            }
+            if (lt1 <= lt0)
+                continue;
+            const int ob = k & 1;
+            bool live = wait_or_abort<false>(&epi_full[ob], (k >> 1) & 1, flags, p.err);
+            live = live && wait_or_abort<false>(&o_full[ob], (k >> 1) & 1, flags, p.err);
+            tc_fence_after();
+            float o[HALVES][GL];
+            if (live) {
+#pragma unroll
+                for (int hv = 0; hv < HALVES; ++hv)
+                    ld_cols<GL>(lane_base + o_col(ob, hv), o[hv]);
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(&o_free[ob]);  // O^T is in registers now
+            ++k;
+            if (!group_all<BAR_EPI>(live))
+                break;  // uniform over the warpgroup
+            // 1 / L of head h and its log-sum-exp (natural log), from the
+            // slot the softmax filled; the slot is released after the stores
+            const float *Ls = epi_l + ob * 16, *Ms = epi_m + ob * 16;
+            auto inv_of = [&](int h) {
+                const float L = Ls[h];
+                return L > 0.f ? 1.f / L : 0.f;
+            };
+            auto release_slot = [&]() {
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(&epi_empty[ob]);
+            };
+            const bool whole = lt0 == 0 && lt1 == it.T;
+            const bool single = whole && it.nsplit == 1;
+            if (single) {
+                const size_t row0 = static_cast<size_t>(it.b) * p.num_q_heads + it.g * G;
+#pragma unroll
+                for (int h = 0; h < GP; ++h) {
+                    if (h >= G)
+                        continue;
+                    const float inv = inv_of(h);
+#pragma unroll
+                    for (int hv = 0; hv < HALVES; ++hv) {
+                        const size_t e = (row0 + h) * D + hv * 128 + t;
+                        const float y = o[hv][h] * inv;
+                        if (p.out_f32)
+                            reinterpret_cast<float *>(p.out)[e] = y;
+                        else
+                            reinterpret_cast<__nv_bfloat16 *>(p.out)[e] = __float2bfloat16_rn(y);
+                    }
+                }
+                release_slot();
+                continue;
+            }
+            // a split's partial state (whole split) or this CTA's part of a cut item
+            const int slot = lt0 > 0 ? 0 : 1;
+            const size_t prow = whole ? (static_cast<size_t>(it.b) * p.num_splits + it.s) *
+                                                p.num_q_heads + it.g * G
+                                      : (static_cast<size_t>(c) * 2 + slot) * NPAD;
+            float *dst_o = whole ? p.part_o : p.sub_o;
+            float *dst_l = whole ? p.part_lse : p.sub_lse;
 #pragma unroll
             for (int h = 0; h < GP; ++h) {
                 if (h >= G)
                     continue;
+                const float inv = inv_of(h);
 #pragma unroll
-                for (int hv = 0; hv < HALVES; ++hv) {
-                    const int d = hv * 128 + t;
-                    const float y = oacc[hv][h] * inv[h];
-                    if (f32)
-                        reinterpret_cast<float *>(ps)[h * D + d] = y;
-                    else
-                        reinterpret_cast<__nv_bfloat16 *>(ps)[h * D + d] = __float2bfloat16_rn(y);
-                }
+                for (int hv = 0; hv < HALVES; ++hv)
+                    dst_o[(prow + h) * D + hv * 128 + t] = o[hv][h] * inv;
             }
-            fence_proxy_async_smem();
-            asm volatile("bar.sync 1, 128;" ::: "memory");
-            // a whole split's partial with a group that is not a multiple of
-            // four heads: its log-sum-exps are not a 16-byte run
-            const bool lse_scalar = whole && !single && (G & 3) != 0;
-            if (lse_scalar && t < G) {
-                const size_t prow = (static_cast<size_t>(it.b) * p.num_splits + it.s) * p.num_q_heads;
-                p.part_lse[prow + it.g * G + t] = lse_s[t];
+            if (t < G) {
+                const float L = Ls[t];
+                dst_l[prow + t] = L > 0.f ? (Ms[t] + log2f(L)) * LN2 : -INFINITY;
             }
-            if (t == 0) {
-                if (single) {
-                    const size_t row0 = static_cast<size_t>(it.b) * p.num_q_heads + it.g * G;
-                    const uint32_t es = p.out_f32 ? 4u : 2u;
-                    bulk_store(static_cast<uint8_t *>(p.out) + row0 * D * es, ps, G * D * es);
-                } else if (!whole) {
-                    const size_t srow = (static_cast<size_t>(c) * 2 + slot) * NPAD;
-                    bulk_store(p.sub_o + srow * D, ps, G * D * 4u);
-                    bulk_store(p.sub_lse + srow, lse_s, NPAD * 4u);
-                } else {
-                    // split-major partials: the group's G rows of split s are one run
-                    const size_t prow =
-                        (static_cast<size_t>(it.b) * p.num_splits + it.s) * p.num_q_heads + it.g * G;
-                    bulk_store(p.part_o + prow * D, ps, G * D * 4u);
-                    if (!lse_scalar)
-                        bulk_store(p.part_lse + prow, lse_s, G * 4u);
-                }
-                bulk_commit();
-                bulk_wait_read();
-            }
-            asm volatile("bar.sync 1, 128;" ::: "memory");  // staging read; red reusable
-            if constexpr (GP < 16) {
-                // P^T rows past the padded group must read as zero again
-                for (int idx = t; idx < PBYTES / 16; idx += 128)
-                    reinterpret_cast<uint4 *>(ps)[idx] = make_uint4(0u, 0u, 0u, 0u);
-            }
-        }
-        if (t == 0) {
-            // publish this CTA's partial states: every bulk store (this thread
-            // issued them all) complete, then the flags
-            bulk_wait_all();
-            fence_proxy_async_global();
-            if (active) {
-                st_release_gpu(&p.tc_flags[c * 2 + 0], 1);
-                st_release_gpu(&p.tc_flags[c * 2 + 1], 1);
+            release_slot();
+            if (whole)
+                continue;
+            // cut item: publish this part, take a ticket; the last part merges
+            int ca = c, cz = c;
+            while (ca > 0 && tile_bound(ca, W, C) > it.start)
+                --ca;
+            const int u_last = it.start + it.T - 1;
+            while (cz + 1 < C && tile_bound(cz + 1, W, C) <= u_last)
+                ++cz;
+            const int nparts = cz - ca + 1;
+            __threadfence();
+            group_sync<BAR_EPI>();
+            if (t == 0)
+                *ticket_s = atomicAdd(&p.tc_flags[ca], 1) == nparts - 1;
+            group_sync<BAR_EPI>();
+            const bool last = *ticket_s != 0;
+            if (last) {
+                __threadfence();
+                merge_parts<D>(p, it, ca, nparts, t);
             }
         }
     }
@@ -1063,8 +1127,6 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         tc_fence_after();
         tmem_dealloc(tmem, TMEM_COLS);
     }
-    if (active)
-        merge_cut_item<D>(p, first, c, W, C, t0, t1, reinterpret_cast<float *>(units));
 }
 
 // ------------------------------------------------------------ host side
@@ -1129,19 +1191,18 @@ static cudaError_t launch_tc_one(const DecodeParams &p, const CUtensorMap &tmk,
             return e;
         configured.store(static_cast<int>(smem), std::memory_order_relaxed);
     }
-    // cooperative: every CTA resident, so the merge's waits on other CTAs end
+    // no CTA waits for another (cut items merge by ticket), so the launch
+    // needs no co-residency guarantee
     cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute attr[2];
+    cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
-    attr[1].id = cudaLaunchAttributeCooperative;
-    attr[1].val.cooperative = 1;
     cfg.gridDim = dim3(grid);
     cfg.blockDim = dim3(TC_THREADS);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
     cfg.attrs = attr;
-    cfg.numAttrs = 2;
+    cfg.numAttrs = 1;
     note_launch();
     return cudaLaunchKernelEx(&cfg, kern, p, tmk, tmv, tmq);
 }
@@ -1180,3 +1241,4 @@ cudaError_t launch_decode_tc(const DecodeParams &p, const CUtensorMap &tmk, cons
 }
 
 }  // namespace pkv
+

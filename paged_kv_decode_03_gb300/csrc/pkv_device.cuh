@@ -114,6 +114,32 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, unsign
     }
 }
 
+// Spinning variant of mbar_wait for the roles on a pipeline's critical path:
+// try_wait without a suspend-time hint returns after a short, system-defined
+// interval, so a completed phase is seen within that interval instead of
+// after a wake-up from a longer sleep.  Bounded like mbar_wait.
+__device__ __forceinline__ bool mbar_wait_spin(uint64_t *bar, uint32_t parity, unsigned int *err,
+                                               uint64_t limit_ns = 2000000000ull)
+{
+    const uint64_t t0 = global_timer_ns();
+    for (uint32_t it = 1;; ++it) {
+        uint32_t ok;
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+            "selp.u32 %0, 1, 0, p;\n\t}"
+            : "=r"(ok)
+            : "r"(smem_u32(bar)), "r"(parity)
+            : "memory");
+        if (ok)
+            return true;
+        if ((it & 255u) == 0 && global_timer_ns() - t0 > limit_ns) {
+            record_error(err, PKV_DEV_TIMEOUT);
+            return false;
+        }
+    }
+}
+
 // ------------------------------------------------ flags between CTAs
 __device__ __forceinline__ void st_release_gpu(int *addr, int v)
 {
@@ -367,6 +393,43 @@ __device__ __forceinline__ void tmem_ld(uint32_t taddr, float (&v)[N])
 #pragma unroll
     for (int i = 0; i < N; ++i)
         v[i] = __uint_as_float(r[i]);
+}
+
+// Store N consecutive fp32 columns (N = 2, 4, 8 or 16) of this thread's
+// TMEM lane and wait until the stores are done.
+template <int N>
+__device__ __forceinline__ void tmem_st(uint32_t taddr, const float (&v)[N])
+{
+    uint32_t r[N];
+#pragma unroll
+    for (int i = 0; i < N; ++i)
+        r[i] = __float_as_uint(v[i]);
+    if constexpr (N == 2) {
+        asm volatile("tcgen05.st.sync.aligned.32x32b.x2.b32 [%0], {%1,%2};\n\t"
+                     "tcgen05.wait::st.sync.aligned;" ::"r"(taddr), "r"(r[0]), "r"(r[1])
+                     : "memory");
+    } else if constexpr (N == 4) {
+        asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1,%2,%3,%4};\n\t"
+                     "tcgen05.wait::st.sync.aligned;" ::"r"(taddr), "r"(r[0]), "r"(r[1]),
+                     "r"(r[2]), "r"(r[3])
+                     : "memory");
+    } else if constexpr (N == 8) {
+        asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};\n\t"
+                     "tcgen05.wait::st.sync.aligned;" ::"r"(taddr),
+                     "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]),
+                     "r"(r[7])
+                     : "memory");
+    } else {
+        static_assert(N == 16, "columns");
+        asm volatile(
+            "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+            "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};\n\t"
+            "tcgen05.wait::st.sync.aligned;" ::"r"(taddr),
+            "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+            "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
+            "r"(r[15])
+            : "memory");
+    }
 }
 
 // 16 consecutive fp32 columns of this thread's TMEM lane (32x32b shape).

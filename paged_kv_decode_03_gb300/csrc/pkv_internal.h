@@ -45,7 +45,7 @@ struct DecodeParams {
     int32_t *tc_seqoff;       // [batch + 1] first tile of each sequence
     float *sub_lse;           // [grid][2][16] partial states of items cut at CTA boundaries
     float *sub_o;             // [grid][2][16][head_dim]
-    int32_t *tc_flags;        // [grid][2] partial state published (cleared by the plan)
+    int32_t *tc_flags;        // [grid][2] tickets of cut items, by first CTA (cleared by the plan)
     // CUDA-core kernel: (sequence, length) pairs longest first (NULL = in
     // order), and the workspace that may hold them ([batch] int2; NULL = none)
     const int32_t *seq_order;

@@ -133,6 +133,31 @@ def test_int8_kv_alias_per_token():
     _run_case(spec, splits=(0, 64))
 
 
+@pytest.mark.parametrize("kv", ["int8_token", "int8_head"])
+def test_append_non_finite_inputs_bit_exact(kv):
+    """NaN and +-inf in the appended rows: codes and scales bit-exact with the
+    oracle (a NaN has no code and is stored as 0; an inf makes the token's
+    per-token scale inf, so its codes are 0, or saturates under a per-head
+    scale)."""
+    import dataclasses
+    spec = synth.Spec(f"nonfinite_{kv}", batch=6, num_q_heads=4, num_kv_heads=2, head_dim=64,
+                      lens=("fixed", (1, 5, 16, 17, 30, 40)), kv=kv, seed=13)
+    w = synth.make_workload(spec)
+    nk, nv = w.new_k.copy(), w.new_v.copy()
+    nk[0, 0, 3] = 0x7F80   # +inf
+    nk[1, 1, 0] = 0x7FC0   # NaN
+    nv[2, 0, 5] = 0xFF80   # -inf
+    nv[3, 1, 7] = 0x7FC0   # NaN
+    nk[4, 0, :] = 0x7FC0   # one head all NaN
+    w = dataclasses.replace(w, new_k=nk, new_v=nv)
+    gp = _gpu.device_pool(w)
+    _gpu.append_all(w, gp)
+    op = _util.oracle_pool(w)
+    torch.cuda.synchronize()
+    _check_pool_bits(gp, op)
+    assert pkv.device_status(clear=True) == 0
+
+
 def test_split_partial_matches_oracle_partials():
     """paged_decode_split_partial writes, per split, the log-sum-exp and the
     normalised output of that split's keys."""

@@ -27,7 +27,8 @@ def test_quantizer_golden(case):
     """Hand-derived vectors (CS336 lecture 10, int8 quantisation section)."""
     mode, scale, x, q = case
     xb = bits(x)
-    assert np.array_equal(synth.bf16_bits_to_f32(xb), x), "fixture inputs must be bf16-exact"
+    assert np.array_equal(synth.bf16_bits_to_f32(xb), x, equal_nan=True), \
+        "fixture inputs must be bf16-exact"
     if mode == "per_token":
         s = oracle.per_token_scale(xb)
         assert s.view(np.uint32) == scale.view(np.uint32), (s, scale)
