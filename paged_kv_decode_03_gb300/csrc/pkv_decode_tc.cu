@@ -910,7 +910,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
 #pragma unroll
                 for (int h = 0; h < GP; ++h) {
                     sc[h] = (live && ok && h < G) ? s[h] * qk : -INFINITY;
-                    big |= sc[h] > mrun_s[h] + 8.f;
+                    big |= sc[h] > mrun_s[h] + 8.f;  // no stores in between: loads overlap
                 }
                 // ---- running max: changed only when some score exceeds it by
                 // more than 2^8.  group_any is also the barrier after which
@@ -963,12 +963,30 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                     }
                     tc_fence_before();
                 }
-                // ---- probabilities, running sums, P^T (bf16, K-major, swizzled)
+                // ---- probabilities, running sums, P^T (bf16, K-major, swizzled).
+                // The maxima and rescale factors are read into registers
+                // first: read inside the loop, behind its shared-memory
+                // stores, every head would wait for its own load.
+                float mr[GP], al[GP];
+#pragma unroll
+                for (int h4 = 0; h4 < GP; h4 += (GP >= 4 ? 4 : GP)) {
+                    if constexpr (GP >= 4) {
+                        const float4 m4 = *reinterpret_cast<const float4 *>(mrun_s + h4);
+                        const float4 a4 = *reinterpret_cast<const float4 *>(alpha_s + h4);
+                        mr[h4] = m4.x; mr[h4 + 1] = m4.y; mr[h4 + 2] = m4.z; mr[h4 + 3] = m4.w;
+                        al[h4] = a4.x; al[h4 + 1] = a4.y; al[h4 + 2] = a4.z; al[h4 + 3] = a4.w;
+                    } else {
+                        const float2 m2 = *reinterpret_cast<const float2 *>(mrun_s + h4);
+                        const float2 a2 = *reinterpret_cast<const float2 *>(alpha_s + h4);
+                        mr[h4] = m2.x; mr[h4 + 1] = m2.y;
+                        al[h4] = a2.x; al[h4 + 1] = a2.y;
+                    }
+                }
                 uint8_t *pb = ps + sb * 8192 + (t >> 6) * 2048;
 #pragma unroll
                 for (int h = 0; h < GP; ++h) {
-                    const float pr = sc[h] == -INFINITY ? 0.f : fast_exp2(sc[h] - mrun_s[h]);
-                    lpart[h] = rescale ? fmaf(lpart[h], alpha_s[h], pr) : lpart[h] + pr;
+                    const float pr = sc[h] == -INFINITY ? 0.f : fast_exp2(sc[h] - mr[h]);
+                    lpart[h] = rescale ? fmaf(lpart[h], al[h], pr) : lpart[h] + pr;
                     const __nv_bfloat16 hi = __float2bfloat16_rn(pr);
                     *reinterpret_cast<__nv_bfloat16 *>(pb + swz(h, t & 63)) = hi;
                     if (precise)
