@@ -55,6 +55,10 @@ def parse_args():
                     help="override the workload's batch (smaller cases for profiling)")
     ap.add_argument("--split-tokens", type=int, default=None,
                     help="override the split length (0 = single pass, -1 = automatic)")
+    ap.add_argument("--no-per-config", action="store_true",
+                    help="skip the per-workload lines (every config, the six-layer step, "
+                         "the oracle at all threads and at one thread)")
+    ap.add_argument("--per-config-steps", type=int, default=100)
     return ap.parse_args()
 
 
@@ -195,24 +199,21 @@ def whole_job_gbs(bytes_per_rank_step: float, ms_per_step: float, world: int) ->
     return world * bytes_per_rank_step / (ms_per_step * 1e-3) / 1e9
 
 
-def run_ours(args, rank, world, local_rank):
+def _dbits(a, dev):
+    import torch
+    return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(dev)
+
+
+def _dnum(a, dev):
+    import torch
+    return torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+
+
+def device_pool(spec, w, dev, hist=True):
+    """A poisoned device pool for the workload, with its history appended."""
     import torch
     import paged_kv_decode_03_gb300 as pkv
-
-    torch.cuda.set_device(local_rank)
-    dev = torch.device("cuda", local_rank)
-    pkv.load_library()
-    spec = workload_spec(args)
-    w = synth.make_workload(spec)
-    B, Hq, D = w.q.shape
-    P = spec.block_size
-
-    def dbits(a):
-        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(dev)
-
-    def dnum(a):
-        return torch.from_numpy(np.ascontiguousarray(a)).to(dev)
-
+    P, D = spec.block_size, spec.head_dim
     shape = (w.layout.num_blocks, P, spec.num_kv_heads, D)
     if spec.kv == "bf16":
         k_pool = torch.full(shape, int(np.int16(synth.BF16_NAN.view(np.int16))), dtype=torch.int16,
@@ -228,122 +229,178 @@ def run_ours(args, rank, world, local_rank):
         vs = None if spec.alias else ks.clone()
     elif spec.kv == "int8_head":
         mode = pkv.SCALE_PER_HEAD
-        ks = dnum(w.k_head_scale)
-        vs = None if spec.alias else dnum(w.v_head_scale)
+        ks = _dnum(w.k_head_scale, dev)
+        vs = None if spec.alias else _dnum(w.v_head_scale, dev)
     pool = pkv.PagedKVPool(k=k_pool, v=v_pool, k_scale=ks, v_scale=vs, scale_mode=mode)
-    T = len(w.hist_slots)
-    for s in range(0, T, 1 << 16):
-        e = min(T, s + (1 << 16))
-        pkv.paged_kv_append(dbits(w.hist_k[s:e]), None if w.hist_v is None else dbits(w.hist_v[s:e]),
-                            dnum(w.hist_slots[s:e]), pool)
-    q = dbits(w.q)
-    bt = dnum(w.block_table)
-    sl = dnum(w.seq_lens)
-    k_new = dbits(w.new_k)
-    v_new = None if w.new_v is None else dbits(w.new_v)
-    slots = dnum(w.new_slots)
-    out = torch.empty((B, Hq, D), dtype=torch.bfloat16, device=dev)
-    max_len = int(w.seq_lens.max())
-    scale = float(np.float32(spec.softmax_scale))
-    req = args.split_tokens if args.split_tokens is not None else (spec.split_tokens
-                                                                    or pkv.SPLIT_AUTO)
-    # A workload that names its split length (or --split-tokens) runs the two
-    # split-KV calls; otherwise one paged_decode_attention call.
-    split_api = req != pkv.SPLIT_AUTO and req > 0
-    st = pkv.paged_decode_split_tokens(B, Hq, spec.num_kv_heads, max_len, spec.window, req)
-    ns = pkv.paged_decode_num_splits(max_len, spec.window, st) if st > 0 else 1
-    split_api = split_api and st > 0
-    ws_bytes = pkv.paged_decode_workspace_bytes(B, Hq, spec.num_kv_heads, D, max_len,
-                                                spec.window, st)
-    ws = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device=dev)
-    pws = torch.empty(max(pkv.paged_decode_partial_workspace_bytes(B, Hq, spec.num_kv_heads, D),
-                          256), dtype=torch.uint8, device=dev)
-    lse = torch.empty((B, ns, Hq), dtype=torch.float32, device=dev)
-    po = torch.empty((B, ns, Hq, D), dtype=torch.float32, device=dev)
-    tc = pkv.uses_tensor_cores(pool, Hq)
-    torch.cuda.synchronize()
-    pkv.device_status(clear=True)
+    if hist:
+        T = len(w.hist_slots)
+        for s in range(0, T, 1 << 16):
+            e = min(T, s + (1 << 16))
+            pkv.paged_kv_append(_dbits(w.hist_k[s:e], dev),
+                                None if w.hist_v is None else _dbits(w.hist_v[s:e], dev),
+                                _dnum(w.hist_slots[s:e], dev), pool)
+    return pool
 
-    def step(ev=None):
-        if ev is not None:
-            ev[0].record()
-        pkv.paged_kv_append(k_new, v_new, slots, pool)
-        if ev is not None:
-            ev[1].record()
-        if split_api:
-            pkv.paged_decode_split_partial(q, pool, bt, sl, spec.window, scale, st, lse, po, out,
-                                           max_len, workspace=pws)
-            if ev is not None:
-                ev[2].record()
-            pkv.paged_decode_lse_combine(lse, po, sl, spec.window, st, out)
+
+def config_dict(spec, w, st, ns, split_api, world):
+    """The workload as both arms describe it (the reference arm's line
+    carries the same dict, so the two lines can be compared key by key)."""
+    dbytes_kv = bytes_model.decode_bytes(spec, w.seq_lens, w.block_table)["kv"]
+    return {
+        "workload": workload_desc(spec),
+        "batch": int(spec.batch), "num_q_heads": spec.num_q_heads,
+        "num_kv_heads": spec.num_kv_heads, "head_dim": spec.head_dim, "window": spec.window,
+        "block_size": spec.block_size, "num_blocks": int(w.layout.num_blocks),
+        "kv": spec.kv, "k_equals_v": bool(spec.alias),
+        "split_tokens": int(st), "num_splits": int(ns),
+        "step": ("append 1 token/seq + decode (split partial + combine)" if split_api
+                 else "append 1 token/seq + paged_decode_attention"),
+        "l2": f"inputs larger than L2 ({dbytes_kv / 1e6:.0f} MB of KV read per step vs 129 MB L2); no flush",
+        "parallelism": "one batch" if world == 1 else f"replicas: one independent batch per GPU x{world}",
+    }
+
+
+class LayerRun:
+    """Device buffers of one layer's decode step and its captured graphs:
+    append, decode (one paged_decode_attention call, or the split partial
+    call when ``split_api``) and, for the split path, the combine."""
+
+    def __init__(self, spec, w, dev, req_split, split_api_allowed=True):
+        import torch
+        import paged_kv_decode_03_gb300 as pkv
+        self.spec, self.w = spec, w
+        B, Hq, D = w.q.shape
+        self.pool = device_pool(spec, w, dev)
+        self.q = _dbits(w.q, dev)
+        self.bt = _dnum(w.block_table, dev)
+        self.sl = _dnum(w.seq_lens, dev)
+        self.k_new = _dbits(w.new_k, dev)
+        self.v_new = None if w.new_v is None else _dbits(w.new_v, dev)
+        self.slots = _dnum(w.new_slots, dev)
+        self.out = torch.empty((B, Hq, D), dtype=torch.bfloat16, device=dev)
+        self.max_len = int(w.seq_lens.max())
+        self.scale = float(np.float32(spec.softmax_scale))
+        # a workload that names its split length (or --split-tokens) runs the
+        # two split-KV calls; otherwise one paged_decode_attention call
+        self.split_api = split_api_allowed and req_split != pkv.SPLIT_AUTO and req_split > 0
+        self.st = pkv.paged_decode_split_tokens(B, Hq, spec.num_kv_heads, self.max_len,
+                                                spec.window, req_split)
+        self.ns = pkv.paged_decode_num_splits(self.max_len, spec.window, self.st) if self.st > 0 else 1
+        self.split_api = self.split_api and self.st > 0
+        ws_bytes = pkv.paged_decode_workspace_bytes(B, Hq, spec.num_kv_heads, D, self.max_len,
+                                                    spec.window, self.st)
+        self.ws = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device=dev)
+        self.pws = torch.empty(max(pkv.paged_decode_partial_workspace_bytes(B, Hq, spec.num_kv_heads, D),
+                                   256), dtype=torch.uint8, device=dev)
+        self.lse = torch.empty((B, self.ns, Hq), dtype=torch.float32, device=dev)
+        self.po = torch.empty((B, self.ns, Hq, D), dtype=torch.float32, device=dev)
+        self.tc = pkv.uses_tensor_cores(self.pool, Hq)
+        dbytes = bytes_model.decode_bytes(spec, w.seq_lens, w.block_table)
+        self.dbytes = dbytes
+        self.abytes = bytes_model.append_bytes(spec, int((w.new_slots >= 0).sum()))
+        self.step_bytes = dbytes["kv"] + dbytes["q"] + dbytes["out"] + self.abytes
+        self.decode_kernel_bytes = dbytes["kv"] + dbytes["q"] + (dbytes["out"] if not self.split_api else 0)
+        self.graphs = None
+
+    def append(self):
+        import paged_kv_decode_03_gb300 as pkv
+        pkv.paged_kv_append(self.k_new, self.v_new, self.slots, self.pool)
+
+    def decode(self):
+        import paged_kv_decode_03_gb300 as pkv
+        s = self.spec
+        if self.split_api:
+            pkv.paged_decode_split_partial(self.q, self.pool, self.bt, self.sl, s.window, self.scale,
+                                           self.st, self.lse, self.po, self.out, self.max_len,
+                                           workspace=self.pws)
         else:
-            pkv.paged_decode_attention(q, pool, bt, sl, spec.window, scale, out, max_len,
-                                       split_tokens=st, workspace=ws)
-            if ev is not None:
-                ev[2].record()
-        if ev is not None:
-            ev[3].record()
+            pkv.paged_decode_attention(self.q, self.pool, self.bt, self.sl, s.window, self.scale,
+                                       self.out, self.max_len, split_tokens=self.st,
+                                       workspace=self.ws)
 
-    # kernels per step, as the library reports them for each call
-    launches_per_step = 0
-    pkv.paged_kv_append(k_new, v_new, slots, pool)
-    launches_per_step += pkv.last_launch_count()
-    if split_api:
-        pkv.paged_decode_split_partial(q, pool, bt, sl, spec.window, scale, st, lse, po, out,
-                                       max_len, workspace=pws)
-        launches_per_step += pkv.last_launch_count()
-        pkv.paged_decode_lse_combine(lse, po, sl, spec.window, st, out)
-        launches_per_step += pkv.last_launch_count()
-    else:
-        pkv.paged_decode_attention(q, pool, bt, sl, spec.window, scale, out, max_len,
-                                   split_tokens=st, workspace=ws)
-        launches_per_step += pkv.last_launch_count()
-    dbytes = bytes_model.decode_bytes(spec, w.seq_lens, w.block_table)
-    abytes = bytes_model.append_bytes(spec, int((w.new_slots >= 0).sum()))
-    step_bytes = dbytes["kv"] + dbytes["q"] + dbytes["out"] + abytes
-    decode_kernel_bytes = dbytes["kv"] + dbytes["q"] + (dbytes["out"] if not split_api else 0)
+    def combine(self):
+        import paged_kv_decode_03_gb300 as pkv
+        pkv.paged_decode_lse_combine(self.lse, self.po, self.sl, self.spec.window, self.st, self.out)
 
-    for _ in range(max(3, args.warmup)):
-        step()
-    torch.cuda.synchronize()
-    # The step's three parts (append, decode, combine) are captured as CUDA
-    # graphs and replayed, so that the timed region measures the GPU and not
-    # the Python loop that enqueues the calls; events between the replays
-    # give the per-part device times.
-    parts = [None, None, None]
-    cap = torch.cuda.Stream()
-    cap.wait_stream(torch.cuda.current_stream())
-    with torch.cuda.stream(cap):
-        parts[0] = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(parts[0], stream=cap):
-            pkv.paged_kv_append(k_new, v_new, slots, pool)
-        parts[1] = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(parts[1], stream=cap):
-            if split_api:
-                pkv.paged_decode_split_partial(q, pool, bt, sl, spec.window, scale, st, lse, po,
-                                               out, max_len, workspace=pws)
-            else:
-                pkv.paged_decode_attention(q, pool, bt, sl, spec.window, scale, out, max_len,
-                                           split_tokens=st, workspace=ws)
-        if split_api:
-            parts[2] = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(parts[2], stream=cap):
-                pkv.paged_decode_lse_combine(lse, po, sl, spec.window, st, out)
-    torch.cuda.current_stream().wait_stream(cap)
-    torch.cuda.synchronize()
+    def step(self):
+        self.append()
+        self.decode()
+        if self.split_api:
+            self.combine()
 
-    def replay(ev):
+    def launches_per_step(self):
+        import paged_kv_decode_03_gb300 as pkv
+        n = 0
+        for part in ([self.append, self.decode] + ([self.combine] if self.split_api else [])):
+            part()
+            n += pkv.last_launch_count()
+        return n
+
+    def capture(self):
+        """The step's parts as CUDA graphs, replayed so that the timed region
+        measures the GPU and not the Python loop that enqueues the calls;
+        events between the replays give the per-part device times."""
+        import torch
+        parts = [None, None, None]
+        cap = torch.cuda.Stream()
+        cap.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(cap):
+            for i, fn in enumerate([self.append, self.decode] + ([self.combine] if self.split_api else [])):
+                parts[i] = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(parts[i], stream=cap):
+                    fn()
+        torch.cuda.current_stream().wait_stream(cap)
+        torch.cuda.synchronize()
+        self.graphs = parts
+
+    def replay(self, ev):
         ev[0].record()
-        parts[0].replay()
+        self.graphs[0].replay()
         ev[1].record()
-        parts[1].replay()
+        self.graphs[1].replay()
         ev[2].record()
-        if parts[2] is not None:
-            parts[2].replay()
+        if self.graphs[2] is not None:
+            self.graphs[2].replay()
         ev[3].record()
 
+
+def part_times(evs):
+    app = statistics.mean(e[0].elapsed_time(e[1]) for e in evs) * 1e3
+    dec = statistics.mean(e[1].elapsed_time(e[2]) for e in evs) * 1e3
+    cmb = statistics.mean(e[2].elapsed_time(e[3]) for e in evs) * 1e3
+    return app, dec, cmb
+
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+    import paged_kv_decode_03_gb300 as pkv
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    pkv.load_library()
+    spec = workload_spec(args)
+    w = synth.make_workload(spec)
+    B, Hq, D = w.q.shape
+    P = spec.block_size
+    req = args.split_tokens if args.split_tokens is not None else (spec.split_tokens
+                                                                    or pkv.SPLIT_AUTO)
+    run = LayerRun(spec, w, dev, req)
+    pool, q, bt, sl = run.pool, run.q, run.bt, run.sl
+    k_new, v_new, slots, out = run.k_new, run.v_new, run.slots, run.out
+    max_len, scale, split_api, st, ns = run.max_len, run.scale, run.split_api, run.st, run.ns
+    ws, pws, lse, po, tc = run.ws, run.pws, run.lse, run.po, run.tc
+    torch.cuda.synchronize()
+    pkv.device_status(clear=True)
+    dbytes, abytes, step_bytes = run.dbytes, run.abytes, run.step_bytes
+    decode_kernel_bytes = run.decode_kernel_bytes
+    launches_per_step = run.launches_per_step()
+    for _ in range(max(3, args.warmup)):
+        run.step()
+    torch.cuda.synchronize()
+    run.capture()
+
     for _ in range(3):
-        replay([torch.cuda.Event(enable_timing=True) for _ in range(4)])
+        run.replay([torch.cuda.Event(enable_timing=True) for _ in range(4)])
     torch.cuda.synchronize()
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
     if world > 1:
@@ -356,7 +413,7 @@ def run_ours(args, rank, world, local_rank):
     t0 = time.time()
     start.record()
     for i in range(args.steps):
-        replay(evs[i])
+        run.replay(evs[i])
     end.record()
     torch.cuda.synchronize()
     t1 = time.time()
@@ -365,10 +422,9 @@ def run_ours(args, rank, world, local_rank):
     clocks = sampler.stop(t0, t1) if sampler else None
     elapsed_ms = max_over_ranks(start.elapsed_time(end), world, dev)
     status = pkv.device_status(clear=True)
-    app_us = statistics.mean(e[0].elapsed_time(e[1]) for e in evs) * 1e3
-    dec_us = statistics.mean(e[1].elapsed_time(e[2]) for e in evs) * 1e3
-    cmb_us = (statistics.mean(e[2].elapsed_time(e[3]) for e in evs) * 1e3
-              if parts[2] is not None else 0.0)
+    app_us, dec_us, cmb_us = part_times(evs)
+    if not split_api:
+        cmb_us = 0.0
     ms_per_step = elapsed_ms / args.steps
     value = whole_job_gbs(step_bytes, ms_per_step, world)
 
@@ -449,18 +505,11 @@ def run_ours(args, rank, world, local_rank):
         "vs_baseline": None,
         "dtype": "bf16" if spec.kv == "bf16" else "int8 KV / bf16 q",
         "data": "synthetic (seeded N(0,1) bf16 K/V/q; shuffled physical blocks)",
-        "config": {
-            "workload": workload_desc(spec),
-            "batch": B, "num_q_heads": Hq, "num_kv_heads": spec.num_kv_heads, "head_dim": D,
-            "window": spec.window, "block_size": P, "num_blocks": w.layout.num_blocks,
-            "split_tokens": st, "num_splits": ns,
-            "step": ("append 1 token/seq + decode (split partial + combine)" if split_api
-                     else "append 1 token/seq + paged_decode_attention"),
+        "config": config_dict(spec, w, st, ns, split_api, world),
+        "method": {
             "timing": "CUDA-graph replays of the step's parts, CUDA events between them",
             "decode_kernel": ("tensor cores (tcgen05), persistent stream-K" if tc
                               else "CUDA cores"),
-            "l2": f"inputs larger than L2 ({dbytes['kv'] / 1e6:.0f} MB of KV read per step vs 129 MB L2); no flush",
-            "parallelism": f"replicas: one independent batch per GPU x{world}",
         },
         "pct_of_nominal_8tbs": round(100 * value / world / NOMINAL_HBM_GBS, 2),
         "pct_of_measured_peak": round(100 * value / world / peak, 2),
@@ -484,7 +533,218 @@ def run_ours(args, rank, world, local_rank):
         line["e2e"] = {k: (round(v, 4) if isinstance(v, float) else v) for k, v in e2e.items()}
     if cpu is not None:
         line["cpu_baseline"] = cpu
+    if (world == 1 and not args.no_per_config and args.config == "c2" and not args.batch
+            and args.split_tokens is None):
+        main = {"workload": workload_desc(spec), "call": "paged_decode_attention",
+                "decode_kernel": line["method"]["decode_kernel"],
+                "kernels_us": line["kernels_us"], "ms_per_step": line["ms_per_step"],
+                "algorithmic_bytes_per_launch": decode_kernel_bytes,
+                "achieved_gbs": round(achieved, 1), "frac_of_measured": round(achieved / peak, 4),
+                "pct_of_8tbs": round(100 * achieved / NOMINAL_HBM_GBS, 2),
+                "traffic": recorded_traffic("c2"),
+                "seq_layer_steps_per_s": round(B / (ms_per_step * 1e-3), 1),
+                "device_error_word": status}
+        del run, pool, q, bt, sl, k_new, v_new, slots, out, ws, pws, lse, po
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
+        line["per_config"] = per_config(args, dev, main, spec, w)
     return line
+
+
+# ------------------------------------------------------- every workload
+def oracle_full_run(spec, w, layers=None):
+    """One full step of the oracle (append every sequence's new token, decode
+    every row) with all host threads and with one thread, in seconds.  For a
+    multi-layer step, ``layers`` are the per-layer workloads (layers sharing
+    history values share one oracle pool: the timing does not depend on the
+    appended token's values)."""
+    import oracle
+    layers = layers or [w]
+    pools = {}
+    for lw in layers:
+        if id(lw.hist_k) not in pools:
+            pools[id(lw.hist_k)] = oracle_setup(lw.spec, lw)
+    threads = oracle.max_threads()
+    times = {}
+    for label, nt in (("all_threads_s", 0), ("one_thread_s", 1)):
+        t = 0.0
+        for lw in layers:
+            pool = pools[id(lw.hist_k)]
+            s = lw.spec
+            t0 = time.perf_counter()
+            oracle.append(lw.new_k, lw.new_v, lw.new_slots, pool)
+            oracle.decode(lw.q, pool, lw.block_table, lw.seq_lens, s.num_q_heads, s.window,
+                          np.float32(s.softmax_scale), num_threads=nt)
+            t += time.perf_counter() - t0
+        times[label] = round(t, 4)
+    return {"kind": "oracle", "threads": threads, **times,
+            "sample": f"one full step: {len(layers)} layer(s) x (append {w.spec.batch} tokens + "
+                      f"decode {w.spec.batch}x{w.spec.num_q_heads} rows), fp64 C oracle"}
+
+
+def measure_layer(spec, w, dev, req, steps, warmup, split_api_allowed=True):
+    """Decode-kernel timing of one workload as the main line takes it."""
+    import torch
+    import paged_kv_decode_03_gb300 as pkv
+    run = LayerRun(spec, w, dev, req, split_api_allowed)
+    launches = run.launches_per_step()
+    for _ in range(max(3, warmup)):
+        run.step()
+    torch.cuda.synchronize()
+    run.capture()
+    for _ in range(3):
+        run.replay([torch.cuda.Event(enable_timing=True) for _ in range(4)])
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(steps)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    start.record()
+    for i in range(steps):
+        run.replay(evs[i])
+    end.record()
+    torch.cuda.synchronize()
+    ms = start.elapsed_time(end) / steps
+    app, dec, cmb = part_times(evs)
+    peak, _ = peaks()
+    achieved = run.decode_kernel_bytes / (dec * 1e-6) / 1e9
+    B = spec.batch
+    entry = {
+        "workload": workload_desc(spec),
+        "call": ("paged_decode_split_partial + paged_decode_lse_combine" if run.split_api
+                 else "paged_decode_attention") + (f", split_tokens {run.st}" if run.st else ""),
+        "decode_kernel": ("tensor cores (tcgen05), persistent stream-K" if run.tc else "CUDA cores"),
+        "kernels_us": {"append": round(app, 3), "decode": round(dec, 3),
+                       "combine": round(cmb if run.split_api else 0.0, 3)},
+        "ms_per_step": round(ms, 6),
+        "algorithmic_bytes_per_launch": run.decode_kernel_bytes,
+        "achieved_gbs": round(achieved, 1), "frac_of_measured": round(achieved / peak, 4),
+        "pct_of_8tbs": round(100 * achieved / NOMINAL_HBM_GBS, 2),
+        "step_gbs": round(run.step_bytes / (ms * 1e-3) / 1e9, 1),
+        "seq_layer_steps_per_s": round(B / (ms * 1e-3), 1),
+        "gpu_launches_per_step": launches,
+        "device_error_word": pkv.device_status(clear=True),
+    }
+    del run
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return entry
+
+
+def measure_step(dev, steps, warmup):
+    """The six-layer continuous-batching step (five int8 per-head sliding
+    layers, one bf16 global layer, one ragged layout with shared prefix
+    blocks): one paged_decode_step call captured as one CUDA graph and
+    replayed; events around each replay."""
+    import torch
+    import paged_kv_decode_03_gb300 as pkv
+    layers = synth.make_step(share_history=True)
+    w0 = layers[0]
+    pools, base = [], {}
+    for lw in layers:
+        key = id(lw.hist_k)
+        if key not in base:
+            base[key] = device_pool(lw.spec, lw, dev)
+            pools.append(base[key])
+        else:
+            b = base[key]
+            pools.append(pkv.PagedKVPool(k=b.k.clone(), v=None if b.v is None else b.v.clone(),
+                                         k_scale=b.k_scale, v_scale=b.v_scale,
+                                         scale_mode=b.scale_mode))
+    del base
+    slots, bt, sl = _dnum(w0.new_slots, dev), _dnum(w0.block_table, dev), _dnum(w0.seq_lens, dev)
+    max_len = int(w0.seq_lens.max())
+    dl = [pkv.DecodeLayer(pool=gp, q=_dbits(lw.q, dev), k_new=_dbits(lw.new_k, dev),
+                          v_new=None if lw.new_v is None else _dbits(lw.new_v, dev),
+                          out=torch.empty(lw.q.shape, dtype=torch.bfloat16, device=dev),
+                          window=lw.spec.window, softmax_scale=float(np.float32(lw.spec.softmax_scale)))
+          for lw, gp in zip(layers, pools)]
+    ws = torch.empty(max(256, pkv.paged_decode_step_workspace_bytes(dl, max_len)),
+                     dtype=torch.uint8, device=dev)
+
+    def call():
+        pkv.paged_decode_step(dl, slots, bt, sl, max_len, workspace=ws)
+
+    call()
+    launches = pkv.last_launch_count()
+    for _ in range(max(3, warmup)):
+        call()
+    torch.cuda.synchronize()
+    cap = torch.cuda.Stream()
+    cap.wait_stream(torch.cuda.current_stream())
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(cap):
+        with torch.cuda.graph(graph, stream=cap):
+            call()
+    torch.cuda.current_stream().wait_stream(cap)
+    for _ in range(3):
+        graph.replay()
+    torch.cuda.synchronize()
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
+    evs[0].record()
+    for i in range(steps):
+        graph.replay()
+        evs[i + 1].record()
+    torch.cuda.synchronize()
+    per = [evs[i].elapsed_time(evs[i + 1]) for i in range(steps)]
+    ms = evs[0].elapsed_time(evs[-1]) / steps
+    step_bytes = 0
+    for lw in layers:
+        d = bytes_model.decode_bytes(lw.spec, lw.seq_lens, lw.block_table)
+        step_bytes += d["kv"] + d["q"] + d["out"]
+        step_bytes += bytes_model.append_bytes(lw.spec, int((lw.new_slots >= 0).sum()))
+    peak, _ = peaks()
+    gbs = step_bytes / (ms * 1e-3) / 1e9
+    B = w0.spec.batch
+    entry = {
+        "workload": (f"c5 continuous-batching step: {len(layers)} layers "
+                     f"({''.join(synth.C5_LAYERS)}) over one layout; sliding: "
+                     f"{workload_desc(layers[0].spec)}; global: {workload_desc(layers[-1].spec)}; "
+                     "history values shared by the sliding layers, each its own pool"),
+        "call": "paged_decode_step (every layer's append + decode), one CUDA graph",
+        "ms_per_step": round(ms, 6), "ms_per_step_median": round(statistics.median(per), 6),
+        "bytes_per_step": int(step_bytes),
+        "step_gbs": round(gbs, 1), "frac_of_measured": round(gbs / peak, 4),
+        "pct_of_8tbs": round(100 * gbs / NOMINAL_HBM_GBS, 2),
+        "seq_layer_steps_per_s": round(B * len(layers) / (ms * 1e-3), 1),
+        "gpu_launches_per_step": launches,
+        "device_error_word": pkv.device_status(clear=True),
+    }
+    del dl, pools, ws, graph
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return entry, layers
+
+
+def per_config(args, dev, main_entry, main_spec, main_w):
+    """Every workload at its full size: the decode kernel's time and roofline
+    fraction (CUDA events over CUDA-graph replays), the six-layer step, and
+    one full run of the oracle per workload at all host threads and at one
+    thread."""
+    import paged_kv_decode_03_gb300 as pkv
+    out = {}
+    steps, warm = args.per_config_steps, 5
+    cpu = not args.no_cpu_baseline
+    out["c2"] = main_entry
+    if cpu:
+        out["c2"]["oracle"] = oracle_full_run(main_spec, main_w)
+    for name in ("c1", "c3", "c4", "c5s", "c5g"):
+        spec = synth.CONFIGS[name]
+        w = synth.make_workload(spec)
+        req = spec.split_tokens or pkv.SPLIT_AUTO
+        # the library's decode call (paged_decode_attention) with the
+        # workload's split length
+        out[name] = measure_layer(spec, w, dev, req, steps, warm, split_api_allowed=False)
+        out[name]["traffic"] = recorded_traffic(name)
+        if spec.split_tokens:
+            # and the two split-KV calls with that split length
+            out[name + "_split_calls"] = measure_layer(spec, w, dev, req, steps, warm)
+        if cpu:
+            out[name]["oracle"] = oracle_full_run(spec, w)
+        del w
+    entry, layers = measure_step(dev, max(20, steps // 2), warm)
+    out["c5"] = entry
+    if cpu:
+        out["c5"]["oracle"] = oracle_full_run(layers[0].spec, layers[0], layers)
+    return out
 
 
 # --------------------------------------------------------- CPU baseline
@@ -531,6 +791,19 @@ def cpu_baseline(spec, w, step_bytes, budget_s):
                       f"{threads} OpenMP threads"}
 
 
+def reference_config(spec, w):
+    """The config dict of our arm's line for the same workload (split length
+    and split count resolved by the library's host-side sizing calls)."""
+    import paged_kv_decode_03_gb300 as pkv
+    B, Hq = w.q.shape[:2]
+    max_len = int(w.seq_lens.max())
+    req = spec.split_tokens or pkv.SPLIT_AUTO
+    st = pkv.paged_decode_split_tokens(B, Hq, spec.num_kv_heads, max_len, spec.window, req)
+    ns = pkv.paged_decode_num_splits(max_len, spec.window, st) if st > 0 else 1
+    split_api = req != pkv.SPLIT_AUTO and req > 0 and st > 0
+    return config_dict(spec, w, st, ns, split_api, 1)
+
+
 def run_reference(args, rank):
     """The oracle timed as the reference arm: each step a bounded sample of
     the workload (whole sequences, all heads), sized so that warmup + steps
@@ -575,8 +848,7 @@ def run_reference(args, rank):
         "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(dt * 1e3, 3), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)",
-        "config": {"workload": workload_desc(spec), "batch": B,
-                   "parallelism": "host cores (OpenMP)"},
+        "config": reference_config(spec, w),
         "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": threads,
                          "kind": "oracle", "sample": sample},
         "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,

@@ -302,6 +302,61 @@ PKV_API int paged_decode_attention_noalloc(const void *q, const pkv_pool *pool,
                                            void *stream);
 
 /*
+ * One layer of a decode step (paged_decode_step).  Every layer has its own
+ * pool, query, new token and output; the layers share the step's layout
+ * (block table, lengths, slot ids), as the layers of one model do.
+ */
+typedef struct pkv_layer {
+    pkv_pool pool;       /* this layer's pool */
+    const void *q;       /* [batch][num_q_heads][head_dim] bf16, 16-byte aligned */
+    const void *k_new;   /* [batch][num_kv_heads][head_dim] bf16: each sequence's new token */
+    const void *v_new;   /* likewise for V; ignored (may be NULL) when the pool has K == V */
+    void *out;           /* [batch][num_q_heads][head_dim], bf16 or fp32 (out_dtype) */
+    int32_t window;      /* 0 = global causal layer; > 0 = sliding window (keys [pos-w, pos]) */
+    float softmax_scale;
+} pkv_layer;
+
+/*
+ * paged_decode_step_workspace_bytes -- device scratch paged_decode_step
+ * needs for these layers: the largest paged_decode_workspace_bytes of any
+ * layer (the layers run one after another on one stream and share it).
+ * `layers` is a host array.  0 if layers is NULL or num_layers <= 0.
+ */
+PKV_API size_t paged_decode_step_workspace_bytes(const pkv_layer *layers, int32_t num_layers,
+                                                 int32_t batch, int32_t num_q_heads,
+                                                 int32_t max_seq_len, int32_t split_tokens);
+
+/*
+ * paged_decode_step -- one decode step of a whole model's attention: for
+ * each layer in order, paged_kv_append of the layer's new tokens at
+ * slot_mapping, then paged_decode_attention over the layer's pool, all
+ * enqueued on `stream` by one call.  (tiniestgpt notes, section 8: a decode
+ * step over static block_table / seq_lens / slot_ids buffers with a host-side
+ * length bound, captured once as a CUDA graph and replayed; CS336 lecture 10,
+ * local/global section: sliding-window layers interleaved with global ones.)
+ *   layers:        host array of num_layers descriptors (read during the
+ *                  call only).
+ *   slot_mapping:  [batch] int64 device array, the new token's slot per
+ *                  sequence (negative = padding, skipped), shared by all
+ *                  layers; block_table, seq_lens, max_seq_len, split_tokens
+ *                  as for paged_decode_attention, shared by all layers.
+ *   workspace:     paged_decode_step_workspace_bytes(...) bytes, 256-byte
+ *                  aligned (shared by the layers; see paged_decode_attention
+ *                  for when it is required).
+ * Every layer's arguments are validated before anything is launched; a
+ * launch that fails part-way leaves the earlier layers enqueued.  Allocates
+ * nothing and reads no device data on the host, so a whole step can be
+ * captured in one CUDA graph.  pkv_last_launch_count() counts every kernel
+ * of the step.
+ */
+PKV_API int paged_decode_step(const pkv_layer *layers, int32_t num_layers,
+                              const int64_t *slot_mapping, const int32_t *block_table,
+                              int32_t max_blocks_per_seq, const int32_t *seq_lens, int32_t batch,
+                              int32_t num_q_heads, int32_t max_seq_len, int32_t split_tokens,
+                              void *workspace, size_t workspace_bytes, int32_t out_dtype,
+                              void *stream);
+
+/*
  * paged_decode_uses_tensor_cores -- 1 if decodes over this pool with
  * num_q_heads query heads run on the tensor-core kernel (bf16 pool,
  * head_dim 128 or 256, 8 to 16 query heads per KV head; PKV_DISABLE_TC=1 /

@@ -3,7 +3,8 @@
 Python face of the C-ABI library ``libpagedkv.so`` (declared in
 ``include/pagedkv.h``): ``paged_kv_append`` and ``paged_decode_attention``,
 plus the two steps of the split-KV path (``paged_decode_split_partial``,
-``paged_decode_lse_combine``).  The binding only marshals arguments; every
+``paged_decode_lse_combine``) and a whole model step over one layout
+(``paged_decode_step``).  The binding only marshals arguments; every
 step of the computation runs in the library's sm_103a kernels.  There is no
 CPU fallback: if the library is missing, the first call raises.
 """
@@ -13,6 +14,6 @@ from .binding import (  # noqa: F401
     paged_decode_lse_combine, paged_decode_workspace_bytes, paged_decode_num_splits,
     paged_decode_split_tokens, PagedKVError, paged_decode_attention_noalloc,
     paged_decode_partial_workspace_bytes, uses_tensor_cores, last_launch_count,
-    STATIC_SCRATCH_BYTES,
+    STATIC_SCRATCH_BYTES, DecodeLayer, paged_decode_step, paged_decode_step_workspace_bytes,
     library_path, load_library, device_status, exported_symbols,
 )

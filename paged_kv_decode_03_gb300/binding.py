@@ -42,6 +42,19 @@ class PkvPoolC(ctypes.Structure):
     ]
 
 
+class PkvLayerC(ctypes.Structure):
+    """Mirror of ``pkv_layer`` in include/pagedkv.h."""
+    _fields_ = [
+        ("pool", PkvPoolC),
+        ("q", ctypes.c_void_p),
+        ("k_new", ctypes.c_void_p),
+        ("v_new", ctypes.c_void_p),
+        ("out", ctypes.c_void_p),
+        ("window", ctypes.c_int32),
+        ("softmax_scale", ctypes.c_float),
+    ]
+
+
 def library_path() -> str:
     return LIB_PATH
 
@@ -78,6 +91,10 @@ def load_library():
     lib.paged_decode_attention_noalloc.argtypes = [p, p, p, i32, p, i32, i32, i32, i32, f32,
                                                    i32, p, i32, p]
     lib.paged_decode_attention_noalloc.restype = ctypes.c_int
+    lib.paged_decode_step_workspace_bytes.argtypes = [p, i32, i32, i32, i32, i32]
+    lib.paged_decode_step_workspace_bytes.restype = sz
+    lib.paged_decode_step.argtypes = [p, i32, p, p, i32, p, i32, i32, i32, i32, p, sz, i32, p]
+    lib.paged_decode_step.restype = ctypes.c_int
     lib.paged_decode_uses_tensor_cores.argtypes = [p, i32]
     lib.paged_decode_uses_tensor_cores.restype = i32
     lib.pkv_last_launch_count.argtypes = []
@@ -331,3 +348,65 @@ def device_status(clear: bool = True) -> int:
     if rc < 0:
         _check(rc, "pkv_device_status")
     return rc
+
+
+@dataclass
+class DecodeLayer:
+    """One layer of a decode step: its pool, query [B, H_q, D] bf16, new
+    token K/V [B, H_kv, D] bf16 (v_new None when K and V are one tensor),
+    output [B, H_q, D] (bf16 or fp32), window (0 = global) and softmax scale."""
+    pool: PagedKVPool
+    q: "object"
+    k_new: "object"
+    v_new: Optional[object]
+    out: "object"
+    window: int
+    softmax_scale: float
+
+    def c_struct(self) -> PkvLayerC:
+        return PkvLayerC(self.pool.c_struct(), _dev_ptr(self.q, "q"), _dev_ptr(self.k_new, "k_new"),
+                         _dev_ptr(self.v_new, "v_new"), _dev_ptr(self.out, "out"), int(self.window),
+                         float(self.softmax_scale))
+
+
+def _layers_c(layers):
+    arr = (PkvLayerC * len(layers))()
+    for i, layer in enumerate(layers):
+        arr[i] = layer.c_struct()
+    return arr
+
+
+def paged_decode_step_workspace_bytes(layers, max_seq_len: int,
+                                      split_tokens: int = SPLIT_AUTO) -> int:
+    B, Hq = (int(x) for x in layers[0].q.shape[:2])
+    return int(load_library().paged_decode_step_workspace_bytes(
+        _layers_c(layers), len(layers), B, Hq, int(max_seq_len), int(split_tokens)))
+
+
+def paged_decode_step(layers, slot_mapping, block_table, seq_lens, max_seq_len: int,
+                      split_tokens: int = SPLIT_AUTO, workspace=None, stream=None) -> None:
+    """One decode step of every layer: append each layer's new tokens at
+    ``slot_mapping`` ([B] int64), then decode it, over one shared layout
+    (``block_table``, ``seq_lens``), in one library call that a CUDA graph
+    can capture.  ``workspace``: uint8 CUDA tensor of at least
+    paged_decode_step_workspace_bytes(...) bytes (allocated through torch if
+    None and needed)."""
+    import torch
+    lib = load_library()
+    arr = _layers_c(layers)
+    B, Hq = (int(x) for x in layers[0].q.shape[:2])
+    for layer in layers:
+        if layer.out.dtype != layers[0].out.dtype:
+            raise PagedKVError("all layers' outputs must have one dtype")
+    need = lib.paged_decode_step_workspace_bytes(arr, len(layers), B, Hq, int(max_seq_len),
+                                                 int(split_tokens))
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=layers[0].q.device)
+    ws_ptr = _dev_ptr(workspace, "workspace") if workspace is not None else None
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    out_dtype = OUT_F32 if layers[0].out.dtype == torch.float32 else OUT_BF16
+    _check(lib.paged_decode_step(arr, len(layers), _dev_ptr(slot_mapping, "slot_mapping"),
+                                 _dev_ptr(block_table, "block_table"), int(block_table.shape[1]),
+                                 _dev_ptr(seq_lens, "seq_lens"), B, Hq, int(max_seq_len),
+                                 int(split_tokens), ws_ptr, ws_bytes, out_dtype, _stream(stream)),
+           "paged_decode_step")

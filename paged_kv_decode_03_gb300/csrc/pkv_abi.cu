@@ -641,6 +641,86 @@ PKV_API int paged_decode_attention(const void *q, const pkv_pool *pool, const in
     return PKV_OK;
 }
 
+PKV_API size_t paged_decode_step_workspace_bytes(const pkv_layer *layers, int32_t num_layers,
+                                                 int32_t batch, int32_t num_q_heads,
+                                                 int32_t max_seq_len, int32_t split_tokens)
+{
+    size_t need = 0;
+    if (!layers || num_layers <= 0)
+        return 0;
+    for (int32_t l = 0; l < num_layers; ++l) {
+        const pkv_pool &pl = layers[l].pool;
+        const size_t n = paged_decode_workspace_bytes(batch, num_q_heads, pl.num_kv_heads,
+                                                      pl.head_dim, pl.block_size, max_seq_len,
+                                                      layers[l].window, split_tokens);
+        need = n > need ? n : need;
+    }
+    return need;
+}
+
+PKV_API int paged_decode_step(const pkv_layer *layers, int32_t num_layers,
+                              const int64_t *slot_mapping, const int32_t *block_table,
+                              int32_t max_blocks_per_seq, const int32_t *seq_lens, int32_t batch,
+                              int32_t num_q_heads, int32_t max_seq_len, int32_t split_tokens,
+                              void *workspace, size_t workspace_bytes, int32_t out_dtype,
+                              void *stream)
+{
+    t_last_error.clear();
+    t_launches = 0;
+    if (!layers || num_layers <= 0)
+        return fail(PKV_E_ARG, "no layers");
+    if (!slot_mapping)
+        return fail(PKV_E_NULL, "slot_mapping is NULL");
+    if (!aligned(slot_mapping, 8))
+        return fail(PKV_E_ALIGN, "slot_mapping must be 8-byte aligned");
+    // validate every layer before anything is enqueued
+    for (int32_t l = 0; l < num_layers; ++l) {
+        const pkv_layer &L = layers[l];
+        if (int rc = check_decode_args(L.q, &L.pool, block_table, max_blocks_per_seq, seq_lens,
+                                       batch, num_q_heads, max_seq_len, L.window, L.out,
+                                       out_dtype))
+            return fail(rc, "layer %d: %s", l, std::string(t_last_error).c_str());
+        const bool alias = L.pool.v == nullptr || L.pool.v == L.pool.k;
+        if (!L.k_new || (!alias && !L.v_new))
+            return fail(PKV_E_NULL, "layer %d: k_new or v_new is NULL", l);
+        if (!aligned(L.k_new, 16) || (!alias && !aligned(L.v_new, 16)))
+            return fail(PKV_E_ALIGN, "layer %d: k_new/v_new must be 16-byte aligned", l);
+        const int32_t st = paged_decode_split_tokens(batch, num_q_heads, L.pool.num_kv_heads,
+                                                     L.pool.block_size, max_seq_len, L.window,
+                                                     split_tokens);
+        if (st < 0)
+            return fail(st, "layer %d: %s", l, std::string(t_last_error).c_str());
+        const bool needs_ws = use_tc(&L.pool, num_q_heads / L.pool.num_kv_heads) || st > 0;
+        const size_t need = paged_decode_workspace_bytes(batch, num_q_heads, L.pool.num_kv_heads,
+                                                         L.pool.head_dim, L.pool.block_size,
+                                                         max_seq_len, L.window, st);
+        if (needs_ws && batch > 0 && (!workspace || workspace_bytes < need))
+            return fail(PKV_E_WORKSPACE, "layer %d: workspace of %zu bytes needed, %zu given", l,
+                        need, workspace ? workspace_bytes : (size_t)0);
+        if (needs_ws && workspace && !aligned(workspace, 256))
+            return fail(PKV_E_ALIGN, "workspace must be 256-byte aligned");
+    }
+    int launches = 0;
+    for (int32_t l = 0; l < num_layers; ++l) {
+        const pkv_layer &L = layers[l];
+        int rc = paged_kv_append(L.k_new, L.v_new, slot_mapping, batch, &L.pool, stream);
+        launches += t_launches;
+        if (rc == PKV_OK) {
+            rc = paged_decode_attention(L.q, &L.pool, block_table, max_blocks_per_seq, seq_lens,
+                                        batch, num_q_heads, max_seq_len, L.window,
+                                        L.softmax_scale, split_tokens, workspace, workspace_bytes,
+                                        L.out, out_dtype, stream);
+            launches += t_launches;
+        }
+        if (rc != PKV_OK) {
+            t_launches = launches;
+            return fail(rc, "layer %d: %s", l, std::string(t_last_error).c_str());
+        }
+    }
+    t_launches = launches;
+    return PKV_OK;
+}
+
 }  // extern "C"
 
 // ---------------------------------------------------------------------------

@@ -262,15 +262,34 @@ def make_workload(spec: Spec, layout: Optional[Layout] = None, seed_offset: int 
 
 
 def make_step(spec_s: Spec = C5_SLIDING, spec_g: Spec = C5_GLOBAL,
-              pattern=C5_LAYERS) -> List[Workload]:
+              pattern=C5_LAYERS, share_history: bool = False) -> List[Workload]:
     """A continuous-batching step: one layout shared by all layers, one
-    workload per layer (sliding or global spec by the pattern)."""
+    workload per layer (sliding or global spec by the pattern).  Each layer
+    draws its own query and new token.  With ``share_history`` the layers of
+    one kind reuse the first such layer's history values (the same arrays,
+    appended into each layer's own pool), which keeps full-size six-layer
+    steps affordable on the host."""
     rng = np.random.default_rng(spec_s.seed)
     layout = make_layout(spec_s, rng)
     out = []
+    first = {}
     for i, kind in enumerate(pattern):
         spec = spec_s if kind == "S" else spec_g
-        out.append(make_workload(spec, layout, seed_offset=i))
+        if not share_history or kind not in first:
+            w = make_workload(spec, layout, seed_offset=i)
+            first.setdefault(kind, w)
+        else:
+            w0 = first[kind]
+            vrng = np.random.default_rng(spec.seed * 1000 + 17 + i)
+            B, Hq, Hkv, D = spec.batch, spec.num_q_heads, spec.num_kv_heads, spec.head_dim
+            sigma = None
+            if spec.kv == "int8_head":
+                sigma = (0.5 + 0.25 * np.arange(Hkv, dtype=np.float32))[None, :, None]
+            q = _normal_bf16(vrng, (B, Hq, D), replace(spec, outlier_frac=0.0))
+            nk = _normal_bf16(vrng, (B, Hkv, D), spec, sigma)
+            nv = None if spec.alias else _normal_bf16(vrng, (B, Hkv, D), spec, sigma)
+            w = replace(w0, q=q, new_k=nk, new_v=nv)
+        out.append(w)
     return out
 
 
