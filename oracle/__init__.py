@@ -41,6 +41,7 @@ class _COraclePool(ctypes.Structure):
         ("head_dim", ctypes.c_int32),
         ("is_int8", ctypes.c_int32),
         ("scale_mode", ctypes.c_int32),
+        ("ring_blocks", ctypes.c_int32),
     ]
 
 
@@ -62,6 +63,8 @@ def _load():
         lib.oracle_partial.restype = ctypes.c_int
         lib.oracle_lse_combine.argtypes = [p, p, i32, i32, p, p]
         lib.oracle_lse_combine.restype = None
+        lib.oracle_slot_mapping.argtypes = [p, p, i32, p, p, i64, p]
+        lib.oracle_slot_mapping.restype = None
         lib.oracle_max_threads.argtypes = []
         lib.oracle_max_threads.restype = ctypes.c_int
         _lib = lib
@@ -91,6 +94,7 @@ class OraclePool:
     k_scale: Optional[np.ndarray] = None
     v_scale: Optional[np.ndarray] = None
     scale_mode: int = SCALE_NONE
+    ring_blocks: int = 0  # 0: paged; > 0: each sequence's ring of this many blocks
 
     @property
     def is_int8(self) -> bool:
@@ -105,7 +109,8 @@ class OraclePool:
             if s is not None:
                 assert s.dtype == np.float32
         return _COraclePool(_ptr(self.k), _ptr(self.v), _ptr(self.k_scale), _ptr(self.v_scale),
-                            nb, p, hkv, d, int(self.is_int8), int(self.scale_mode))
+                            nb, p, hkv, d, int(self.is_int8), int(self.scale_mode),
+                            int(self.ring_blocks))
 
 
 def bf16_bits_to_f64(bits: np.ndarray) -> np.ndarray:
@@ -123,6 +128,21 @@ def quantize(x_bits: np.ndarray, scale: float) -> np.ndarray:
     q = np.empty(x_bits.shape, np.int8)
     _load().oracle_quantize(_ptr(x_bits), x_bits.size, ctypes.c_float(scale), _ptr(q))
     return q
+
+
+def slot_mapping(pool: OraclePool, block_table: np.ndarray, seq: np.ndarray,
+                 pos: np.ndarray) -> np.ndarray:
+    """Slot ids of tokens (sequence seq[i], absolute position pos[i]) under the
+    pool's layout: paged, or the ring (position t in slot t mod W of the
+    sequence's ring of W = ring_blocks * block_size slots); -1 for a negative
+    position or an unallocated table entry."""
+    bt = np.ascontiguousarray(block_table, dtype=np.int32)
+    seq = np.ascontiguousarray(seq, dtype=np.int32)
+    pos = np.ascontiguousarray(pos, dtype=np.int64)
+    out = np.empty(len(pos), np.int64)
+    _load().oracle_slot_mapping(ctypes.byref(pool._c()), _ptr(bt), bt.shape[1], _ptr(seq),
+                                _ptr(pos), len(pos), _ptr(out))
+    return out
 
 
 def append(k_bits: np.ndarray, v_bits: Optional[np.ndarray], slot_mapping: np.ndarray,

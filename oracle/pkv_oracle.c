@@ -56,6 +56,8 @@ typedef struct {
     int32_t head_dim;
     int32_t is_int8;    /* 0: bf16 elements, 1: int8 elements */
     int32_t scale_mode; /* 0: none, 1: per token, 2: per kv head */
+    int32_t ring_blocks; /* 0: paged (the table lists every logical block);
+                          * > 0: ring of ring_blocks blocks per sequence */
 } oracle_pool;
 
 enum { OR_OK = 0, OR_E_ARG = -1, OR_E_BLOCK = -2, OR_E_SLOT = -3 };
@@ -187,17 +189,54 @@ static int mask_allows(int64_t j, int64_t pos, int32_t window)
     return 1;
 }
 
-/* Physical block of logical key j of sequence b, or -1 if out of range. */
-static int64_t phys_block(const oracle_pool *pool, const int32_t *block_table,
-                          int32_t max_blocks_per_seq, int32_t b, int64_t j)
+/* Table entry and offset of the slot that holds position j of a sequence.
+ * Paged ([Lab5] Paged Attention): entry j / P, offset j % P.
+ * Ring ([Lab5] Ring KV Cache: the KV of absolute position t lives in slot
+ * t mod W of a fixed ring of W slots): slot r = j mod W with
+ * W = ring_blocks * P, i.e. entry r / P, offset r % P. */
+static void slot_of_position(const oracle_pool *pool, int64_t j, int64_t *entry, int64_t *off)
 {
-    int64_t lb = j / pool->block_size;
+    const int64_t P = pool->block_size;
+    if (pool->ring_blocks > 0) {
+        const int64_t W = (int64_t)pool->ring_blocks * P;
+        const int64_t r = j % W;
+        *entry = r / P;
+        *off = r % P;
+    } else {
+        *entry = j / P;
+        *off = j % P;
+    }
+}
+
+/* Physical block of logical key j of sequence b (its offset in *off), or -1
+ * if out of range. */
+static int64_t phys_block(const oracle_pool *pool, const int32_t *block_table,
+                          int32_t max_blocks_per_seq, int32_t b, int64_t j, int64_t *off)
+{
+    int64_t lb;
+    slot_of_position(pool, j, &lb, off);
     if (lb >= max_blocks_per_seq)
         return -1;
     int32_t p = block_table[(int64_t)b * max_blocks_per_seq + lb];
     if (p < 0 || p >= pool->num_blocks)
         return -1;
     return p;
+}
+
+/* Slot ids of n tokens (sequence seq[i], absolute position pos[i]) under
+ * the pool's layout: block_table[seq][entry] * P + offset, or -1 for a
+ * negative position or a table entry that names no block of the pool. */
+void oracle_slot_mapping(const oracle_pool *pool, const int32_t *block_table,
+                         int32_t max_blocks_per_seq, const int32_t *seq, const int64_t *pos,
+                         int64_t n, int64_t *out)
+{
+    for (int64_t i = 0; i < n; ++i) {
+        int64_t off;
+        int64_t p = pos[i] < 0 ? -1
+                               : phys_block(pool, block_table, max_blocks_per_seq, seq[i], pos[i],
+                                            &off);
+        out[i] = p < 0 ? -1 : p * pool->block_size + off;
+    }
 }
 
 /* One output row (sequence b, query head h) of masked softmax attention over
@@ -243,15 +282,15 @@ static int attend_row(const uint16_t *q, const oracle_pool *pool, const int32_t 
         s[i] = -INFINITY; /* M_j = -inf outside the mask */
         if (!mask_allows(j, pos, window))
             continue;
-        int64_t p = phys_block(pool, block_table, max_blocks_per_seq, b, j);
+        int64_t off;
+        int64_t p = phys_block(pool, block_table, max_blocks_per_seq, b, j, &off);
         if (p < 0) {
             rc = OR_E_BLOCK;
             break;
         }
         double acc = 0.0;
         for (int32_t d = 0; d < D; ++d)
-            acc += (double)bf16_bits_to_float(qrow[d]) *
-                   kv_value(pool, 0, p, j % pool->block_size, g, d);
+            acc += (double)bf16_bits_to_float(qrow[d]) * kv_value(pool, 0, p, off, g, d);
         s[i] = softmax_scale * acc;
         if (s[i] > m)
             m = s[i];
@@ -262,11 +301,12 @@ static int attend_row(const uint16_t *q, const oracle_pool *pool, const int32_t 
             if (s[i] == -INFINITY)
                 continue;
             int64_t j = key_begin + i;
-            int64_t p = phys_block(pool, block_table, max_blocks_per_seq, b, j);
+            int64_t off;
+            int64_t p = phys_block(pool, block_table, max_blocks_per_seq, b, j, &off);
             double e = exp(s[i] - m);
             z += e;
             for (int32_t d = 0; d < D; ++d)
-                o[d] += e * kv_value(pool, 1, p, j % pool->block_size, g, d);
+                o[d] += e * kv_value(pool, 1, p, off, g, d);
         }
         for (int32_t d = 0; d < D; ++d)
             o[d] /= z;
@@ -282,6 +322,8 @@ static int check_shapes(const oracle_pool *pool, int32_t num_q_heads)
         num_q_heads <= 0 || num_q_heads % pool->num_kv_heads != 0)
         return OR_E_ARG;
     if (pool->is_int8 && pool->scale_mode == 0)
+        return OR_E_ARG;
+    if (pool->ring_blocks < 0)
         return OR_E_ARG;
     return OR_OK;
 }

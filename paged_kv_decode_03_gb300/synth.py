@@ -71,6 +71,10 @@ class Spec:
     shared_min_len: int = 0
     split_tokens: int = 0
     seed: int = 1234
+    # 0: paged layout (the block table lists every logical block); > 0: ring
+    # layout of a sliding layer, each sequence owning a ring of this many
+    # blocks (only the blocks its length reaches are allocated)
+    ring_blocks: int = 0
 
     @property
     def softmax_scale(self) -> float:
@@ -97,7 +101,19 @@ C5_SLIDING = Spec("c5_step_sliding", batch=256, num_q_heads=16, num_kv_heads=8, 
 C5_GLOBAL = replace(C5_SLIDING, name="c5_step_global", num_kv_heads=1, window=0, kv="bf16")
 C5_LAYERS = ("S", "S", "S", "S", "S", "G")
 
-CONFIGS = {"c1": C1, "c2": C2, "c3": C3, "c4": C4, "c5s": C5_SLIDING, "c5g": C5_GLOBAL}
+# Ring-KV variants of the sliding layers (Lab5-Gemma4, Ring KV Cache): each
+# sequence's keys live in a ring of W = ring_blocks * 16 slots, W >= w + 1 so
+# that the inclusive window [pos - w, pos] fits.
+def ring_blocks_for(window: int, block_size: int = 16) -> int:
+    return -(-(window + 1) // block_size)
+
+
+C2_RING = replace(C2, name="c2_gemma4_sliding_ring", ring_blocks=ring_blocks_for(C2.window))
+C5_SLIDING_RING = replace(C5_SLIDING, name="c5_step_sliding_ring", shared_prefix_blocks=0,
+                          shared_prefix_seqs=0, ring_blocks=ring_blocks_for(C5_SLIDING.window))
+
+CONFIGS = {"c1": C1, "c2": C2, "c3": C3, "c4": C4, "c5s": C5_SLIDING, "c5g": C5_GLOBAL,
+           "c2r": C2_RING, "c5sr": C5_SLIDING_RING}
 
 
 @dataclass
@@ -120,9 +136,11 @@ class Workload:
     hist_slots: np.ndarray               # [T] int64
     new_k: np.ndarray                    # [B, H_kv, D] uint16, the step's token (position len-1)
     new_v: Optional[np.ndarray]
-    new_slots: np.ndarray                # [B] int64
+    new_slots: Optional[np.ndarray]      # [B] int64 (paged layouts; None for rings)
     k_head_scale: Optional[np.ndarray] = None   # [H_kv] fp32 (int8_head only)
     v_head_scale: Optional[np.ndarray] = None
+    hist_seq: Optional[np.ndarray] = None       # [T] int32 sequence of each history token
+    hist_pos: Optional[np.ndarray] = None       # [T] int64 its absolute position
 
     @property
     def seq_lens(self):
@@ -162,12 +180,16 @@ def make_layout(spec: Spec, rng: np.random.Generator) -> Layout:
         pick = rng.permutation(cand)[: spec.shared_prefix_seqs]
         shared[pick] = True
     nshared = spec.shared_prefix_blocks if shared.any() else 0
+    if spec.ring_blocks:
+        # a ring holds at most ring_blocks blocks per sequence
+        assert not nshared, "ring layouts share no prefix blocks"
+        nblk = np.minimum(nblk, spec.ring_blocks)
     # logical blocks that need a private physical block
     private = int(nblk.sum() - nshared * (shared.sum() - 1)) if nshared else int(nblk.sum())
     num_blocks = spec.pool_blocks or max(1, int(math.ceil(private * spec.pool_factor)))
     assert num_blocks >= private
     perm = rng.permutation(num_blocks).astype(np.int32)
-    maxb = max(1, int(nblk.max()))
+    maxb = spec.ring_blocks or max(1, int(nblk.max()))
     bt = np.full((B, maxb), -1, np.int32)
     owner = np.zeros(num_blocks, bool)
     nxt = 0
@@ -249,16 +271,19 @@ def make_workload(spec: Spec, layout: Optional[Layout] = None, seed_offset: int 
         v_hs = (np.float32(3.0) * sig / np.float32(127.0)).astype(np.float32)
     q = _normal_bf16(vrng, (B, Hq, D), replace(spec, outlier_frac=0.0))
     seq, pos = history_positions(spec, layout)
-    hist_slots = slot_of(layout, P, seq, pos)
+    # paged layouts carry their slot ids; for a ring the caller maps
+    # (sequence, position) to a slot with its own address map
+    hist_slots = None if spec.ring_blocks else slot_of(layout, P, seq, pos)
     hist_k = _normal_bf16(vrng, (len(seq), Hkv, D), spec, sigma)
     hist_v = None if spec.alias else _normal_bf16(vrng, (len(seq), Hkv, D), spec, sigma)
     last = layout.seq_lens.astype(np.int64) - 1
     bidx = np.arange(B, dtype=np.int64)
-    new_slots = np.where(last >= 0, slot_of(layout, P, bidx, np.maximum(last, 0)), -1)
+    new_slots = (None if spec.ring_blocks else
+                 np.where(last >= 0, slot_of(layout, P, bidx, np.maximum(last, 0)), -1))
     new_k = _normal_bf16(vrng, (B, Hkv, D), spec, sigma)
     new_v = None if spec.alias else _normal_bf16(vrng, (B, Hkv, D), spec, sigma)
     return Workload(spec, layout, q, hist_k, hist_v, hist_slots, new_k, new_v, new_slots,
-                    k_hs, v_hs)
+                    k_hs, v_hs, seq.astype(np.int32), pos)
 
 
 def make_step(spec_s: Spec = C5_SLIDING, spec_g: Spec = C5_GLOBAL,
