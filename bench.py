@@ -231,14 +231,22 @@ def device_pool(spec, w, dev, hist=True):
         mode = pkv.SCALE_PER_HEAD
         ks = _dnum(w.k_head_scale, dev)
         vs = None if spec.alias else _dnum(w.v_head_scale, dev)
-    pool = pkv.PagedKVPool(k=k_pool, v=v_pool, k_scale=ks, v_scale=vs, scale_mode=mode)
+    pool = pkv.PagedKVPool(k=k_pool, v=v_pool, k_scale=ks, v_scale=vs, scale_mode=mode,
+                           ring_blocks=spec.ring_blocks)
     if hist:
-        T = len(w.hist_slots)
+        T = len(w.hist_pos)
+        bt = _dnum(w.block_table, dev)
         for s in range(0, T, 1 << 16):
             e = min(T, s + (1 << 16))
+            if w.hist_slots is not None:
+                slots = _dnum(w.hist_slots[s:e], dev)
+            else:  # ring layout: the library's own address map
+                slots = torch.empty(e - s, dtype=torch.int64, device=dev)
+                pkv.paged_kv_slot_mapping(pool, bt, _dnum(w.hist_pos[s:e], dev), slots,
+                                          seq_ids=_dnum(w.hist_seq[s:e], dev))
             pkv.paged_kv_append(_dbits(w.hist_k[s:e], dev),
                                 None if w.hist_v is None else _dbits(w.hist_v[s:e], dev),
-                                _dnum(w.hist_slots[s:e], dev), pool)
+                                slots, pool)
     return pool
 
 
@@ -276,7 +284,12 @@ class LayerRun:
         self.sl = _dnum(w.seq_lens, dev)
         self.k_new = _dbits(w.new_k, dev)
         self.v_new = None if w.new_v is None else _dbits(w.new_v, dev)
-        self.slots = _dnum(w.new_slots, dev)
+        # ring layouts: the step maps each new token's position (seq_lens - 1)
+        # to its ring slot on the device before appending it
+        self.ring = spec.ring_blocks > 0
+        self.positions = _dnum(w.seq_lens.astype(np.int64) - 1, dev) if self.ring else None
+        self.slots = (torch.empty(B, dtype=torch.int64, device=dev) if self.ring
+                      else _dnum(w.new_slots, dev))
         self.out = torch.empty((B, Hq, D), dtype=torch.bfloat16, device=dev)
         self.max_len = int(w.seq_lens.max())
         self.scale = float(np.float32(spec.softmax_scale))
@@ -297,13 +310,15 @@ class LayerRun:
         self.tc = pkv.uses_tensor_cores(self.pool, Hq)
         dbytes = bytes_model.decode_bytes(spec, w.seq_lens, w.block_table)
         self.dbytes = dbytes
-        self.abytes = bytes_model.append_bytes(spec, int((w.new_slots >= 0).sum()))
+        self.abytes = bytes_model.append_bytes(spec, int((w.seq_lens > 0).sum()))
         self.step_bytes = dbytes["kv"] + dbytes["q"] + dbytes["out"] + self.abytes
         self.decode_kernel_bytes = dbytes["kv"] + dbytes["q"] + (dbytes["out"] if not self.split_api else 0)
         self.graphs = None
 
     def append(self):
         import paged_kv_decode_03_gb300 as pkv
+        if self.ring:
+            pkv.paged_kv_slot_mapping(self.pool, self.bt, self.positions, self.slots)
         pkv.paged_kv_append(self.k_new, self.v_new, self.slots, self.pool)
 
     def decode(self):
@@ -331,7 +346,15 @@ class LayerRun:
     def launches_per_step(self):
         import paged_kv_decode_03_gb300 as pkv
         n = 0
-        for part in ([self.append, self.decode] + ([self.combine] if self.split_api else [])):
+        if self.ring:
+            pkv.paged_kv_slot_mapping(self.pool, self.bt, self.positions, self.slots)
+            n += pkv.last_launch_count()
+            pkv.paged_kv_append(self.k_new, self.v_new, self.slots, self.pool)
+            n += pkv.last_launch_count()
+        else:
+            self.append()
+            n += pkv.last_launch_count()
+        for part in ([self.decode] + ([self.combine] if self.split_api else [])):
             part()
             n += pkv.last_launch_count()
         return n
@@ -572,7 +595,7 @@ def oracle_full_run(spec, w, layers=None):
             pool = pools[id(lw.hist_k)]
             s = lw.spec
             t0 = time.perf_counter()
-            oracle.append(lw.new_k, lw.new_v, lw.new_slots, pool)
+            oracle.append(lw.new_k, lw.new_v, oracle_new_slots(lw, pool), pool)
             oracle.decode(lw.q, pool, lw.block_table, lw.seq_lens, s.num_q_heads, s.window,
                           np.float32(s.softmax_scale), num_threads=nt)
             t += time.perf_counter() - t0
@@ -726,7 +749,7 @@ def per_config(args, dev, main_entry, main_spec, main_w):
     out["c2"] = main_entry
     if cpu:
         out["c2"]["oracle"] = oracle_full_run(main_spec, main_w)
-    for name in ("c1", "c3", "c4", "c5s", "c5g"):
+    for name in ("c1", "c3", "c4", "c5s", "c5g", "c2r", "c5sr"):
         spec = synth.CONFIGS[name]
         w = synth.make_workload(spec)
         req = spec.split_tokens or pkv.SPLIT_AUTO
@@ -763,10 +786,23 @@ def oracle_setup(spec, w):
     if spec.kv == "int8_head":
         ks = w.k_head_scale.copy()
         vs = None if spec.alias else w.v_head_scale.copy()
-    pool = oracle.OraclePool(k=k, v=v, k_scale=ks, v_scale=vs, scale_mode=mode)
-    if len(w.hist_slots):
-        oracle.append(w.hist_k, w.hist_v, w.hist_slots, pool)
+    pool = oracle.OraclePool(k=k, v=v, k_scale=ks, v_scale=vs, scale_mode=mode,
+                             ring_blocks=spec.ring_blocks)
+    hist = (w.hist_slots if w.hist_slots is not None
+            else oracle.slot_mapping(pool, w.block_table, w.hist_seq, w.hist_pos))
+    if len(hist):
+        oracle.append(w.hist_k, w.hist_v, hist, pool)
     return pool
+
+
+def oracle_new_slots(w, pool):
+    """The step's new-token slots (the oracle's own address map for rings)."""
+    import oracle
+    if w.new_slots is not None:
+        return w.new_slots
+    B = len(w.seq_lens)
+    return oracle.slot_mapping(pool, w.block_table, np.arange(B, dtype=np.int32),
+                               w.seq_lens.astype(np.int64) - 1)
 
 
 def cpu_baseline(spec, w, step_bytes, budget_s):
@@ -779,7 +815,7 @@ def cpu_baseline(spec, w, step_bytes, budget_s):
     reps, t = 0, 0.0
     while reps == 0 or t < budget_s:
         t0 = time.perf_counter()
-        oracle.append(w.new_k, w.new_v, w.new_slots, pool)
+        oracle.append(w.new_k, w.new_v, oracle_new_slots(w, pool), pool)
         oracle.decode(w.q, pool, w.block_table, w.seq_lens, spec.num_q_heads, spec.window,
                       np.float32(spec.softmax_scale))
         t += time.perf_counter() - t0
@@ -821,7 +857,8 @@ def run_reference(args, rank):
     def sample_step(nseq):
         idx = np.sort(order[:nseq])
         rows = np.array([(b, h) for b in idx for h in range(Hq)], np.int32)
-        oracle.append(w.new_k[idx], None if w.new_v is None else w.new_v[idx], w.new_slots[idx], pool)
+        oracle.append(w.new_k[idx], None if w.new_v is None else w.new_v[idx],
+                      oracle_new_slots(w, pool)[idx], pool)
         oracle.decode(w.q, pool, w.block_table, w.seq_lens, Hq, spec.window,
                       np.float32(spec.softmax_scale), rows=rows)
         return idx

@@ -99,6 +99,15 @@ extern "C" {
  *          PKV_SCALE_PER_HEAD:  [num_kv_heads], set by the caller (static).
  *          Unused (may be NULL) for bf16 pools; v_scale unused when K == V.
  *   block_size must be 16; head_dim must be 64, 128 or 256.
+ *   ring_blocks: 0 = paged layout: row b of a block table lists the
+ *          sequence's blocks in logical order (entry j holds positions
+ *          [16j, 16j+16)).  > 0 = ring layout of a sliding-window layer
+ *          (Lab5-Gemma4, Ring KV Cache: position t in slot t mod W of a fixed
+ *          ring, W = ring_blocks * block_size): row b lists the sequence's
+ *          ring, and position t lives in entry (t mod W) / 16 at offset
+ *          t mod 16, overwriting a position W earlier.  A decode with window
+ *          w over a ring needs W >= w + 1 (the w + 1 keys of [pos-w, pos]);
+ *          a sequence uses min(len, W) slots whatever its length.
  */
 typedef struct pkv_pool {
     void *k;
@@ -111,6 +120,7 @@ typedef struct pkv_pool {
     int32_t head_dim;
     int32_t dtype;      /* PKV_BF16 | PKV_INT8 */
     int32_t scale_mode; /* PKV_SCALE_* (PKV_SCALE_NONE only for bf16) */
+    int32_t ring_blocks; /* 0 = paged; > 0 = ring of this many blocks per sequence */
 } pkv_pool;
 
 /*
@@ -136,6 +146,26 @@ typedef struct pkv_pool {
  */
 PKV_API int paged_kv_append(const void *k, const void *v, const int64_t *slot_mapping,
                             int32_t num_tokens, const pkv_pool *pool, void *stream);
+
+/*
+ * paged_kv_slot_mapping -- slot ids of num_tokens new tokens under the
+ * pool's layout, computed on the device (so that a captured step needs only
+ * positions, not host-computed slots): token i of sequence seq_ids[i] (or i
+ * when seq_ids is NULL) at absolute position positions[i] goes to
+ *   paged (ring_blocks 0):  block_table[seq][pos / 16] * 16 + pos % 16
+ *   ring:                   block_table[seq][(pos mod W) / 16] * 16 + pos % 16
+ * (Lab5-Gemma4, Paged Attention and Ring KV Cache sections).  A negative
+ * position gives slot -1 (padding, which paged_kv_append skips); a table
+ * entry past max_blocks_per_seq or outside [0, num_blocks) gives -1 and sets
+ * PKV_DEV_BAD_BLOCK.
+ *   block_table: [batch][max_blocks_per_seq] int32; seq_ids: [num_tokens]
+ *   int32 or NULL; positions: [num_tokens] int64; slot_mapping (output):
+ *   [num_tokens] int64, 8-byte aligned.  All device pointers.
+ */
+PKV_API int paged_kv_slot_mapping(const pkv_pool *pool, const int32_t *block_table,
+                                  int32_t max_blocks_per_seq, const int32_t *seq_ids,
+                                  const int64_t *positions, int32_t num_tokens,
+                                  int64_t *slot_mapping, void *stream);
 
 /*
  * paged_decode_split_tokens -- the split length paged_decode_attention uses
@@ -197,7 +227,9 @@ PKV_API size_t paged_decode_partial_workspace_bytes(int32_t batch, int32_t num_q
  * section): scores are never written to memory.  Blocks outside [lo, pos]
  * are never read.
  *   q:            [batch][num_q_heads][head_dim] bf16, 16-byte aligned.
- *   block_table:  [batch][max_blocks_per_seq] int32.
+ *   block_table:  [batch][max_blocks_per_seq] int32 (for a ring pool, each
+ *                 row is the sequence's ring; max_blocks_per_seq >=
+ *                 ring_blocks, and lengths are not bounded by the table).
  *   seq_lens:     [batch] int32, length including the token appended this
  *                 step; 0 gives a zero output row.
  *   max_seq_len:  host upper bound on every seq_lens[b] (tiniestgpt notes,

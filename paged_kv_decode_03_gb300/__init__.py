@@ -10,7 +10,7 @@ CPU fallback: if the library is missing, the first call raises.
 """
 from .binding import (  # noqa: F401
     PKV_BF16, PKV_INT8, SCALE_NONE, SCALE_PER_TOKEN, SCALE_PER_HEAD, SPLIT_AUTO, OUT_BF16, OUT_F32,
-    PagedKVPool, paged_kv_append, paged_decode_attention, paged_decode_split_partial,
+    PagedKVPool, paged_kv_append, paged_kv_slot_mapping, paged_decode_attention, paged_decode_split_partial,
     paged_decode_lse_combine, paged_decode_workspace_bytes, paged_decode_num_splits,
     paged_decode_split_tokens, PagedKVError, paged_decode_attention_noalloc,
     paged_decode_partial_workspace_bytes, uses_tensor_cores, last_launch_count,

@@ -39,6 +39,7 @@ class PkvPoolC(ctypes.Structure):
         ("head_dim", ctypes.c_int32),
         ("dtype", ctypes.c_int32),
         ("scale_mode", ctypes.c_int32),
+        ("ring_blocks", ctypes.c_int32),
     ]
 
 
@@ -91,6 +92,8 @@ def load_library():
     lib.paged_decode_attention_noalloc.argtypes = [p, p, p, i32, p, i32, i32, i32, i32, f32,
                                                    i32, p, i32, p]
     lib.paged_decode_attention_noalloc.restype = ctypes.c_int
+    lib.paged_kv_slot_mapping.argtypes = [p, p, i32, p, p, i32, p, p]
+    lib.paged_kv_slot_mapping.restype = ctypes.c_int
     lib.paged_decode_step_workspace_bytes.argtypes = [p, i32, i32, i32, i32, i32]
     lib.paged_decode_step_workspace_bytes.restype = sz
     lib.paged_decode_step.argtypes = [p, i32, p, p, i32, p, i32, i32, i32, i32, p, sz, i32, p]
@@ -151,12 +154,16 @@ class PagedKVPool:
     k, v: [num_blocks, block_size, num_kv_heads, head_dim], bf16 or int8;
     v None means K and V are one tensor.  int8 pools carry fp32 scale tables
     (per token: [num_blocks * block_size]; per head: [num_kv_heads]).
+    ring_blocks: 0 for the paged layout; > 0 for a sliding layer's ring
+    layout (each block-table row is the sequence's ring of that many blocks,
+    position t in slot t mod (ring_blocks * block_size)).
     """
     k: "object"
     v: Optional[object] = None
     k_scale: Optional[object] = None
     v_scale: Optional[object] = None
     scale_mode: int = SCALE_NONE
+    ring_blocks: int = 0
 
     @property
     def dtype(self) -> int:
@@ -193,7 +200,7 @@ class PagedKVPool:
         return PkvPoolC(_dev_ptr(self.k, "pool.k"), _dev_ptr(self.v, "pool.v"),
                         _dev_ptr(self.k_scale, "pool.k_scale"), _dev_ptr(self.v_scale, "pool.v_scale"),
                         self.num_blocks, self.block_size, self.num_kv_heads, self.head_dim,
-                        self.dtype, int(self.scale_mode))
+                        self.dtype, int(self.scale_mode), int(self.ring_blocks))
 
 
 def paged_kv_append(k, v, slot_mapping, pool: PagedKVPool, stream=None) -> None:
@@ -204,6 +211,22 @@ def paged_kv_append(k, v, slot_mapping, pool: PagedKVPool, stream=None) -> None:
     n = int(slot_mapping.shape[0])
     _check(lib.paged_kv_append(_dev_ptr(k, "k"), _dev_ptr(v, "v"), _dev_ptr(slot_mapping, "slot_mapping"),
                                n, ctypes.byref(pc), _stream(stream)), "paged_kv_append")
+
+
+def paged_kv_slot_mapping(pool: PagedKVPool, block_table, positions, slot_mapping,
+                          seq_ids=None, stream=None):
+    """Slots ([T] int64, written into ``slot_mapping``) of tokens at absolute
+    ``positions`` ([T] int64) of sequences ``seq_ids`` ([T] int32; None =
+    token i of sequence i) under the pool's layout (paged, or the ring
+    t mod W), computed on the device."""
+    lib = load_library()
+    pc = pool.c_struct()
+    _check(lib.paged_kv_slot_mapping(ctypes.byref(pc), _dev_ptr(block_table, "block_table"),
+                                     int(block_table.shape[1]), _dev_ptr(seq_ids, "seq_ids"),
+                                     _dev_ptr(positions, "positions"), int(positions.shape[0]),
+                                     _dev_ptr(slot_mapping, "slot_mapping"), _stream(stream)),
+           "paged_kv_slot_mapping")
+    return slot_mapping
 
 
 def paged_decode_split_tokens(batch, num_q_heads, num_kv_heads, max_seq_len, window,

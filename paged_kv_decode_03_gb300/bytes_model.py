@@ -33,8 +33,10 @@ def bytes_per_key(num_kv_heads: int, head_dim: int, kv: str, alias: bool) -> int
     return b
 
 
-def window_slots(seq_lens: np.ndarray, block_table: np.ndarray, window: int, P: int = 16):
-    """Physical slot ids of every key a decode reads (keys [lo, pos])."""
+def window_slots(seq_lens: np.ndarray, block_table: np.ndarray, window: int, P: int = 16,
+                 ring_blocks: int = 0):
+    """Physical slot ids of every key a decode reads (keys [lo, pos]); for a
+    ring layout key j sits in table entry (j mod W) / P, W = ring_blocks * P."""
     out = []
     for b, L in enumerate(np.asarray(seq_lens, np.int64)):
         if L <= 0:
@@ -42,13 +44,15 @@ def window_slots(seq_lens: np.ndarray, block_table: np.ndarray, window: int, P: 
         pos = L - 1
         lo = max(0, pos - window) if window > 0 else 0
         j = np.arange(lo, pos + 1, dtype=np.int64)
-        out.append(block_table[b, j // P].astype(np.int64) * P + j % P)
+        entry = (j % (ring_blocks * P)) // P if ring_blocks else j // P
+        out.append(block_table[b, entry].astype(np.int64) * P + j % P)
     return np.concatenate(out) if out else np.zeros(0, np.int64)
 
 
 def decode_bytes(spec, seq_lens, block_table, out_bytes_per_elem: int = 2) -> dict:
     """Algorithmic bytes of one decode of one layer."""
-    slots = window_slots(seq_lens, block_table, spec.window, spec.block_size)
+    slots = window_slots(seq_lens, block_table, spec.window, spec.block_size,
+                         getattr(spec, "ring_blocks", 0))
     uniq = int(np.unique(slots).size)
     kv = uniq * bytes_per_key(spec.num_kv_heads, spec.head_dim, spec.kv, spec.alias)
     if spec.kv == "int8_head":

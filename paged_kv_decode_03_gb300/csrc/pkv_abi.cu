@@ -192,6 +192,8 @@ static int check_pool(const pkv_pool *pool)
         return fail(PKV_E_SHAPE, "pool has more than 2^31 slots");
     if (pool->dtype != PKV_BF16 && pool->dtype != PKV_INT8)
         return fail(PKV_E_UNSUPPORTED, "dtype %d", pool->dtype);
+    if (pool->ring_blocks < 0)
+        return fail(PKV_E_ARG, "ring_blocks %d < 0", pool->ring_blocks);
     if (!aligned(pool->k, 16) || (pool->v && !aligned(pool->v, 16)))
         return fail(PKV_E_ALIGN, "pool k/v must be 16-byte aligned");
     const bool alias = pool->v == nullptr || pool->v == pool->k;
@@ -310,6 +312,38 @@ PKV_API int paged_kv_append(const void *k, const void *v, const int64_t *slot_ma
     return PKV_OK;
 }
 
+PKV_API int paged_kv_slot_mapping(const pkv_pool *pool, const int32_t *block_table,
+                                  int32_t max_blocks_per_seq, const int32_t *seq_ids,
+                                  const int64_t *positions, int32_t num_tokens,
+                                  int64_t *slot_mapping, void *stream)
+{
+    t_last_error.clear();
+    t_launches = 0;
+    if (int rc = check_pool(pool))
+        return rc;
+    if (num_tokens < 0 || max_blocks_per_seq <= 0)
+        return fail(PKV_E_ARG, "num_tokens < 0 or max_blocks_per_seq <= 0");
+    if (num_tokens == 0)
+        return PKV_OK;
+    if (!block_table || !positions || !slot_mapping)
+        return fail(PKV_E_NULL, "block_table, positions or slot_mapping is NULL");
+    if (!aligned(block_table, 4) || !aligned(positions, 8) || !aligned(slot_mapping, 8) ||
+        (seq_ids && !aligned(seq_ids, 4)))
+        return fail(PKV_E_ALIGN, "misaligned block_table, seq_ids, positions or slot_mapping");
+    if (pool->ring_blocks > max_blocks_per_seq)
+        return fail(PKV_E_SHAPE, "block table rows (%d) shorter than the ring (%d blocks)",
+                    max_blocks_per_seq, pool->ring_blocks);
+    unsigned int *err = error_word_ptr();
+    if (!err)
+        return fail(PKV_E_DRIVER, "cannot resolve the device error word");
+    cudaError_t e = launch_slot_mapping(block_table, max_blocks_per_seq, pool->ring_blocks,
+                                        pool->num_blocks, seq_ids, positions, num_tokens,
+                                        slot_mapping, err, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess)
+        return cuda_fail(e, "slot mapping launch");
+    return PKV_OK;
+}
+
 PKV_API int32_t paged_decode_num_splits(int32_t block_size, int32_t max_seq_len, int32_t window,
                                         int32_t split_tokens)
 {
@@ -396,8 +430,20 @@ static int check_decode_args(const void *q, const pkv_pool *pool, const int32_t 
         return fail(PKV_E_UNSUPPORTED, "batch > 65535");
     if (window < 0)
         return fail(PKV_E_ARG, "window < 0");
-    if ((int64_t)max_seq_len > (int64_t)max_blocks_per_seq * pool->block_size)
+    if (pool->ring_blocks > 0) {
+        // a ring holds the last W = ring_blocks * block_size positions: the
+        // inclusive window's w + 1 keys must fit
+        if (window == 0)
+            return fail(PKV_E_ARG, "a ring layout needs a sliding window (window > 0)");
+        if ((int64_t)pool->ring_blocks * pool->block_size < (int64_t)window + 1)
+            return fail(PKV_E_SHAPE, "ring of %d slots is shorter than the window's %d keys",
+                        pool->ring_blocks * pool->block_size, window + 1);
+        if (max_blocks_per_seq < pool->ring_blocks)
+            return fail(PKV_E_SHAPE, "block table rows (%d) shorter than the ring (%d blocks)",
+                        max_blocks_per_seq, pool->ring_blocks);
+    } else if ((int64_t)max_seq_len > (int64_t)max_blocks_per_seq * pool->block_size) {
         return fail(PKV_E_SHAPE, "max_seq_len exceeds max_blocks_per_seq * block_size");
+    }
     if (out_dtype != PKV_OUT_BF16 && out_dtype != PKV_OUT_F32)
         return fail(PKV_E_ARG, "out_dtype %d", out_dtype);
     if (!q || !block_table || !seq_lens || !out)
@@ -445,6 +491,7 @@ static int run_decode(const void *q, const pkv_pool *pool, const int32_t *block_
     p.part_o = part_o;
     p.out = out;
     p.max_blocks = max_blocks_per_seq;
+    p.ring_blocks = pool->ring_blocks;
     p.scale_mode = pool->scale_mode;
     p.batch = batch;
     p.num_q_heads = num_q_heads;

@@ -136,4 +136,43 @@ cudaError_t launch_append(const AppendParams &p, int int8, cudaStream_t s)
     return cudaGetLastError();
 }
 
+// Slot of each token under the pool's layout: entry pos / 16 of the
+// sequence's table row (paged) or entry (pos mod W) / 16 of its ring
+// (W = ring_blocks * 16), offset pos % 16; -1 for padding (negative
+// position) or a table entry that names no block of the pool (reported).
+__global__ void slot_mapping_kernel(const int32_t *block_table, int max_blocks, int ring_blocks,
+                                    int num_blocks, const int32_t *seq_ids,
+                                    const int64_t *positions, int num_tokens, int64_t *slots,
+                                    unsigned int *err)
+{
+    const int i = blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= num_tokens)
+        return;
+    const int64_t pos = positions[i];
+    int64_t slot = -1;
+    if (pos >= 0) {
+        const int64_t seq = seq_ids ? seq_ids[i] : i;
+        const int64_t r = ring_blocks > 0 ? pos % (static_cast<int64_t>(ring_blocks) * kBlock) : pos;
+        const int64_t entry = r / kBlock;
+        const int32_t phys = entry < max_blocks ? block_table[seq * max_blocks + entry] : -1;
+        if (phys >= 0 && phys < num_blocks)
+            slot = static_cast<int64_t>(phys) * kBlock + r % kBlock;
+        else
+            record_error(err, PKV_DEV_BAD_BLOCK);
+    }
+    slots[i] = slot;
+}
+
+cudaError_t launch_slot_mapping(const int32_t *block_table, int max_blocks, int ring_blocks,
+                                int num_blocks, const int32_t *seq_ids, const int64_t *positions,
+                                int num_tokens, int64_t *slots, unsigned int *err, cudaStream_t s)
+{
+    const int threads = 256;
+    slot_mapping_kernel<<<(num_tokens + threads - 1) / threads, threads, 0, s>>>(
+        block_table, max_blocks, ring_blocks, num_blocks, seq_ids, positions, num_tokens, slots,
+        err);
+    note_launch();
+    return cudaGetLastError();
+}
+
 }  // namespace pkv

@@ -33,6 +33,7 @@
 //   * Keys outside [lo, pos] in the first/last block are masked with a
 //     select (never arithmetic), so stale or NaN slots contribute nothing.
 #include <cuda_bf16.h>
+#include <limits.h>
 #include <math.h>
 
 #include <atomic>
@@ -219,7 +220,7 @@ __device__ __forceinline__ void decode_body(const DecodeParams &p, const CUtenso
     const int SB = alias ? KS : 2 * KS;  // one stage: K slot [+ V slot]
 
     const bool reporter = threadIdx.x == 0 && split == 0 && blockIdx.y == 0;
-    if (len > p.max_blocks * C::P) {
+    if (p.ring_blocks == 0 && len > p.max_blocks * C::P) {  // a ring does not bound the length
         if (reporter)
             record_error(p.err, PKV_DEV_LEN_TABLE);
         len = p.max_blocks * C::P;
@@ -262,7 +263,7 @@ __device__ __forceinline__ void decode_body(const DecodeParams &p, const CUtenso
             }
             const uint64_t pol = policy_evict_first();
             TableCursor tc;
-            tc.init(bt_row + ub0, n, lane);
+            tc.init(bt_row, ub0, n, p.ring_blocks, lane);
             int issued[2] = {0, 0};
             bool ok = true;
             int st = 0;             // ring slot of stage sidx
@@ -642,14 +643,14 @@ constexpr auto decode_entry()
 constexpr int ORDER_BINS = 4096;
 
 __global__ void __launch_bounds__(1024) seq_order_kernel(const int32_t *seq_lens, int batch,
-                                                         int window, int max_blocks,
+                                                         int window, int len_cap,
                                                          int2 *order)
 {
     __shared__ int hist[ORDER_BINS];
     __shared__ int wsum[32];
     pdl_launch_dependents();
     auto key = [&](int b) {
-        const int len = min(seq_lens[b], max_blocks * kBlock);
+        const int len = min(seq_lens[b], len_cap);
         const KeyRange kr = key_range(len, window, 0);
         return ORDER_BINS - 1 - min(kr.nblk, ORDER_BINS - 1);  // longest first
     };
@@ -817,7 +818,8 @@ static cudaError_t launch_one(const DecodeParams &p, const CUtensorMap &tmk,
         note_launch();
         return cudaGetLastError();
     }
-    seq_order_kernel<<<1, 1024, 0, s>>>(p.seq_lens, p.batch, p.window, p.max_blocks,
+    seq_order_kernel<<<1, 1024, 0, s>>>(p.seq_lens, p.batch, p.window,
+                                        p.ring_blocks ? INT_MAX : p.max_blocks * kBlock,
                                         reinterpret_cast<int2 *>(p.order_ws));
     note_launch();
     if ((e = cudaGetLastError()) != cudaSuccess)

@@ -242,7 +242,8 @@ __device__ __forceinline__ void item_geom(const DecodeParams &p, Item &it)
 {
     int len = p.seq_lens[it.b];
     const int cap = p.max_blocks * kBlock;
-    len = len > cap ? cap : len;
+    if (p.ring_blocks == 0)  // a ring does not bound the length
+        len = len > cap ? cap : len;
     it.pos = len - 1;
     it.lo = p.window > 0 ? max(0, it.pos - p.window) : 0;
     const int blk_lo = len > 0 ? it.lo / kBlock : 0;
@@ -324,7 +325,7 @@ __global__ void __launch_bounds__(1024) tc_plan_kernel(const DecodeParams p, int
         if (b < p.batch) {
             int len = p.seq_lens[b];
             const int cap = p.max_blocks * kBlock;
-            if (len > cap) {
+            if (p.ring_blocks == 0 && len > cap) {
                 record_error(p.err, PKV_DEV_LEN_TABLE);
                 len = cap;
             }
@@ -656,10 +657,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                     q_last = kq;
                 }
                 ++kq;
-                const int32_t *bt_row =
-                    p.block_table + static_cast<size_t>(it.b) * p.max_blocks + it.ub0 + lt0 * 8;
+                const int32_t *bt_row = p.block_table + static_cast<size_t>(it.b) * p.max_blocks;
                 TableCursor tc;
-                tc.init(bt_row, it.n - lt0 * 8, lane);
+                tc.init(bt_row, it.ub0 + lt0 * 8, it.n - lt0 * 8, p.ring_blocks, lane);
                 for (int i = lt0; i < lt1 && !stop; ++i) {
                     int row[8];
 #pragma unroll

@@ -456,26 +456,39 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16])
 
 namespace pkv {
 
-// Block-table entries of a unit, read 32 at a time by a whole warp: lane j
-// holds entry base + j of the current chunk, the next chunk is fetched half
-// a chunk ahead, and entry i is shuffled out, so no iteration waits on a
-// global load.
+// Block-table entries of logical blocks first, first+1, ... of one
+// sequence, read 32 at a time by a whole warp: lane j holds the entry of
+// block first + base + j of the current chunk, the next chunk is fetched
+// ahead, and entry i is shuffled out, so no iteration waits on a global
+// load.  With a ring of `ring` blocks, logical block x lives in table entry
+// x % ring (position t in slot t mod (ring * 16)); ring 0 is the paged
+// layout, entry x.
 struct TableCursor {
     const int32_t *row;
-    int n, cur, nxt;
-    __device__ __forceinline__ void init(const int32_t *r, int count, int lane)
+    int first, n, ring, cur, nxt;
+    __device__ __forceinline__ int load(int i) const
+    {
+        int x = first + i;
+        if (ring > 0)
+            x %= ring;
+        return __ldg(row + x);
+    }
+    __device__ __forceinline__ void init(const int32_t *r, int first_block, int count, int ring_blocks,
+                                         int lane)
     {
         row = r;
+        first = first_block;
         n = count;
-        cur = lane < n ? __ldg(row + lane) : -1;
-        nxt = 32 + lane < n ? __ldg(row + 32 + lane) : -1;
+        ring = ring_blocks;
+        cur = lane < n ? load(lane) : -1;
+        nxt = 32 + lane < n ? load(32 + lane) : -1;
     }
     // entry i (all lanes call with the same i, in increasing order)
     __device__ __forceinline__ int get(int i, int lane)
     {
         if ((i & 31) == 0 && i > 0) {
             cur = nxt;
-            nxt = i + 32 + lane < n ? __ldg(row + i + 32 + lane) : -1;
+            nxt = i + 32 + lane < n ? load(i + 32 + lane) : -1;
         }
         return __shfl_sync(FULL_MASK, cur, i & 31);
     }

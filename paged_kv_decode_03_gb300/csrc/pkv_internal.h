@@ -23,6 +23,7 @@ struct DecodeParams {
     float *part_o;            // [B][num_splits][H_q][D]
     void *out;                // [B][H_q][D]
     int32_t max_blocks;       // block_table row length
+    int32_t ring_blocks;      // 0: paged; > 0: logical block j lives in entry j % ring_blocks
     int32_t scale_mode;
     int32_t batch;
     int32_t num_q_heads;
@@ -108,6 +109,9 @@ cudaError_t launch_decode_tc(const DecodeParams &p, const CUtensorMap &tmk,
                              const CUtensorMap &tmv, const CUtensorMap &tmq, int head_dim,
                              cudaStream_t s);
 cudaError_t launch_append(const AppendParams &p, int int8, cudaStream_t s);
+cudaError_t launch_slot_mapping(const int32_t *block_table, int max_blocks, int ring_blocks,
+                                int num_blocks, const int32_t *seq_ids, const int64_t *positions,
+                                int num_tokens, int64_t *slots, unsigned int *err, cudaStream_t s);
 
 // Count one kernel launch of the current API call (pkv_last_launch_count).
 void note_launch();

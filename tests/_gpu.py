@@ -30,20 +30,44 @@ def device_pool(w: synth.Workload) -> pkv.PagedKVPool:
     conv = to_dev_bits if k.dtype == np.uint16 else to_dev
     return pkv.PagedKVPool(k=conv(k), v=None if v is None else conv(v),
                            k_scale=None if ks is None else to_dev(ks),
-                           v_scale=None if vs is None else to_dev(vs), scale_mode=mode)
+                           v_scale=None if vs is None else to_dev(vs), scale_mode=mode,
+                           ring_blocks=w.spec.ring_blocks)
+
+
+def library_slots(w: synth.Workload, pool: pkv.PagedKVPool, seq, pos) -> torch.Tensor:
+    """Slots of (sequence, position) pairs from the library's own address map
+    (paged_kv_slot_mapping), on the device."""
+    slots = torch.empty(len(pos), dtype=torch.int64, device="cuda")
+    if len(pos):
+        pkv.paged_kv_slot_mapping(pool, to_dev(w.block_table),
+                                  to_dev(np.asarray(pos, np.int64)), slots,
+                                  seq_ids=to_dev(np.asarray(seq, np.int32)))
+    return slots
+
+
+def new_token_slots(w: synth.Workload, pool: pkv.PagedKVPool) -> torch.Tensor:
+    """The step's new-token slots: the workload's (paged) or the library's
+    slot mapping at positions seq_lens - 1 (ring layouts)."""
+    if w.new_slots is not None:
+        return to_dev(w.new_slots)
+    B = len(w.seq_lens)
+    return library_slots(w, pool, np.arange(B, dtype=np.int32), w.seq_lens.astype(np.int64) - 1)
 
 
 def append_all(w: synth.Workload, pool: pkv.PagedKVPool, new: bool = True, chunk: int = 1 << 16):
-    """History then (optionally) the step's new tokens, through paged_kv_append."""
-    T = len(w.hist_slots)
+    """History then (optionally) the step's new tokens, through paged_kv_append
+    (ring layouts: at the slots the library's slot mapping gives)."""
+    T = len(w.hist_pos)
     for s in range(0, T, chunk):
         e = min(T, s + chunk)
+        slots = (to_dev(w.hist_slots[s:e]) if w.hist_slots is not None
+                 else library_slots(w, pool, w.hist_seq[s:e], w.hist_pos[s:e]))
         pkv.paged_kv_append(to_dev_bits(w.hist_k[s:e]),
                             None if w.hist_v is None else to_dev_bits(w.hist_v[s:e]),
-                            to_dev(w.hist_slots[s:e]), pool)
+                            slots, pool)
     if new:
         pkv.paged_kv_append(to_dev_bits(w.new_k), None if w.new_v is None else to_dev_bits(w.new_v),
-                            to_dev(w.new_slots), pool)
+                            new_token_slots(w, pool), pool)
 
 
 def pool_to_host(pool: pkv.PagedKVPool):

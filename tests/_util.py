@@ -27,12 +27,26 @@ def oracle_pool(w: synth.Workload, append_new: bool = True) -> oracle.OraclePool
     if spec.kv == "int8_head":
         ks = w.k_head_scale.copy()
         vs = None if spec.alias else w.v_head_scale.copy()
-    pool = oracle.OraclePool(k=k, v=v, k_scale=ks, v_scale=vs, scale_mode=mode)
-    if len(w.hist_slots):
-        oracle.append(w.hist_k, w.hist_v, w.hist_slots, pool)
+    pool = oracle.OraclePool(k=k, v=v, k_scale=ks, v_scale=vs, scale_mode=mode,
+                             ring_blocks=spec.ring_blocks)
+    hist_slots, new_slots = oracle_slots(w, pool)
+    if len(hist_slots):
+        oracle.append(w.hist_k, w.hist_v, hist_slots, pool)
     if append_new:
-        oracle.append(w.new_k, w.new_v, w.new_slots, pool)
+        oracle.append(w.new_k, w.new_v, new_slots, pool)
     return pool
+
+
+def oracle_slots(w: synth.Workload, pool: oracle.OraclePool):
+    """History and new-token slots: the workload's own for paged layouts, the
+    oracle's address map for rings (positions seq_lens - 1 for the step)."""
+    if w.hist_slots is not None:
+        return w.hist_slots, w.new_slots
+    B = len(w.seq_lens)
+    hist = oracle.slot_mapping(pool, w.block_table, w.hist_seq, w.hist_pos)
+    new = oracle.slot_mapping(pool, w.block_table, np.arange(B, dtype=np.int32),
+                              w.seq_lens.astype(np.int64) - 1)
+    return hist, new
 
 
 def oracle_decode(w: synth.Workload, pool: oracle.OraclePool, rows=None, num_threads=0):

@@ -82,6 +82,37 @@ def test_decode_argument_validation(lib, kw, code):
     assert _decode(lib, _pool(), **kw) == code
 
 
+@pytest.mark.parametrize("kw,code", [
+    (dict(ring=-1, window=32), E_ARG),
+    (dict(ring=3, window=0), E_ARG),        # a ring needs a sliding window
+    (dict(ring=3, window=48), E_SHAPE),     # 48 slots < the window's 49 keys
+    (dict(ring=4, window=48, max_blocks=3), E_SHAPE),  # table rows shorter than the ring
+])
+def test_ring_layout_validation(lib, kw, code):
+    """Ring layouts (position t in slot t mod W, W = ring_blocks * 16) are
+    checked on the host: W must hold the inclusive window's w + 1 keys."""
+    ring = kw.pop("ring")
+    assert _decode(lib, _pool(ring_blocks=ring), **kw) == code
+    assert lib.pkv_last_error().decode()
+
+
+def test_ring_lengths_are_not_bounded_by_the_table(lib):
+    """A ring of 4 blocks serves a length far beyond 4 * 16: the host check
+    passes (the call then needs a device; here it stops at the tensor map or
+    the error word, never at the shape check)."""
+    rc = _decode(lib, _pool(ring_blocks=4), max_blocks=4, max_len=5000, window=40)
+    assert rc not in (E_SHAPE, E_ARG, E_ALIGN, E_NULL), lib.pkv_last_error()
+
+
+def test_slot_mapping_validation(lib):
+    pool = _pool(ring_blocks=4)
+    f = lib.paged_kv_slot_mapping
+    assert f(ctypes.byref(pool), None, 4, None, FAKE, 8, FAKE, None) == E_NULL
+    assert f(ctypes.byref(pool), FAKE, 4, None, FAKE + 4, 8, FAKE, None) == E_ALIGN
+    assert f(ctypes.byref(pool), FAKE, 3, None, FAKE, 8, FAKE, None) == E_SHAPE
+    assert f(ctypes.byref(pool), FAKE, 4, None, FAKE, 0, FAKE, None) == 0
+
+
 def test_append_validation(lib):
     pool = _pool()
     assert lib.paged_kv_append(None, FAKE, FAKE, 4, ctypes.byref(pool), None) == E_NULL
