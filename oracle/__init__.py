@@ -63,6 +63,8 @@ def _load():
         lib.oracle_partial.restype = ctypes.c_int
         lib.oracle_lse_combine.argtypes = [p, p, i32, i32, p, p]
         lib.oracle_lse_combine.restype = None
+        lib.oracle_prefill.argtypes = [p, p, p, i32, p, p, i32, i32, i32, f64, p, i32]
+        lib.oracle_prefill.restype = ctypes.c_int
         lib.oracle_slot_mapping.argtypes = [p, p, i32, p, p, i64, p]
         lib.oracle_slot_mapping.restype = None
         lib.oracle_max_threads.argtypes = []
@@ -181,6 +183,26 @@ def decode(q_bits: np.ndarray, pool: OraclePool, block_table: np.ndarray, seq_le
                                _ptr(rows), n, _ptr(out), num_threads)
     if rc != 0:
         raise ValueError(f"oracle_decode failed ({rc})")
+    return out
+
+
+def prefill(q_bits: np.ndarray, pool: OraclePool, block_table: np.ndarray, seq_lens: np.ndarray,
+            q_start: np.ndarray, num_q_heads: int, window: int, softmax_scale: float,
+            num_threads: int = 0) -> np.ndarray:
+    """fp64 attention of each sequence's chunk of new tokens: q_bits
+    [total, H_q, D] (rows q_start[b] .. q_start[b+1]-1 are sequence b's last
+    tokens, causal among themselves).  Returns [total, H_q, D]."""
+    q_bits = np.ascontiguousarray(q_bits, dtype=np.uint16)
+    bt = np.ascontiguousarray(block_table, dtype=np.int32)
+    sl = np.ascontiguousarray(seq_lens, dtype=np.int32)
+    qs = np.ascontiguousarray(q_start, dtype=np.int32)
+    D = pool.k.shape[3]
+    out = np.zeros((q_bits.shape[0], num_q_heads, D), np.float64)
+    rc = _load().oracle_prefill(_ptr(q_bits), ctypes.byref(pool._c()), _ptr(bt), bt.shape[1],
+                                _ptr(sl), _ptr(qs), len(sl), num_q_heads, window,
+                                float(softmax_scale), _ptr(out), num_threads)
+    if rc != 0:
+        raise ValueError(f"oracle_prefill failed ({rc})")
     return out
 
 

@@ -249,17 +249,37 @@ void oracle_slot_mapping(const oracle_pool *pool, const int32_t *block_table,
  * h / (H_q / H_kv) ([Lab5] 分组查询注意力: consecutive query heads share a KV
  * head, the same as repeating each KV head G times).  Softmax with the
  * maximum subtracted, all in fp64. */
+static int attend_row_at(const uint16_t *qrow, const oracle_pool *pool,
+                         const int32_t *block_table, int32_t max_blocks_per_seq, int64_t len,
+                         int64_t pos, int32_t num_q_heads, int32_t window, double softmax_scale,
+                         int32_t b, int32_t h, int64_t key_begin, int64_t key_end,
+                         double *lse_out, double *o);
+
 static int attend_row(const uint16_t *q, const oracle_pool *pool, const int32_t *block_table,
                       int32_t max_blocks_per_seq, const int32_t *seq_lens, int32_t num_q_heads,
                       int32_t window, double softmax_scale, int32_t b, int32_t h,
                       int64_t key_begin, int64_t key_end, double *lse_out, double *o)
 {
+    const int64_t len = seq_lens[b];
+    return attend_row_at(q + ((int64_t)b * num_q_heads + h) * pool->head_dim, pool, block_table,
+                         max_blocks_per_seq, len, len - 1, num_q_heads, window, softmax_scale, b,
+                         h, key_begin, key_end, lse_out, o);
+}
+
+/* The same for a query row qrow at absolute position pos of a sequence whose
+ * cache holds len keys (pos <= len - 1): keys j <= pos (and j >= pos - w on
+ * a sliding layer), so a query sees the keys before it and itself -- causal
+ * within a chunk of several new tokens ([Lab5] Flash Attention: q_len > 1 in
+ * prefill; [Lab5] 滑动窗口注意力: mask M). */
+static int attend_row_at(const uint16_t *qrow, const oracle_pool *pool,
+                         const int32_t *block_table, int32_t max_blocks_per_seq, int64_t len,
+                         int64_t pos, int32_t num_q_heads, int32_t window, double softmax_scale,
+                         int32_t b, int32_t h, int64_t key_begin, int64_t key_end,
+                         double *lse_out, double *o)
+{
     const int32_t D = pool->head_dim;
     const int32_t G = num_q_heads / pool->num_kv_heads;
     const int32_t g = h / G;
-    const int64_t len = seq_lens[b];
-    const int64_t pos = len - 1;
-    const uint16_t *qrow = q + ((int64_t)b * num_q_heads + h) * D;
 
     for (int32_t d = 0; d < D; ++d)
         o[d] = 0.0;
@@ -360,6 +380,51 @@ int oracle_decode(const uint16_t *q, const oracle_pool *pool, const int32_t *blo
     }
     (void)num_threads;
     return bad ? OR_E_BLOCK : OR_OK;
+}
+
+/* Attention of a chunk of new tokens per sequence (chunked prefill, or the
+ * gamma + 1 tokens a speculative step verifies: tiniestgpt notes, section 7).
+ * Sequence b's query tokens are rows q_start[b] .. q_start[b+1]-1 of
+ * q [total][num_q_heads][head_dim]; they are the sequence's last n_b tokens,
+ * so token i sits at position seq_lens[b] - n_b + i and attends the keys
+ * allowed at that position (causal within the chunk, windowed on sliding
+ * layers).  out: [total][num_q_heads][head_dim] fp64. */
+int oracle_prefill(const uint16_t *q, const oracle_pool *pool, const int32_t *block_table,
+                   int32_t max_blocks_per_seq, const int32_t *seq_lens, const int32_t *q_start,
+                   int32_t batch, int32_t num_q_heads, int32_t window, double softmax_scale,
+                   double *out, int32_t num_threads)
+{
+    int rc = check_shapes(pool, num_q_heads);
+    if (rc)
+        return rc;
+    const int32_t D = pool->head_dim;
+    const int64_t total = q_start[batch];
+    int bad = 0;
+#ifdef _OPENMP
+    if (num_threads <= 0)
+        num_threads = omp_get_max_threads();
+#pragma omp parallel for schedule(dynamic, 1) num_threads(num_threads) reduction(| : bad)
+#endif
+    for (int64_t r = 0; r < total * num_q_heads; ++r) {
+        const int64_t row = r / num_q_heads;
+        const int32_t h = (int32_t)(r % num_q_heads);
+        int32_t b = 0;
+        while (q_start[b + 1] <= row)
+            ++b;
+        const int64_t n = q_start[b + 1] - q_start[b];
+        const int64_t len = seq_lens[b];
+        const int64_t pos = len - n + (row - q_start[b]);
+        double lse;
+        int e = pos < 0 ? OR_E_ARG
+                        : attend_row_at(q + (row * num_q_heads + h) * D, pool, block_table,
+                                        max_blocks_per_seq, len, pos, num_q_heads, window,
+                                        softmax_scale, b, h, 0, pos + 1, &lse,
+                                        out + r * D);
+        if (e)
+            bad |= 1;
+    }
+    (void)num_threads;
+    return bad ? OR_E_ARG : OR_OK;
 }
 
 /* Partial attention of every row (b, h) over its own key range

@@ -337,3 +337,77 @@ def empty_pool_arrays(spec: Spec, layout: Layout):
 def shrink(spec: Spec, **kw) -> Spec:
     """A smaller variant of a workload for oracle-speed parity tests."""
     return replace(spec, **kw)
+
+
+@dataclass
+class ChunkWorkload:
+    """A chunk of n_b new tokens per sequence (chunked prefill, or the
+    gamma + 1 tokens a speculative step verifies): the chunk is the last n_b
+    tokens of each sequence (seq_lens include it); queries are rows
+    q_start[b] .. q_start[b+1]-1 of q; the chunk's K/V are appended before
+    attending, after the history the chunk's queries may read."""
+    spec: Spec
+    layout: Layout
+    q: np.ndarray              # [total, H_q, D] uint16
+    q_start: np.ndarray        # [B + 1] int32
+    hist_k: np.ndarray         # [T, H_kv, D] uint16
+    hist_v: Optional[np.ndarray]
+    hist_slots: np.ndarray     # [T] int64
+    new_k: np.ndarray          # [total, H_kv, D] uint16, the chunk's tokens in order
+    new_v: Optional[np.ndarray]
+    new_slots: np.ndarray      # [total] int64
+    k_head_scale: Optional[np.ndarray] = None
+    v_head_scale: Optional[np.ndarray] = None
+
+    @property
+    def seq_lens(self):
+        return self.layout.seq_lens
+
+    @property
+    def block_table(self):
+        return self.layout.block_table
+
+
+def make_chunk_workload(spec: Spec, q_lens) -> ChunkWorkload:
+    """``q_lens``: chunk length per sequence (an int for all, or a sequence of
+    B ints), clipped to each sequence's length.  Paged layouts only."""
+    assert not spec.ring_blocks
+    rng = np.random.default_rng(spec.seed)
+    layout = make_layout(spec, rng)
+    vrng = np.random.default_rng(spec.seed * 1000 + 29)
+    B, Hq, Hkv, D, P = spec.batch, spec.num_q_heads, spec.num_kv_heads, spec.head_dim, spec.block_size
+    lens = layout.seq_lens.astype(np.int64)
+    n = np.broadcast_to(np.asarray(q_lens, np.int64), (B,))
+    n = np.minimum(n, lens).astype(np.int64)
+    q_start = np.zeros(B + 1, np.int32)
+    q_start[1:] = np.cumsum(n)
+    total = int(q_start[-1])
+    sigma = None
+    k_hs = v_hs = None
+    if spec.kv == "int8_head":
+        sig = (0.5 + 0.25 * np.arange(Hkv, dtype=np.float32)).astype(np.float32)
+        sigma = sig[None, :, None]
+        k_hs = (np.float32(4.0) * sig / np.float32(127.0)).astype(np.float32)
+        v_hs = (np.float32(3.0) * sig / np.float32(127.0)).astype(np.float32)
+    q = _normal_bf16(vrng, (total, Hq, D), replace(spec, outlier_frac=0.0))
+    # history: the positions before each chunk that its first query may read
+    seqs, poss = [], []
+    for b in range(B):
+        first = int(lens[b] - n[b])
+        lo = max(0, first - spec.window) if spec.window > 0 else 0
+        if first > lo:
+            seqs.append(np.full(first - lo, b, np.int64))
+            poss.append(np.arange(lo, first, dtype=np.int64))
+    hseq = np.concatenate(seqs) if seqs else np.zeros(0, np.int64)
+    hpos = np.concatenate(poss) if poss else np.zeros(0, np.int64)
+    hist_slots = slot_of(layout, P, hseq, hpos)
+    hist_k = _normal_bf16(vrng, (len(hseq), Hkv, D), spec, sigma)
+    hist_v = None if spec.alias else _normal_bf16(vrng, (len(hseq), Hkv, D), spec, sigma)
+    nseq = np.repeat(np.arange(B, dtype=np.int64), n)
+    npos = np.concatenate([np.arange(lens[b] - n[b], lens[b], dtype=np.int64) for b in range(B)]) \
+        if total else np.zeros(0, np.int64)
+    new_slots = slot_of(layout, P, nseq, npos)
+    new_k = _normal_bf16(vrng, (total, Hkv, D), spec, sigma)
+    new_v = None if spec.alias else _normal_bf16(vrng, (total, Hkv, D), spec, sigma)
+    return ChunkWorkload(spec, layout, q, q_start, hist_k, hist_v, hist_slots, new_k, new_v,
+                         new_slots, k_hs, v_hs)
