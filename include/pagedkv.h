@@ -259,6 +259,41 @@ PKV_API int paged_decode_attention(const void *q, const pkv_pool *pool, const in
                                    int32_t out_dtype, void *stream);
 
 /*
+ * paged_prefill_attention -- attention of a chunk of new tokens per sequence
+ * (q_len > 1: chunked prefill, or the gamma + 1 tokens a speculative step
+ * verifies).  Lab5-Gemma4, Flash Attention section: prefill's q_len > 1
+ * beside decode's q_len = 1, causal and sliding-window masks over the
+ * cache's history, GQA without repeated K/V, the partial last tile;
+ * tiniestgpt notes, section 7: the verify step feeds gamma + 1 tokens.
+ * Sequence b's chunk is its last n_b = q_start[b+1] - q_start[b] tokens,
+ * already appended to the pool (seq_lens include them): query row
+ * q_start[b] + i is the token at position seq_lens[b] - n_b + i, and for
+ * each query head h
+ *     out[row][h] = softmax_j(softmax_scale * <q[row][h], K_b[j]>) V_b[j]
+ * over the keys j in [lo, pos] of its own position pos (lo = pos - window
+ * on sliding layers, else 0): causal within the chunk.  A chunk of one
+ * token is the decode.
+ *   q:          [total_q][num_q_heads][head_dim] bf16, 16-byte aligned.
+ *   q_start:    [batch + 1] int32, non-decreasing, q_start[0] = 0,
+ *               q_start[batch] = total_q.
+ *   max_q_len:  host bound on every n_b (sizes the grid); a chunk longer
+ *               than it, or than its sequence, sets PKV_DEV_LEN_BOUND.
+ *   pool:       bf16 only (PKV_E_UNSUPPORTED for int8), paged or ring (a
+ *               ring must hold window + max_q_len slots: the chunk's first
+ *               query still sees keys its last token's slot would
+ *               overwrite in a smaller ring); num_q_heads / num_kv_heads in
+ *               {1, 2, 4, 8, 16}.
+ *   other arguments as for paged_decode_attention; out: [total_q]
+ *   [num_q_heads][head_dim], bf16 or fp32.  No workspace.
+ */
+PKV_API int paged_prefill_attention(const void *q, const int32_t *q_start, int32_t total_q,
+                                    int32_t max_q_len, const pkv_pool *pool,
+                                    const int32_t *block_table, int32_t max_blocks_per_seq,
+                                    const int32_t *seq_lens, int32_t batch, int32_t num_q_heads,
+                                    int32_t max_seq_len, int32_t window, float softmax_scale,
+                                    void *out, int32_t out_dtype, void *stream);
+
+/*
  * paged_decode_split_partial -- the first step of the split-KV path: every
  * (sequence, query head, split s) attends over keys
  * [lo + s*split_tokens', ...) where split_tokens' counts from the block

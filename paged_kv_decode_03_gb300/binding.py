@@ -92,6 +92,9 @@ def load_library():
     lib.paged_decode_attention_noalloc.argtypes = [p, p, p, i32, p, i32, i32, i32, i32, f32,
                                                    i32, p, i32, p]
     lib.paged_decode_attention_noalloc.restype = ctypes.c_int
+    lib.paged_prefill_attention.argtypes = [p, p, i32, i32, p, p, i32, p, i32, i32, i32, i32, f32,
+                                            p, i32, p]
+    lib.paged_prefill_attention.restype = ctypes.c_int
     lib.paged_kv_slot_mapping.argtypes = [p, p, i32, p, p, i32, p, p]
     lib.paged_kv_slot_mapping.restype = ctypes.c_int
     lib.paged_decode_step_workspace_bytes.argtypes = [p, i32, i32, i32, i32, i32]
@@ -433,3 +436,26 @@ def paged_decode_step(layers, slot_mapping, block_table, seq_lens, max_seq_len: 
                                  _dev_ptr(seq_lens, "seq_lens"), B, Hq, int(max_seq_len),
                                  int(split_tokens), ws_ptr, ws_bytes, out_dtype, _stream(stream)),
            "paged_decode_step")
+
+
+def paged_prefill_attention(q, q_start, pool: PagedKVPool, block_table, seq_lens, window: int,
+                            softmax_scale: float, out, max_seq_len: int, max_q_len: int,
+                            stream=None):
+    """Attention of each sequence's chunk of new tokens (q_len > 1): q
+    [total, H_q, D] bf16, rows q_start[b] .. q_start[b+1]-1 ([B + 1] int32)
+    are sequence b's last tokens (already appended), causal among
+    themselves; out [total, H_q, D] bf16 or fp32.  ``max_q_len`` bounds every
+    chunk's length on the host."""
+    import torch
+    lib = load_library()
+    pc = pool.c_struct()
+    total, Hq, _ = (int(x) for x in q.shape)
+    B = int(seq_lens.shape[0])
+    out_dtype = OUT_F32 if out.dtype == torch.float32 else OUT_BF16
+    _check(lib.paged_prefill_attention(_dev_ptr(q, "q"), _dev_ptr(q_start, "q_start"), total,
+                                       int(max_q_len), ctypes.byref(pc),
+                                       _dev_ptr(block_table, "block_table"), int(block_table.shape[1]),
+                                       _dev_ptr(seq_lens, "seq_lens"), B, Hq, int(max_seq_len),
+                                       int(window), float(softmax_scale), _dev_ptr(out, "out"),
+                                       out_dtype, _stream(stream)), "paged_prefill_attention")
+    return out

@@ -145,6 +145,28 @@ static int encode_q_map(CUtensorMap *map, const void *q, int32_t rows, int32_t h
     return PKV_OK;
 }
 
+// Tensor map over the chunk queries q [total][H_q][D] bf16 for the chunk
+// attention kernel: box = {64 dims, G heads, 128 / G tokens} with the
+// 128-byte swizzle, i.e. 128 query rows (token, head) of one kv head's group
+// as the K-major A operand.
+static int encode_chunk_q_map(CUtensorMap *map, const void *q, int32_t total, int32_t num_q_heads,
+                              int32_t head_dim, int32_t group)
+{
+    auto fn = encode_fn();
+    if (!fn)
+        return fail(PKV_E_DRIVER, "cuTensorMapEncodeTiled is unavailable");
+    cuuint64_t dims[3] = {(cuuint64_t)head_dim, (cuuint64_t)num_q_heads, (cuuint64_t)total};
+    cuuint64_t strides[2] = {(cuuint64_t)head_dim * 2, (cuuint64_t)num_q_heads * head_dim * 2};
+    cuuint32_t box[3] = {64u, (cuuint32_t)group, (cuuint32_t)(128 / group)};
+    cuuint32_t estr[3] = {1u, 1u, 1u};
+    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(q), dims, strides,
+                    box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS)
+        return fail(PKV_E_DRIVER, "cuTensorMapEncodeTiled (chunk q) failed (%d)", (int)r);
+    return PKV_OK;
+}
+
 static bool env_flag(const char *name)
 {
     const char *e = getenv(name);
@@ -550,6 +572,80 @@ static int run_decode(const void *q, const pkv_pool *pool, const int32_t *block_
     cudaError_t e = launch_decode(p, tmk, tmv, pool->head_dim, pool->dtype == PKV_INT8, gt, s);
     if (e != cudaSuccess)
         return cuda_fail(e, "decode launch");
+    return PKV_OK;
+}
+
+PKV_API int paged_prefill_attention(const void *q, const int32_t *q_start, int32_t total_q,
+                                    int32_t max_q_len, const pkv_pool *pool,
+                                    const int32_t *block_table, int32_t max_blocks_per_seq,
+                                    const int32_t *seq_lens, int32_t batch, int32_t num_q_heads,
+                                    int32_t max_seq_len, int32_t window, float softmax_scale,
+                                    void *out, int32_t out_dtype, void *stream)
+{
+    t_last_error.clear();
+    t_launches = 0;
+    if (int rc = check_decode_args(q, pool, block_table, max_blocks_per_seq, seq_lens, batch,
+                                   num_q_heads, max_seq_len, window, out, out_dtype))
+        return rc;
+    if (!q_start)
+        return fail(PKV_E_NULL, "q_start is NULL");
+    if (!aligned(q_start, 4))
+        return fail(PKV_E_ALIGN, "q_start must be 4-byte aligned");
+    if (total_q < 0 || max_q_len < 0)
+        return fail(PKV_E_SHAPE, "total_q or max_q_len < 0");
+    if (pool->dtype != PKV_BF16)
+        return fail(PKV_E_UNSUPPORTED, "chunk attention needs a bf16 pool (tensor-core operands)");
+    // a ring must hold the first query's window and the whole chunk at once
+    if (pool->ring_blocks > 0 &&
+        (int64_t)pool->ring_blocks * pool->block_size < (int64_t)window + max_q_len)
+        return fail(PKV_E_SHAPE, "ring of %d slots cannot hold a %d-token chunk and its window %d",
+                    pool->ring_blocks * pool->block_size, max_q_len, window);
+    const int group = num_q_heads / pool->num_kv_heads;
+    if (group != 1 && group != 2 && group != 4 && group != 8 && group != 16)
+        return fail(PKV_E_UNSUPPORTED, "chunk attention: %d query heads per kv head (1..16, "
+                    "a power of two)", group);
+    if (pool->num_kv_heads > 65535)
+        return fail(PKV_E_UNSUPPORTED, "too many kv heads");
+    if (batch == 0 || total_q == 0 || max_q_len == 0)
+        return PKV_OK;
+    if ((int64_t)max_q_len * group > (int64_t)128 * 65535)
+        return fail(PKV_E_UNSUPPORTED, "max_q_len too large");
+    const bool alias = pool->v == nullptr || pool->v == pool->k;
+    CUtensorMap tmk, tmv, tmq;
+    if (int rc = encode_pool_map_tc(&tmk, pool->k, *pool))
+        return rc;
+    if (alias)
+        tmv = tmk;
+    else if (int rc = encode_pool_map_tc(&tmv, pool->v, *pool))
+        return rc;
+    if (int rc = encode_chunk_q_map(&tmq, q, total_q, num_q_heads, pool->head_dim, group))
+        return rc;
+    PrefillParams p{};
+    p.q_start = q_start;
+    p.block_table = block_table;
+    p.seq_lens = seq_lens;
+    p.out = out;
+    p.err = error_word_ptr();
+    if (!p.err)
+        return fail(PKV_E_DRIVER, "cannot resolve the device error word");
+    p.max_blocks = max_blocks_per_seq;
+    p.ring_blocks = pool->ring_blocks;
+    p.batch = batch;
+    p.num_q_heads = num_q_heads;
+    p.num_kv_heads = pool->num_kv_heads;
+    p.group = group;
+    p.num_blocks = pool->num_blocks;
+    p.window = window;
+    p.max_seq_len = max_seq_len;
+    p.max_q_len = max_q_len;
+    p.alias = alias;
+    p.out_f32 = out_dtype == PKV_OUT_F32;
+    p.num_buffers = prefill_num_buffers(pool->head_dim, alias);
+    p.qk_scale_log2 = softmax_scale * LOG2E;
+    cudaError_t e = launch_prefill(p, tmk, tmv, tmq, pool->head_dim,
+                                   static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess)
+        return cuda_fail(e, "chunk attention launch");
     return PKV_OK;
 }
 

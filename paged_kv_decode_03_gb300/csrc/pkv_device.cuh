@@ -236,6 +236,14 @@ __device__ __forceinline__ uint64_t policy_evict_first()
     return p;
 }
 
+// L2 policy for data read by every CTA of a group (kept in L2 if possible).
+__device__ __forceinline__ uint64_t policy_evict_last()
+{
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
 // ------------------------------------------------------------ exp2 approx
 // ex2.approx.ftz.f32: hardware 2^x (relative error ~2^-22); ex2(-inf) = +0.
 __device__ __forceinline__ float fast_exp2(float x)

@@ -53,6 +53,29 @@ struct DecodeParams {
     int32_t *order_ws;
 };
 
+// Parameters of the chunk (q_len > 1) attention kernel.
+struct PrefillParams {
+    const int32_t *q_start;   // [B + 1] first query row of each sequence's chunk
+    const int32_t *block_table;
+    const int32_t *seq_lens;
+    void *out;                // [total][H_q][D]
+    unsigned int *err;
+    int32_t max_blocks;
+    int32_t ring_blocks;
+    int32_t batch;
+    int32_t num_q_heads;
+    int32_t num_kv_heads;
+    int32_t group;
+    int32_t num_blocks;
+    int32_t window;
+    int32_t max_seq_len;
+    int32_t max_q_len;        // host bound on any chunk's length (sizes the grid)
+    int32_t alias;
+    int32_t out_f32;
+    int32_t num_buffers;      // K/V tile buffers
+    float qk_scale_log2;
+};
+
 struct AppendParams {
     const uint16_t *k;
     const uint16_t *v;
@@ -109,6 +132,12 @@ cudaError_t launch_decode_tc(const DecodeParams &p, const CUtensorMap &tmk,
                              const CUtensorMap &tmv, const CUtensorMap &tmq, int head_dim,
                              cudaStream_t s);
 cudaError_t launch_append(const AppendParams &p, int int8, cudaStream_t s);
+// Chunk attention (tensor cores, bf16 pools): K/V tile buffers that fit, the
+// shared memory of a launch, and the launch itself.
+int prefill_num_buffers(int head_dim, int alias);
+size_t prefill_smem_bytes(int head_dim, int alias, int num_buffers);
+cudaError_t launch_prefill(const PrefillParams &p, const CUtensorMap &tmk, const CUtensorMap &tmv,
+                           const CUtensorMap &tmq, int head_dim, cudaStream_t s);
 cudaError_t launch_slot_mapping(const int32_t *block_table, int max_blocks, int ring_blocks,
                                 int num_blocks, const int32_t *seq_ids, const int64_t *positions,
                                 int num_tokens, int64_t *slots, unsigned int *err, cudaStream_t s);

@@ -355,9 +355,13 @@ class ChunkWorkload:
     hist_slots: np.ndarray     # [T] int64
     new_k: np.ndarray          # [total, H_kv, D] uint16, the chunk's tokens in order
     new_v: Optional[np.ndarray]
-    new_slots: np.ndarray      # [total] int64
+    new_slots: Optional[np.ndarray]  # [total] int64 (paged layouts; None for rings)
     k_head_scale: Optional[np.ndarray] = None
     v_head_scale: Optional[np.ndarray] = None
+    hist_seq: Optional[np.ndarray] = None
+    hist_pos: Optional[np.ndarray] = None
+    new_seq: Optional[np.ndarray] = None
+    new_pos: Optional[np.ndarray] = None
 
     @property
     def seq_lens(self):
@@ -370,8 +374,8 @@ class ChunkWorkload:
 
 def make_chunk_workload(spec: Spec, q_lens) -> ChunkWorkload:
     """``q_lens``: chunk length per sequence (an int for all, or a sequence of
-    B ints), clipped to each sequence's length.  Paged layouts only."""
-    assert not spec.ring_blocks
+    B ints), clipped to each sequence's length.  For a ring layout the slots
+    are left to each side's own address map (positions are given)."""
     rng = np.random.default_rng(spec.seed)
     layout = make_layout(spec, rng)
     vrng = np.random.default_rng(spec.seed * 1000 + 29)
@@ -400,14 +404,15 @@ def make_chunk_workload(spec: Spec, q_lens) -> ChunkWorkload:
             poss.append(np.arange(lo, first, dtype=np.int64))
     hseq = np.concatenate(seqs) if seqs else np.zeros(0, np.int64)
     hpos = np.concatenate(poss) if poss else np.zeros(0, np.int64)
-    hist_slots = slot_of(layout, P, hseq, hpos)
+    hist_slots = None if spec.ring_blocks else slot_of(layout, P, hseq, hpos)
     hist_k = _normal_bf16(vrng, (len(hseq), Hkv, D), spec, sigma)
     hist_v = None if spec.alias else _normal_bf16(vrng, (len(hseq), Hkv, D), spec, sigma)
     nseq = np.repeat(np.arange(B, dtype=np.int64), n)
     npos = np.concatenate([np.arange(lens[b] - n[b], lens[b], dtype=np.int64) for b in range(B)]) \
         if total else np.zeros(0, np.int64)
-    new_slots = slot_of(layout, P, nseq, npos)
+    new_slots = None if spec.ring_blocks else slot_of(layout, P, nseq, npos)
     new_k = _normal_bf16(vrng, (total, Hkv, D), spec, sigma)
     new_v = None if spec.alias else _normal_bf16(vrng, (total, Hkv, D), spec, sigma)
     return ChunkWorkload(spec, layout, q, q_start, hist_k, hist_v, hist_slots, new_k, new_v,
-                         new_slots, k_hs, v_hs)
+                         new_slots, k_hs, v_hs, hseq.astype(np.int32), hpos,
+                         nseq.astype(np.int32), npos)
