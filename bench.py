@@ -59,6 +59,9 @@ def parse_args():
                     help="skip the per-workload lines (every config, the six-layer step, "
                          "the oracle at all threads and at one thread)")
     ap.add_argument("--per-config-steps", type=int, default=100)
+    ap.add_argument("--chunk-only", type=int, default=0,
+                    help="time only the chunk attention (q_len > 1) with chunks of this many "
+                         "tokens on --config's shapes (prints that measurement, not a bench line)")
     return ap.parse_args()
 
 
@@ -547,7 +550,8 @@ def run_ours(args, rank, world, local_rank):
                      "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "peak_source": peak_kind,
                      "algorithmic_bytes_per_launch": decode_kernel_bytes,
-                     "traffic": recorded_traffic(args.config)},
+                     "traffic": recorded_traffic(args.config + ("_split_calls" if split_api
+                                                                else ""))},
         "gpu_launches": launches_per_step * args.steps,
         "device_error_word": status,
         "clocks": clocks,
@@ -737,6 +741,115 @@ def measure_step(dev, steps, warmup):
     return entry, layers
 
 
+def measure_prefill(spec, q_len, dev, steps, warmup, with_oracle):
+    """Chunk attention (q_len > 1): every sequence's last ``q_len`` tokens
+    attend their cache (chunked prefill), one paged_prefill_attention call
+    captured in a CUDA graph; events around each replay."""
+    import torch
+    import paged_kv_decode_03_gb300 as pkv
+    w = synth.make_chunk_workload(spec, q_len)
+    B, G = spec.batch, spec.group
+    pool = device_pool(spec, synth.Workload(spec, w.layout, w.q, w.hist_k, w.hist_v, w.hist_slots,
+                                            w.new_k, w.new_v, w.new_slots, None, None,
+                                            None, None), dev, hist=False)
+    for k_, v_, sl_ in ((w.hist_k, w.hist_v, w.hist_slots), (w.new_k, w.new_v, w.new_slots)):
+        for s0 in range(0, len(sl_), 1 << 16):
+            e0 = min(len(sl_), s0 + (1 << 16))
+            pkv.paged_kv_append(_dbits(k_[s0:e0], dev), None if v_ is None else _dbits(v_[s0:e0], dev),
+                                _dnum(sl_[s0:e0], dev), pool)
+    q = _dbits(w.q, dev)
+    qs, bt, sl = _dnum(w.q_start, dev), _dnum(w.block_table, dev), _dnum(w.seq_lens, dev)
+    out = torch.empty(q.shape, dtype=torch.bfloat16, device=dev)
+    max_len, max_q = int(w.seq_lens.max()), int(np.diff(w.q_start).max())
+    scale = float(np.float32(spec.softmax_scale))
+
+    def call():
+        pkv.paged_prefill_attention(q, qs, pool, bt, sl, spec.window, scale, out, max_len, max_q)
+
+    call()
+    launches = pkv.last_launch_count()
+    for _ in range(max(3, warmup)):
+        call()
+    torch.cuda.synchronize()
+    cap = torch.cuda.Stream()
+    cap.wait_stream(torch.cuda.current_stream())
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(cap):
+        with torch.cuda.graph(graph, stream=cap):
+            call()
+    torch.cuda.current_stream().wait_stream(cap)
+    for _ in range(3):
+        graph.replay()
+    torch.cuda.synchronize()
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
+    evs[0].record()
+    for i in range(steps):
+        graph.replay()
+        evs[i + 1].record()
+    torch.cuda.synchronize()
+    us = evs[0].elapsed_time(evs[-1]) / steps * 1e3
+    # algorithmic work: every (query, head) row against the keys its mask
+    # allows, two contractions of head_dim each; bytes: the unique KV rows
+    # the chunks read, Q and the output
+    n = np.diff(w.q_start).astype(np.int64)
+    lens = w.seq_lens.astype(np.int64)
+    keys = 0
+    for b in range(B):
+        pos = lens[b] - n[b] + np.arange(n[b])
+        lo = np.maximum(0, pos - spec.window) if spec.window else np.zeros_like(pos)
+        keys += int((pos - lo + 1).sum())
+    flops = 4 * keys * spec.num_q_heads * spec.head_dim
+    kv = 0
+    for b in range(B):
+        first = lens[b] - n[b]
+        lo = max(0, first - spec.window) if spec.window else 0
+        kv += int(lens[b] - lo)
+    kv_bytes = kv * bytes_model.bytes_per_key(spec.num_kv_heads, spec.head_dim, spec.kv, spec.alias)
+    qo_bytes = 2 * int(n.sum()) * spec.num_q_heads * spec.head_dim * 2
+    peaks_d = {}
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            peaks_d = json.load(f)
+    except Exception:
+        pass
+    tf_peak = float(peaks_d.get("bf16_tflops", 1900.0))
+    hbm_peak, _ = peaks()
+    tflops = flops / (us * 1e-6) / 1e12
+    gbs = (kv_bytes + qo_bytes) / (us * 1e-6) / 1e9
+    entry = {
+        "workload": f"{workload_desc(spec)}; chunks of {q_len} tokens per sequence (chunked prefill)",
+        "call": "paged_prefill_attention, one CUDA graph",
+        "decode_kernel": "tensor cores (tcgen05): S = Q K^T, O += P V in TMEM, 128 query rows per CTA",
+        "kernel_us": round(us, 3),
+        "query_tokens_per_s": round(int(n.sum()) / (us * 1e-6), 1),
+        "algorithmic_tflop": round(flops / 1e12, 4),
+        "achieved_tflops": round(tflops, 2), "bf16_peak_tflops": tf_peak,
+        "frac_of_bf16_peak": round(tflops / tf_peak, 4),
+        "hbm_gbs": round(gbs, 1), "frac_of_measured_hbm": round(gbs / hbm_peak, 4),
+        "gpu_launches_per_step": launches,
+        "device_error_word": pkv.device_status(clear=True),
+    }
+    if with_oracle:
+        import oracle
+        sub = synth.make_chunk_workload(synth.shrink(spec, batch=4), q_len)
+        k_, v_, _, _ = synth.empty_pool_arrays(sub.spec, sub.layout)
+        opool = oracle.OraclePool(k=k_, v=v_)
+        oracle.append(sub.hist_k, sub.hist_v, sub.hist_slots, opool)
+        oracle.append(sub.new_k, sub.new_v, sub.new_slots, opool)
+        t0 = time.perf_counter()
+        oracle.prefill(sub.q, opool, sub.block_table, sub.seq_lens, sub.q_start, spec.num_q_heads,
+                       spec.window, np.float32(spec.softmax_scale))
+        t = time.perf_counter() - t0
+        entry["oracle"] = {"kind": "oracle", "threads": oracle.max_threads(),
+                           "all_threads_s": round(t, 4),
+                           "query_tokens_per_s": round(int(sub.q_start[-1]) / t, 1),
+                           "sample": f"4 of {B} sequences, chunks of {q_len}, fp64 C oracle"}
+    del pool, q, out, graph
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return entry
+
+
 def per_config(args, dev, main_entry, main_spec, main_w):
     """Every workload at its full size: the decode kernel's time and roofline
     fraction (CUDA events over CUDA-graph replays), the six-layer step, and
@@ -760,6 +873,7 @@ def per_config(args, dev, main_entry, main_spec, main_w):
         if spec.split_tokens:
             # and the two split-KV calls with that split length
             out[name + "_split_calls"] = measure_layer(spec, w, dev, req, steps, warm)
+            out[name + "_split_calls"]["traffic"] = recorded_traffic(name + "_split_calls")
         if cpu:
             out[name]["oracle"] = oracle_full_run(spec, w)
         del w
@@ -767,6 +881,8 @@ def per_config(args, dev, main_entry, main_spec, main_w):
     out["c5"] = entry
     if cpu:
         out["c5"]["oracle"] = oracle_full_run(layers[0].spec, layers[0], layers)
+    del layers
+    out["c2_chunk128"] = measure_prefill(synth.C2, 128, dev, steps, warm, cpu)
     return out
 
 
@@ -902,6 +1018,15 @@ def main():
         line = run_reference(args, rank)
         if line is not None:
             print(json.dumps(line), flush=True)
+        return 0
+    if args.chunk_only:
+        import torch
+        import paged_kv_decode_03_gb300 as pkv
+        torch.cuda.set_device(local_rank)
+        pkv.load_library()
+        entry = measure_prefill(workload_spec(args), args.chunk_only, torch.device("cuda", local_rank),
+                                args.steps, args.warmup, not args.no_cpu_baseline)
+        print(json.dumps(entry), flush=True)
         return 0
     if world > 1:
         import torch

@@ -432,6 +432,20 @@ PKV_API int paged_decode_step(const pkv_layer *layers, int32_t num_layers,
  */
 PKV_API int32_t paged_decode_uses_tensor_cores(const pkv_pool *pool, int32_t num_q_heads);
 
+/*
+ * pkv_check_bounded_wait -- diagnostic of the failure path every pipeline
+ * wait of this library takes: one CTA of `threads` threads waits, with the
+ * kernels' own bounded wait (spin = 0: the sleeping wait; 1: the polling
+ * wait), on an mbarrier phase that nothing completes.  Each wait gives up
+ * after limit_ns nanoseconds (1 us .. 2 s), sets PKV_DEV_TIMEOUT in the
+ * device error word and the kernel returns; out[t] = 1 for every thread
+ * whose wait gave up.  Nothing faults and the context stays usable.  Read
+ * the result after synchronising (pkv_device_status).  out: [threads] int32
+ * device array.
+ */
+PKV_API int pkv_check_bounded_wait(uint64_t limit_ns, int32_t spin, int32_t *out,
+                                   int32_t threads, void *stream);
+
 /* Number of kernels the calling thread's last call of this library launched. */
 PKV_API int32_t pkv_last_launch_count(void);
 

@@ -14,6 +14,6 @@ from .binding import (  # noqa: F401
     paged_decode_lse_combine, paged_decode_workspace_bytes, paged_decode_num_splits,
     paged_decode_split_tokens, PagedKVError, paged_decode_attention_noalloc,
     paged_decode_partial_workspace_bytes, uses_tensor_cores, last_launch_count,
-    STATIC_SCRATCH_BYTES, DecodeLayer, paged_prefill_attention, paged_decode_step, paged_decode_step_workspace_bytes,
+    STATIC_SCRATCH_BYTES, DecodeLayer, paged_prefill_attention, check_bounded_wait, paged_decode_step, paged_decode_step_workspace_bytes,
     library_path, load_library, device_status, exported_symbols,
 )

@@ -92,6 +92,8 @@ def load_library():
     lib.paged_decode_attention_noalloc.argtypes = [p, p, p, i32, p, i32, i32, i32, i32, f32,
                                                    i32, p, i32, p]
     lib.paged_decode_attention_noalloc.restype = ctypes.c_int
+    lib.pkv_check_bounded_wait.argtypes = [ctypes.c_uint64, i32, p, i32, p]
+    lib.pkv_check_bounded_wait.restype = ctypes.c_int
     lib.paged_prefill_attention.argtypes = [p, p, i32, i32, p, p, i32, p, i32, i32, i32, i32, f32,
                                             p, i32, p]
     lib.paged_prefill_attention.restype = ctypes.c_int
@@ -459,3 +461,12 @@ def paged_prefill_attention(q, q_start, pool: PagedKVPool, block_table, seq_lens
                                        int(window), float(softmax_scale), _dev_ptr(out, "out"),
                                        out_dtype, _stream(stream)), "paged_prefill_attention")
     return out
+
+
+def check_bounded_wait(limit_ns: int, spin: bool, out, stream=None) -> None:
+    """Run the pipelines' bounded wait out on purpose (see
+    pkv_check_bounded_wait): ``out`` is an int32 CUDA tensor, one entry per
+    waiting thread, set to 1 where the wait gave up."""
+    _check(load_library().pkv_check_bounded_wait(int(limit_ns), 1 if spin else 0,
+                                                 _dev_ptr(out, "out"), int(out.numel()),
+                                                 _stream(stream)), "pkv_check_bounded_wait")

@@ -283,6 +283,27 @@ PKV_API int pkv_device_status(int32_t clear)
     return static_cast<int>(w);
 }
 
+PKV_API int pkv_check_bounded_wait(uint64_t limit_ns, int32_t spin, int32_t *out,
+                                   int32_t threads, void *stream)
+{
+    t_last_error.clear();
+    t_launches = 0;
+    if (!out || !aligned(out, 4))
+        return fail(PKV_E_NULL, "out is NULL or misaligned");
+    if (threads < 1 || threads > 1024)
+        return fail(PKV_E_ARG, "threads %d", threads);
+    if (limit_ns < 1000 || limit_ns > 2000000000ull)
+        return fail(PKV_E_ARG, "limit_ns must be in [1 us, 2 s]");
+    unsigned int *err = error_word_ptr();
+    if (!err)
+        return fail(PKV_E_DRIVER, "cannot resolve the device error word");
+    cudaError_t e = launch_bounded_wait(limit_ns, spin, out, threads, err,
+                                        static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess)
+        return cuda_fail(e, "bounded-wait check launch");
+    return PKV_OK;
+}
+
 PKV_API int32_t paged_decode_uses_tensor_cores(const pkv_pool *pool, int32_t num_q_heads)
 {
     t_last_error.clear();

@@ -175,4 +175,29 @@ cudaError_t launch_slot_mapping(const int32_t *block_table, int max_blocks, int 
     return cudaGetLastError();
 }
 
+// The pipelines' bounded waits, run out on purpose: every thread waits on
+// an mbarrier phase that nothing completes, with the same wait functions the
+// decode kernels use (sleeping and polling), and must give up after
+// limit_ns, record PKV_DEV_TIMEOUT and return.  out[threadIdx.x] = 1 if that
+// thread's wait returned false.
+__global__ void bounded_wait_kernel(uint64_t limit_ns, int spin, int *out, unsigned int *err)
+{
+    __shared__ __align__(8) uint64_t bar;
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);  // one arrival would complete the phase; none comes
+        fence_barrier_init();
+    }
+    __syncthreads();
+    const bool ok = spin ? mbar_wait_spin(&bar, 0, err, limit_ns) : mbar_wait(&bar, 0, err, limit_ns);
+    out[threadIdx.x] = ok ? 0 : 1;
+}
+
+cudaError_t launch_bounded_wait(uint64_t limit_ns, int spin, int *out, int threads,
+                                unsigned int *err, cudaStream_t s)
+{
+    bounded_wait_kernel<<<1, threads, 0, s>>>(limit_ns, spin, out, err);
+    note_launch();
+    return cudaGetLastError();
+}
+
 }  // namespace pkv

@@ -132,6 +132,8 @@ cudaError_t launch_decode_tc(const DecodeParams &p, const CUtensorMap &tmk,
                              const CUtensorMap &tmv, const CUtensorMap &tmq, int head_dim,
                              cudaStream_t s);
 cudaError_t launch_append(const AppendParams &p, int int8, cudaStream_t s);
+cudaError_t launch_bounded_wait(uint64_t limit_ns, int spin, int *out, int threads,
+                                unsigned int *err, cudaStream_t s);
 // Chunk attention (tensor cores, bf16 pools): K/V tile buffers that fit, the
 // shared memory of a launch, and the launch itself.
 int prefill_num_buffers(int head_dim, int alias);

@@ -548,3 +548,23 @@ def test_tensor_core_and_cuda_core_kernels_agree():
         del os.environ["PKV_DISABLE_TC"]
     torch.cuda.synchronize()
     assert _gpu.max_row_rel_err(a, c) <= 2 * F32_REL_TOL
+
+
+@pytest.mark.parametrize("spin", [False, True])
+def test_bounded_wait_runs_out_and_reports(spin):
+    """The failure path of every pipeline wait: a wait on an mbarrier phase
+    that nothing completes gives up after its limit (1 ms here), sets
+    PKV_DEV_TIMEOUT and returns; the context stays usable (a decode right
+    after it matches the oracle)."""
+    assert pkv.device_status(clear=True) == 0
+    out = torch.zeros(64, dtype=torch.int32, device="cuda")
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record()
+    pkv.check_bounded_wait(1_000_000, spin, out)
+    t1.record()
+    torch.cuda.synchronize()
+    assert int(out.sum()) == 64, "every thread's wait must give up"
+    assert pkv.device_status(clear=True) & 8  # PKV_DEV_TIMEOUT
+    assert t0.elapsed_time(t1) < 1000.0  # bounded: returned well within a second
+    _run_case(synth.C1, splits=(0,), out_modes=(False,))
