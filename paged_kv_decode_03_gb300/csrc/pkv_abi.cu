@@ -236,15 +236,14 @@ static int check_pool(const pkv_pool *pool)
     return PKV_OK;
 }
 
-// Ring depth override for tuning sweeps (PKV_STAGES); 0 = automatic.
-static int stages_override()
+// Ring depth override for tuning builds (-DPKV_RING_STAGES=n); 0, the
+// product's value, = automatic.
+#ifndef PKV_RING_STAGES
+#define PKV_RING_STAGES 0
+#endif
+static constexpr int stages_override()
 {
-    static int v = [] {
-        const char *e = getenv("PKV_STAGES");
-        int s = e ? atoi(e) : 0;
-        return s < 0 ? 0 : (s > 16 ? 16 : s);
-    }();
-    return v;
+    return PKV_RING_STAGES < 0 ? 0 : (PKV_RING_STAGES > 16 ? 16 : PKV_RING_STAGES);
 }
 
 // Most paged blocks the key range of a length-<=L sequence can touch.
@@ -549,8 +548,8 @@ static int run_decode(const void *q, const pkv_pool *pool, const int32_t *block_
     p.alias = alias;
     p.out_f32 = out_dtype == PKV_OUT_F32;
     // Ring depth: the most CTAs per SM, then the deepest ring that keeps
-    // them (decode_ring_stages); PKV_STAGES overrides it within the opt-in
-    // shared-memory limit of one CTA.
+    // them (decode_ring_stages); a tuning build's PKV_RING_STAGES overrides
+    // it within the opt-in shared-memory limit of one CTA.
     {
         const int i8 = pool->dtype == PKV_INT8;
         const int pt = i8 && pool->scale_mode == PKV_SCALE_PER_TOKEN;
@@ -576,7 +575,7 @@ static int run_decode(const void *q, const pkv_pool *pool, const int32_t *block_
     if ((int64_t)p.num_kv_heads * p.head_chunks > 65535)
         return fail(PKV_E_UNSUPPORTED, "too many kv heads");
     if (tc) {
-        // ring of 32 KB units: 6 by default (one CTA per SM), PKV_STAGES overrides
+        // ring of 32 KB units: 6 by default (one CTA per SM), PKV_RING_STAGES overrides
         int nu = stages_override() ? stages_override() : 6;
         while (nu > 2 && decode_tc_smem_bytes(nu) > 227u * 1024u)
             --nu;

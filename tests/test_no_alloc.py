@@ -4,8 +4,8 @@ an engine that reserved all of HBM for its KV pool, a loop in which an
 allocation would synchronise the device).  Its split partials live in a fixed
 per-device array inside the library instead of a caller workspace.
 
-Collected last on purpose: a run that stops at the first failure has then
-already run every other test."""
+Run last (tests/conftest.py orders the collection): a run that stops at the
+first failure has then already run every other test."""
 from __future__ import annotations
 
 import ctypes
