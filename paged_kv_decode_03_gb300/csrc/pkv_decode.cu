@@ -45,7 +45,13 @@ namespace pkv {
 
 constexpr int NC = 4;                    // consumer warps per CTA
 constexpr int THREADS = (NC + 1) * 32;   // + one producer warp
-constexpr int BAR_BYTES = 640;           // mbarriers + stage masks at the start of smem
+// Start of smem: mbarriers (512 B) and stage masks (64 B); at PW_OFF the
+// consumer warps' P.V weights of a stage (NC x at most 32 x 8 B); at RED_OFF
+// the int8 score transposes (Cfg::RED_BYTES, instances with a GQA tile); the
+// ring after them.
+constexpr int PW_OFF = 640;
+constexpr int RED_OFF = PW_OFF + NC * 32 * 8;
+constexpr int BAR_BYTES = RED_OFF;
 
 // Paged blocks per ring stage: about 8 KB of K per stage (int8: at least four
 // blocks, i.e. 16 keys per consumer warp, since unpacking makes its per-key
@@ -112,6 +118,12 @@ struct Cfg {
     static_assert(KPL >= 1 && KPW % KG == 0, "keys per lane");
     static_assert(NV >= 1 && NV <= LPK && LPK % NV == 0, "reduction width");
     static_assert(KPW <= P || KPW % P == 0, "warp keys within or across whole blocks");
+    static_assert(KPW * GT <= 32, "weights of a warp's stage fit its PW_OFF slice");
+    // int8 with a GQA tile: the scores' cross-lane sums go through shared
+    // memory (a transpose) instead of a shuffle reduce-scatter
+    static constexpr bool RED = INT8 && GT >= 2 && NV == LPK && (LPK == 8 || LPK == 16);
+    static constexpr int RED_KG = NV * LPK + LPK;               // floats per key group
+    static constexpr int RED_BYTES = RED ? NC * KG * RED_KG * 4 : 0;
 };
 
 __host__ __device__ constexpr int round_up(int x, int a) { return (x + a - 1) / a * a; }
@@ -195,7 +207,8 @@ __device__ __forceinline__ void decode_body(const DecodeParams &p, const CUtenso
     uint64_t *vfull = kfull + 32;
     uint64_t *vempty = kfull + 48;
     uint32_t *smask = reinterpret_cast<uint32_t *>(kfull + 64);  // valid blocks per stage
-    uint8_t *ring = smem + BAR_BYTES;
+    uint8_t *ring = smem + BAR_BYTES + C::RED_BYTES;
+    float *red = reinterpret_cast<float *>(smem + RED_OFF);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int split = blockIdx.x;
@@ -394,6 +407,16 @@ __device__ __forceinline__ void decode_body(const DecodeParams &p, const CUtenso
     const int my_h = my_idx / KPL, my_r = my_idx % KPL;
     const int km = kb + KG * my_r;          // its key within a stage
     const bool l_owner = (dl % DUP) == 0;   // one lane per value adds to l
+    const uint32_t km_bit = 1u << (km / C::P);  // its block within a stage
+    // the blocks of a stage that hold this warp's keys
+    uint32_t wmask = 0;
+#pragma unroll
+    for (int t = 0; t < BPS; ++t)
+        if (t * C::P < k0w + KPW && (t + 1) * C::P > k0w)
+            wmask |= 1u << t;
+    // This key group's P.V weights of a stage, [key][head], each stored as a
+    // (p, p) pair so that the packed FMAs take it as it is loaded.
+    float2 *pw = reinterpret_cast<float2 *>(smem + PW_OFF) + (warp * KG + kg) * (KPL * GT);
 
     int st = 0;          // ring slot of stage sidx
     uint32_t par = 0;    // parity of its fill
@@ -408,29 +431,72 @@ __device__ __forceinline__ void decode_body(const DecodeParams &p, const CUtenso
         const int jst = (ub0 + sidx * BPS) * C::P;  // key index of the stage's first row
         const int jw = jst + k0w;
         // all of this warp's keys hold data and lie in [lo, pos]
-        bool all_in = jw >= kr.lo && jw + KPW - 1 <= kr.pos;
-#pragma unroll
-        for (int t = 0; t < BPS; ++t)
-            if (t * C::P < k0w + KPW && (t + 1) * C::P > k0w && !(vmask >> t & 1u))
-                all_in = false;
+        const bool all_in = jw >= kr.lo && jw + KPW - 1 <= kr.pos && (vmask & wmask) == wmask;
         // ---- scores of this lane's KPL keys for the GT heads
         float acc[NV];
+        if constexpr (INT8 && GT >= 2 && KPL % 2 == 0) {
+            // two keys at a time: twice the independent multiply-add chains
+            // in flight (the int8 unpack makes each chain long)
 #pragma unroll
-        for (int r = 0; r < KPL; ++r) {
-            float2 kf[NPR];
-            load_chunk<INT8, C::CB>(kt + lane_base + koff(r), kf);
+            for (int r = 0; r < KPL; r += 2) {
+                float2 ka[NPR], kb2[NPR];
+                load_chunk<INT8, C::CB>(kt + lane_base + koff(r), ka);
+                load_chunk<INT8, C::CB>(kt + lane_base + koff(r + 1), kb2);
 #pragma unroll
-            for (int h = 0; h < GT; ++h) {
-                float2 a = __fmul2_rn(qf[h][0], kf[0]);
+                for (int h = 0; h < GT; ++h) {
+                    float2 a = __fmul2_rn(qf[h][0], ka[0]);
+                    float2 c = __fmul2_rn(qf[h][0], kb2[0]);
 #pragma unroll
-                for (int e = 1; e < NPR; ++e)
-                    a = __ffma2_rn(qf[h][e], kf[e], a);
-                acc[h * KPL + r] = a.x + a.y;
+                    for (int e = 1; e < NPR; ++e) {
+                        a = __ffma2_rn(qf[h][e], ka[e], a);
+                        c = __ffma2_rn(qf[h][e], kb2[e], c);
+                    }
+                    acc[h * KPL + r] = a.x + a.y;
+                    acc[h * KPL + r + 1] = c.x + c.y;
+                }
+            }
+        } else {
+#pragma unroll
+            for (int r = 0; r < KPL; ++r) {
+                float2 kf[NPR];
+                load_chunk<INT8, C::CB>(kt + lane_base + koff(r), kf);
+#pragma unroll
+                for (int h = 0; h < GT; ++h) {
+                    float2 a = __fmul2_rn(qf[h][0], kf[0]);
+#pragma unroll
+                    for (int e = 1; e < NPR; ++e)
+                        a = __ffma2_rn(qf[h][e], kf[e], a);
+                    acc[h * KPL + r] = a.x + a.y;
+                }
             }
         }
-        float s = reduce_scatter<NV, LPK>(acc, lane);
+        float s;
+        if constexpr (C::RED) {
+            // row v holds value v's LPK partial sums; 4-float chunks are
+            // xor-swizzled by row so that both the row-wise stores and the
+            // chunked row reads are free of bank conflicts
+            constexpr int RPB = 32 / LPK;  // rows per 32 banks
+            auto swz = [](int v) { return (v / RPB) & (LPK / 4 - 1); };
+            float *rd = red + (warp * KG + kg) * C::RED_KG;
+#pragma unroll
+            for (int v = 0; v < NV; ++v)
+                rd[v * LPK + (((dl >> 2) ^ swz(v)) << 2) + (dl & 3)] = acc[v];
+            __syncwarp();
+            const float4 *row = reinterpret_cast<const float4 *>(rd + dl * LPK);
+            const int sw = swz(dl);
+            float t0 = 0.f, t1 = 0.f;
+#pragma unroll
+            for (int c = 0; c < LPK / 4; ++c) {
+                const float4 x = row[c ^ sw];
+                t0 += x.x + x.y;
+                t1 += x.z + x.w;
+            }
+            s = t0 + t1;
+        } else {
+            s = reduce_scatter<NV, LPK>(acc, lane);
+        }
         const int jm = jst + km;
-        const bool ok = (vmask >> (km / C::P) & 1u) && jm >= kr.lo && jm <= kr.pos;
+        const bool ok = (vmask & km_bit) && jm >= kr.lo && jm <= kr.pos;
         if (per_token)
             s *= ksc[km];
         s = ok ? s : -INFINITY;
@@ -485,27 +551,70 @@ __device__ __forceinline__ void decode_body(const DecodeParams &p, const CUtenso
         if (per_token)
             pv = ok ? pr * vsc[km] : 0.f;
         // ---- P.V over this lane's KPL keys
+        if constexpr (INT8 && GT >= 2) {
+            // int8: the weights go through shared memory as (p, p) pairs
+            // (one load per key for all heads, no register moves to form the
+            // pairs), and stages whose keys all count skip the masking
+            if (l_owner)
+                pw[my_r * GT + my_h] = make_float2(pv, pv);
+            __syncwarp();
+            auto pv_key = [&](int r) {
+                float2 w2[GT];
+                if constexpr (GT == 1) {
+                    w2[0] = pw[r];
+                } else {
 #pragma unroll
-        for (int r = 0; r < KPL; ++r) {
-            float w[GT];
+                    for (int h = 0; h < GT; h += 2) {
+                        const float4 t = *reinterpret_cast<const float4 *>(pw + r * GT + h);
+                        w2[h] = make_float2(t.x, t.y);
+                        w2[h + 1] = make_float2(t.z, t.w);
+                    }
+                }
+                float2 vf[NPR];
+                load_chunk<INT8, C::CB>(vt + lane_base + koff(r), vf);
 #pragma unroll
-            for (int h = 0; h < GT; ++h)
-                w[h] = __shfl_sync(FULL_MASK, pv, (h * KPL + r) * DUP, LPK);
-            if (!all_in) {
-                // masked key: its slot may hold stale data, do not touch it
-                const int k = kb + KG * r;
-                const int j = jst + k;
-                if (!(vmask >> (k / C::P) & 1u) || j < kr.lo || j > kr.pos)
-                    continue;
+                for (int h = 0; h < GT; ++h)
+#pragma unroll
+                    for (int e = 0; e < NPR; ++e)
+                        o[h][e] = __ffma2_rn(w2[h], vf[e], o[h][e]);
+            };
+            if (all_in) {
+#pragma unroll
+                for (int r = 0; r < KPL; ++r)
+                    pv_key(r);
+            } else {
+#pragma unroll
+                for (int r = 0; r < KPL; ++r) {
+                    // masked key: its slot may hold stale data, do not touch it
+                    const int k = kb + KG * r;
+                    const int j = jst + k;
+                    if ((vmask >> (k / C::P) & 1u) && j >= kr.lo && j <= kr.pos)
+                        pv_key(r);
+                }
             }
-            float2 vf[NPR];
-            load_chunk<INT8, C::CB>(vt + lane_base + koff(r), vf);
+        } else {
 #pragma unroll
-            for (int h = 0; h < GT; ++h) {
-                const float2 w2 = make_float2(w[h], w[h]);
+            for (int r = 0; r < KPL; ++r) {
+                float w[GT];
 #pragma unroll
-                for (int e = 0; e < NPR; ++e)
-                    o[h][e] = __ffma2_rn(w2, vf[e], o[h][e]);
+                for (int h = 0; h < GT; ++h)
+                    w[h] = __shfl_sync(FULL_MASK, pv, (h * KPL + r) * DUP, LPK);
+                if (!all_in) {
+                    // masked key: its slot may hold stale data, do not touch it
+                    const int k = kb + KG * r;
+                    const int j = jst + k;
+                    if (!(vmask >> (k / C::P) & 1u) || j < kr.lo || j > kr.pos)
+                        continue;
+                }
+                float2 vf[NPR];
+                load_chunk<INT8, C::CB>(vt + lane_base + koff(r), vf);
+#pragma unroll
+                for (int h = 0; h < GT; ++h) {
+                    const float2 w2 = make_float2(w[h], w[h]);
+#pragma unroll
+                    for (int e = 0; e < NPR; ++e)
+                        o[h][e] = __ffma2_rn(w2, vf[e], o[h][e]);
+                }
             }
         }
         __syncwarp();
@@ -608,12 +717,16 @@ __device__ __forceinline__ void decode_body(const DecodeParams &p, const CUtenso
 // The kernels.  One query head per CTA has its own entry with at most 80
 // registers, so that five CTAs fit an SM (left to itself the compiler takes
 // 81 for the int8 head_dim-128 instance, which then runs four CTAs per SM and
-// measured 6% slower); the other instances keep the compiler's choice (an
-// explicit bound of one CTA makes it take more registers than without).
+// measured 6% slower).  The int8 two-head instances are bounded to three
+// CTAs per SM (at most 136 registers), which their shared memory allows
+// anyway; the others carry an explicit bound of one CTA, with which the
+// compiler takes more registers than without (the bf16 two-head instance
+// then runs four CTAs per SM instead of five and measured 2-3% faster on
+// the Gemma4 sliding shape).
 template <int D, int GT, bool INT8>
-__global__ void __launch_bounds__(THREADS) decode_kernel(const DecodeParams p,
-                                                         const __grid_constant__ CUtensorMap tmk,
-                                                         const __grid_constant__ CUtensorMap tmv)
+__global__ void __launch_bounds__(THREADS, (INT8 && GT == 2) ? 3 : 1)
+    decode_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmk,
+                  const __grid_constant__ CUtensorMap tmv)
 {
     decode_body<D, GT, INT8>(p, &tmk, &tmv);
 }
@@ -706,6 +819,24 @@ int decode_group_tile(int group)
     return group >= 4 ? 4 : (group >= 2 ? (group == 2 ? 2 : 4) : 1);
 }
 
+template <int D>
+static int red_bytes_d(int int8, int gt)
+{
+    if (!int8)
+        return 0;
+    return gt == 1 ? Cfg<D, 1, true>::RED_BYTES
+                   : (gt == 2 ? Cfg<D, 2, true>::RED_BYTES : Cfg<D, 4, true>::RED_BYTES);
+}
+
+static int red_bytes(int head_dim, int int8, int gt)
+{
+    switch (head_dim) {
+    case 64: return red_bytes_d<64>(int8, gt);
+    case 128: return red_bytes_d<128>(int8, gt);
+    default: return red_bytes_d<256>(int8, gt);
+    }
+}
+
 size_t decode_smem_bytes(int head_dim, int int8, int alias, int per_token, int group_tile,
                          int num_stages)
 {
@@ -715,7 +846,7 @@ size_t decode_smem_bytes(int head_dim, int int8, int alias, int per_token, int g
                         slot_bytes(tile, bps, per_token);
     const size_t merge = (2 * NC * group_tile + static_cast<size_t>(NC) * group_tile * head_dim) *
                          sizeof(float);
-    return BAR_BYTES + (ring > merge ? ring : merge);
+    return BAR_BYTES + red_bytes(head_dim, int8, group_tile) + (ring > merge ? ring : merge);
 }
 
 // Let the kernel use the opt-in maximum of dynamic shared memory (once).
