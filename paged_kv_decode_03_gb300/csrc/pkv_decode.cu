@@ -22,12 +22,18 @@
 //     (a quarter of its keys each) and keep independent online-softmax
 //     states that merge at the end.
 //   * A lane owns one 16-byte chunk of a key row (8 bf16 or 16 int8
-//     values; 8 bytes for int8 rows of 256 bytes), so head_dim spans
-//     LPK = row bytes / chunk bytes lanes and a warp reads 32/LPK keys at
-//     once with vector shared loads.  The partial dot
-//     products of a lane's keys x GT heads finish with one butterfly
-//     reduce-scatter inside its LPK-lane group; P.V accumulates per lane and
-//     the key groups are summed once at the end.
+//     values; 8-byte chunks where four heads per CTA would otherwise hold
+//     too many q and o values per lane), so head_dim spans LPK = row bytes /
+//     chunk bytes lanes and a warp reads 32/LPK keys at once with vector
+//     shared loads.  The partial dot products of a lane's keys x GT heads
+//     finish with one butterfly reduce-scatter inside its LPK-lane group;
+//     P.V accumulates per lane and the key groups are summed once at the end.
+//   * int8 with two or more heads per CTA, where unpacking makes each key's
+//     work long and registers scarce: each partial score goes to shared
+//     memory as it is formed and lane i sums row i of that transpose, and
+//     the P.V weights are read back from shared memory as (p, p) pairs
+//     (measured 68% -> 77% of the HBM copy bandwidth on the Gemma4 sliding
+//     layer with int8 KV).
 //   * The running max is warp-uniform, so o and l are rescaled only in
 //     stages where a max grows.
 //   * Keys outside [lo, pos] in the first/last block are masked with a
@@ -433,29 +439,43 @@ __device__ __forceinline__ void decode_body(const DecodeParams &p, const CUtenso
         // all of this warp's keys hold data and lie in [lo, pos]
         const bool all_in = jw >= kr.lo && jw + KPW - 1 <= kr.pos && (vmask & wmask) == wmask;
         // ---- scores of this lane's KPL keys for the GT heads
-        float acc[NV];
-        if constexpr (INT8 && GT >= 2 && KPL % 2 == 0) {
-            // two keys at a time: twice the independent multiply-add chains
-            // in flight (the int8 unpack makes each chain long)
+        float s;
+        if constexpr (C::RED) {
+            // Each partial score goes to shared memory as soon as it is
+            // formed (row v = value v, column = lane within the key group;
+            // 4-float chunks xor-swizzled by row, so that the stores and the
+            // chunked row reads are free of bank conflicts); lane dl then
+            // sums row dl.
+            constexpr int RPB = 32 / LPK;  // rows per 32 banks
+            auto swz = [](int v) { return (v / RPB) & (LPK / 4 - 1); };
+            float *rd = red + (warp * KG + kg) * C::RED_KG;
+            auto put = [&](int v, float x) { rd[v * LPK + (dl ^ (swz(v) << 2))] = x; };
 #pragma unroll
-            for (int r = 0; r < KPL; r += 2) {
-                float2 ka[NPR], kb2[NPR];
-                load_chunk<INT8, C::CB>(kt + lane_base + koff(r), ka);
-                load_chunk<INT8, C::CB>(kt + lane_base + koff(r + 1), kb2);
+            for (int r = 0; r < KPL; ++r) {
+                float2 kf[NPR];
+                load_chunk<INT8, C::CB>(kt + lane_base + koff(r), kf);
 #pragma unroll
                 for (int h = 0; h < GT; ++h) {
-                    float2 a = __fmul2_rn(qf[h][0], ka[0]);
-                    float2 c = __fmul2_rn(qf[h][0], kb2[0]);
+                    float2 a = __fmul2_rn(qf[h][0], kf[0]);
 #pragma unroll
-                    for (int e = 1; e < NPR; ++e) {
-                        a = __ffma2_rn(qf[h][e], ka[e], a);
-                        c = __ffma2_rn(qf[h][e], kb2[e], c);
-                    }
-                    acc[h * KPL + r] = a.x + a.y;
-                    acc[h * KPL + r + 1] = c.x + c.y;
+                    for (int e = 1; e < NPR; ++e)
+                        a = __ffma2_rn(qf[h][e], kf[e], a);
+                    put(h * KPL + r, a.x + a.y);
                 }
             }
+            __syncwarp();
+            const float4 *row = reinterpret_cast<const float4 *>(rd + dl * LPK);
+            const int sw = swz(dl);
+            float t0 = 0.f, t1 = 0.f;
+#pragma unroll
+            for (int c = 0; c < LPK / 4; ++c) {
+                const float4 x = row[c ^ sw];
+                t0 += x.x + x.y;
+                t1 += x.z + x.w;
+            }
+            s = t0 + t1;
         } else {
+            float acc[NV];
 #pragma unroll
             for (int r = 0; r < KPL; ++r) {
                 float2 kf[NPR];
@@ -469,30 +489,6 @@ __device__ __forceinline__ void decode_body(const DecodeParams &p, const CUtenso
                     acc[h * KPL + r] = a.x + a.y;
                 }
             }
-        }
-        float s;
-        if constexpr (C::RED) {
-            // row v holds value v's LPK partial sums; 4-float chunks are
-            // xor-swizzled by row so that both the row-wise stores and the
-            // chunked row reads are free of bank conflicts
-            constexpr int RPB = 32 / LPK;  // rows per 32 banks
-            auto swz = [](int v) { return (v / RPB) & (LPK / 4 - 1); };
-            float *rd = red + (warp * KG + kg) * C::RED_KG;
-#pragma unroll
-            for (int v = 0; v < NV; ++v)
-                rd[v * LPK + (((dl >> 2) ^ swz(v)) << 2) + (dl & 3)] = acc[v];
-            __syncwarp();
-            const float4 *row = reinterpret_cast<const float4 *>(rd + dl * LPK);
-            const int sw = swz(dl);
-            float t0 = 0.f, t1 = 0.f;
-#pragma unroll
-            for (int c = 0; c < LPK / 4; ++c) {
-                const float4 x = row[c ^ sw];
-                t0 += x.x + x.y;
-                t1 += x.z + x.w;
-            }
-            s = t0 + t1;
-        } else {
             s = reduce_scatter<NV, LPK>(acc, lane);
         }
         const int jm = jst + km;

@@ -96,20 +96,13 @@ constexpr int CHUNK = 16384;      // 128 keys x 64 dims bf16 (one swizzled colum
 constexpr int CTRL = 1024;        // barriers, TMEM address, flags, exchange
 constexpr int QBUF = 8192;        // Q^T of one item: up to 4 columns x 16 heads x 128 B
 constexpr int QBYTES = 2 * QBUF;  // two Q^T buffers
-constexpr int PBYTES = 16384;     // P^T: 2 buffers x (hi, lo) x 2 columns x 16 heads x 128 B
+constexpr int PBYTES = 16384;     // P^T: 2 buffers x (hi, lo) x 128 keys x 16 heads x 2 B
 constexpr int RING_OFF = CTRL + QBYTES + PBYTES;
 constexpr uint32_t TMEM_COLS = 128;
 
 // TMEM columns: S^T of tile parity sb, O^T half `half` of item parity ob.
 __device__ __forceinline__ uint32_t s_col(int sb) { return sb * 16; }
 __device__ __forceinline__ uint32_t o_col(int ob, int half) { return 32 + ob * 32 + half * 16; }
-
-// Byte offset of element (row, col) of a [rows][64] bf16 column stored with
-// the 128-byte swizzle (16-byte chunk index XOR row % 8).
-__device__ __forceinline__ int swz(int row, int col)
-{
-    return row * 128 + ((((col >> 3) ^ row) & 7) << 4) + (col & 7) * 2;
-}
 
 struct Flags {
     volatile int *abort;
@@ -772,7 +765,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         // blocks (only the block holding the window start and the block
         // holding pos can have them), lane 0 then issues the MMAs, which
         // accumulate into the item's O^T from its second tile on.
-        constexpr uint32_t IDESC_PV = umma_idesc_bf16(128, NPAD, true, false);
+        constexpr uint32_t IDESC_PV = umma_idesc_bf16(128, NPAD, true, true);
         const uint32_t p_base = smem_u32(ps), u_base = smem_u32(units);
         int i_g = 0, j = 0, k = 0;
         bool ok = true;
@@ -845,9 +838,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                                 // 8-key groups 1 KB apart
                                 const uint64_t a =
                                     umma_smem_desc(u_base + slot * UNIT + kk * 2048, CHUNK, 1024);
-                                const uint64_t bd = umma_smem_desc(
-                                    p_base + sb * 8192 + pass * 4096 + (kk >> 2) * 2048 + (kk & 3) * 32,
-                                    16, 1024);
+                                // P^T: MN-major, one 32-byte row of 16 heads
+                                // per key, 8-key groups 256 B apart
+                                const uint64_t bd = umma_smem_desc_sw32(
+                                    p_base + sb * 8192 + pass * 4096 + kk * 512, 4096, 256);
                                 umma_bf16(tmem + o_col(ob, h), a, bd, IDESC_PV,
                                           i > lt0 || pass > 0 || kk > 0);
                             }
@@ -982,17 +976,46 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                         al[h4] = a2.x; al[h4 + 1] = a2.y;
                     }
                 }
-                uint8_t *pb = ps + sb * 8192 + (t >> 6) * 2048;
+                // P^T is MN-major with the 32-byte swizzle: key t's 16 heads
+                // are one 32-byte row (8-key groups of 256 B), its two 16-byte
+                // halves swapped in rows 4-7 of a group; the thread writes
+                // its row with one or two vector stores
+                uint8_t *pb = ps + sb * 8192 + (t >> 3) * 256 + (t & 7) * 32;
+                const int sw = (t >> 2) & 1;
+                uint32_t whi[GP / 2], wlo[GP / 2];
 #pragma unroll
-                for (int h = 0; h < GP; ++h) {
-                    const float pr = sc[h] == -INFINITY ? 0.f : fast_exp2(sc[h] - mr[h]);
-                    lpart[h] = rescale ? fmaf(lpart[h], al[h], pr) : lpart[h] + pr;
-                    const __nv_bfloat16 hi = __float2bfloat16_rn(pr);
-                    *reinterpret_cast<__nv_bfloat16 *>(pb + swz(h, t & 63)) = hi;
-                    if (precise)
-                        *reinterpret_cast<__nv_bfloat16 *>(pb + 4096 + swz(h, t & 63)) =
-                            __float2bfloat16_rn(pr - __bfloat162float(hi));
+                for (int h = 0; h < GP; h += 2) {
+                    float pr2[2];
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        pr2[e] = sc[h + e] == -INFINITY ? 0.f : fast_exp2(sc[h + e] - mr[h + e]);
+                        lpart[h + e] = rescale ? fmaf(lpart[h + e], al[h + e], pr2[e])
+                                               : lpart[h + e] + pr2[e];
+                    }
+                    const __nv_bfloat162 hi = __floats2bfloat162_rn(pr2[0], pr2[1]);
+                    whi[h / 2] = *reinterpret_cast<const uint32_t *>(&hi);
+                    if (precise) {
+                        const float2 hf = __bfloat1622float2(hi);
+                        const __nv_bfloat162 lo =
+                            __floats2bfloat162_rn(pr2[0] - hf.x, pr2[1] - hf.y);
+                        wlo[h / 2] = *reinterpret_cast<const uint32_t *>(&lo);
+                    }
                 }
+                auto put_row = [&](uint8_t *row, const uint32_t(&w)[GP / 2]) {
+                    if constexpr (GP >= 8) {
+#pragma unroll
+                        for (int c = 0; c < GP / 8; ++c)
+                            *reinterpret_cast<uint4 *>(row + ((c ^ sw) << 4)) =
+                                make_uint4(w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
+                    } else if constexpr (GP == 4) {
+                        *reinterpret_cast<uint2 *>(row + (sw << 4)) = make_uint2(w[0], w[1]);
+                    } else {
+                        *reinterpret_cast<uint32_t *>(row + (sw << 4)) = w[0];
+                    }
+                };
+                put_row(pb, whi);
+                if (precise)
+                    put_row(pb + 4096, wlo);
                 fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0)

@@ -118,20 +118,28 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, unsign
 // try_wait without a suspend-time hint returns after a short, system-defined
 // interval, so a completed phase is seen within that interval instead of
 // after a wake-up from a longer sleep.  Bounded like mbar_wait.
+__device__ __forceinline__ bool mbar_try_wait_short(uint64_t *bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
 __device__ __forceinline__ bool mbar_wait_spin(uint64_t *bar, uint32_t parity, unsigned int *err,
                                                uint64_t limit_ns = 2000000000ull)
 {
+    // the common case, a phase already complete, costs no timer read
+    if (mbar_try_wait_short(bar, parity))
+        return true;
     const uint64_t t0 = global_timer_ns();
     for (uint32_t it = 1;; ++it) {
-        uint32_t ok;
-        asm volatile(
-            "{\n\t.reg .pred p;\n\t"
-            "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-            "selp.u32 %0, 1, 0, p;\n\t}"
-            : "=r"(ok)
-            : "r"(smem_u32(bar)), "r"(parity)
-            : "memory");
-        if (ok)
+        if (mbar_try_wait_short(bar, parity))
             return true;
         if ((it & 255u) == 0 && global_timer_ns() - t0 > limit_ns) {
             record_error(err, PKV_DEV_TIMEOUT);
@@ -318,6 +326,19 @@ __device__ __forceinline__ uint64_t umma_smem_desc(uint32_t saddr, uint32_t lbo,
     d |= static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32;
     d |= 1ull << 46;
     d |= 2ull << 61;
+    return d;
+}
+
+// The same with the 32-byte swizzle (mode 6): 16-byte chunk bit 4 of the
+// address XOR address bit 7, i.e. rows of 32 bytes in 256-byte atoms.
+__device__ __forceinline__ uint64_t umma_smem_desc_sw32(uint32_t saddr, uint32_t lbo, uint32_t sbo)
+{
+    uint64_t d = 0;
+    d |= static_cast<uint64_t>((saddr >> 4) & 0x3FFFu);
+    d |= static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16;
+    d |= static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32;
+    d |= 1ull << 46;
+    d |= 6ull << 61;
     return d;
 }
 
