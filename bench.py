@@ -59,6 +59,10 @@ def parse_args():
                     help="skip the per-workload lines (every config, the six-layer step, "
                          "the oracle at all threads and at one thread)")
     ap.add_argument("--per-config-steps", type=int, default=100)
+    ap.add_argument("--record-traffic", metavar="RAW_CSV", default=None,
+                    help="write profiles/traffic.json's entry for --config from an ncu capture of "
+                         "its decode kernel on --batch sequences (the raw page as CSV: ncu -i "
+                         "REPORT --page raw --csv), scaled to the full batch by algorithmic bytes")
     ap.add_argument("--chunk-only", type=int, default=0,
                     help="time only the chunk attention (q_len > 1) with chunks of this many "
                          "tokens on --config's shapes (prints that measurement, not a bench line)")
@@ -116,6 +120,59 @@ def recorded_traffic(config: str):
     except Exception:
         pass
     return None
+
+
+def layout_bytes(spec) -> int:
+    """Algorithmic bytes of one decode of the workload (KV once, q, out),
+    from its layout alone (no K/V values are drawn)."""
+    layout = synth.make_layout(spec, np.random.default_rng(spec.seed))
+    d = bytes_model.decode_bytes(spec, layout.seq_lens, layout.block_table)
+    return int(d["kv"] + d["q"] + d["out"])
+
+
+def record_traffic(args) -> dict:
+    """profiles/traffic.json entry of --config: DRAM bytes of the captured
+    launch (dram__bytes_read.sum + dram__bytes_write.sum, one launch) times
+    full-batch / captured-batch algorithmic bytes, keyed by the kernel's
+    source hash."""
+    import csv
+    with open(args.record_traffic) as f:
+        rows = [r for r in csv.reader(f)]
+    hdr, vals = rows[0], rows[2]
+    col = {h: i for i, h in enumerate(hdr)}
+    unit = {"byte": 1, "Kbyte": 1e3, "Mbyte": 1e6, "Gbyte": 1e9}
+
+    def metric(name):
+        return float(vals[col[name]].replace(",", "")) * unit[rows[1][col[name]]]
+
+    dram = metric("dram__bytes_read.sum") + metric("dram__bytes_write.sum")
+    kernel = vals[col["Kernel Name"]]
+    family = "tensor_core" if "decode_tc_kernel" in kernel else "cuda_core"
+    full = synth.CONFIGS[args.config]
+    cap = workload_spec(args)
+    a_cap, a_full = layout_bytes(cap), layout_bytes(full)
+    entry = {
+        "kernel_family": family,
+        "sources_sha": csrc_sha(KERNEL_SOURCES[family]),
+        "bytes_per_launch": int(round(dram * a_full / a_cap)),
+        "kernel": kernel.split("(")[0].strip(),
+        "source": f"ncu capture of one launch on {args.config} with batch {cap.batch} "
+                  f"(dram__bytes_read.sum + dram__bytes_write.sum), scaled to batch "
+                  f"{full.batch} by the ratio of algorithmic bytes",
+        "capture_dram_bytes": int(round(dram)),
+        "capture_algorithmic_bytes": a_cap,
+    }
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+    except Exception:
+        d = {}
+    d[args.config] = entry
+    with open(path, "w") as f:
+        json.dump(d, f, indent=1, sort_keys=True)
+        f.write("\n")
+    return entry
 
 
 def workload_desc(spec) -> str:
@@ -1014,6 +1071,9 @@ def main():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.record_traffic:
+        print(json.dumps(record_traffic(args)), flush=True)
+        return 0
     if args.impl == "reference":
         line = run_reference(args, rank)
         if line is not None:

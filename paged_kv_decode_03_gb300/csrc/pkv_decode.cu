@@ -714,17 +714,25 @@ __device__ __forceinline__ void decode_body(const DecodeParams &p, const CUtenso
 // registers, so that five CTAs fit an SM (left to itself the compiler takes
 // 81 for the int8 head_dim-128 instance, which then runs four CTAs per SM and
 // measured 6% slower).  The int8 two-head instances are bounded to three
-// CTAs per SM (at most 136 registers), which their shared memory allows
-// anyway; the others carry an explicit bound of one CTA, with which the
-// compiler takes more registers than without (the bf16 two-head instance
-// then runs four CTAs per SM instead of five and measured 2-3% faster on
-// the Gemma4 sliding shape).
+// CTAs per SM (at most 136 registers; 1% faster than the compiler's choice on
+// the Gemma4 sliding layer with int8 KV).  The others keep the compiler's
+// choice: an explicit bound of one CTA makes it take more registers (the
+// bf16 two-head instance then runs four CTAs per SM instead of five and
+// measured 1-2% slower on the Gemma4 sliding layer).
 template <int D, int GT, bool INT8>
-__global__ void __launch_bounds__(THREADS, (INT8 && GT == 2) ? 3 : 1)
-    decode_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmk,
-                  const __grid_constant__ CUtensorMap tmv)
+__global__ void __launch_bounds__(THREADS) decode_kernel(const DecodeParams p,
+                                                         const __grid_constant__ CUtensorMap tmk,
+                                                         const __grid_constant__ CUtensorMap tmv)
 {
     decode_body<D, GT, INT8>(p, &tmk, &tmv);
+}
+
+template <int D>
+__global__ void __launch_bounds__(THREADS, 3) decode_kernel_i8x2(const DecodeParams p,
+                                                                const __grid_constant__ CUtensorMap tmk,
+                                                                const __grid_constant__ CUtensorMap tmv)
+{
+    decode_body<D, 2, true>(p, &tmk, &tmv);
 }
 
 template <int D, bool INT8>
@@ -740,6 +748,8 @@ constexpr auto decode_entry()
 {
     if constexpr (GT == 1)
         return decode_kernel_1h<D, INT8>;
+    else if constexpr (GT == 2 && INT8)
+        return decode_kernel_i8x2<D>;
     else
         return decode_kernel<D, GT, INT8>;
 }
