@@ -52,7 +52,8 @@ constexpr int PF_CTRL = 1024;
 constexpr int PF_QCHUNK = PF_ROWS * 128;   // 128 rows x 64 dims bf16
 constexpr int PF_KCHUNK = PF_KEYS * 128;   // 64 keys x 64 dims bf16
 constexpr int PF_PROW = PF_ROWS * 128;     // 128 rows x 64 keys bf16
-constexpr int PF_PBYTES = 2 * PF_PROW;     // P as bf16, and its bf16 residual (fp32 output)
+// P: two bf16 buffers (bf16 output), or one P and its bf16 residual (fp32 output)
+constexpr int PF_PBYTES = 2 * PF_PROW;
 constexpr int PF_MAX_BUF = 4;
 
 __device__ __forceinline__ int pf_swz(int row, int chunk16)
@@ -110,9 +111,13 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
     uint64_t *kv_empty = kv_full + PF_MAX_BUF;               // [PF_MAX_BUF]
     uint64_t *s_full = kv_full + 2 * PF_MAX_BUF;             // [2]
     uint64_t *s_empty = s_full + 2;                          // [2]
-    uint64_t *p_full = s_full + 4;
-    uint64_t *pv_done = s_full + 5;
-    uint64_t *q_full = s_full + 6;
+    uint64_t *p_full = s_full + 4;   // [2] P of a tile written
+    uint64_t *pv_done = s_full + 6;  // [2] a tile's P.V complete
+    uint64_t *q_full = s_full + 8;
+    // separate K and V: K slot i is free once the scores have read it, V
+    // slot i once the P.V has (kv_full / kv_empty then serve the K slots)
+    uint64_t *v_full = s_full + 9;                           // [PF_MAX_BUF]
+    uint64_t *v_empty = v_full + PF_MAX_BUF;                 // [PF_MAX_BUF]
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + 256);
     volatile int *abort_f = reinterpret_cast<volatile int *>(sm + 260);
     uint8_t *qs = sm + PF_CTRL;
@@ -124,6 +129,9 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
     const int tile = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
     const bool alias = p.alias != 0;
     const int NB = p.num_buffers;
+    // P buffers: tile i's P in buffer i % NPB; with fp32 output the second
+    // half holds the residual of the one buffer
+    const int NPB = p.out_f32 ? 1 : 2;
     const int KVB = alias ? KV_TILE : 2 * KV_TILE;  // one buffer: K [+ V]
 
     if (threadIdx.x == 0 && tile == 0 && kvh == 0) {
@@ -143,13 +151,17 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
         for (int i = 0; i < PF_MAX_BUF; ++i) {
             mbar_init(&kv_full[i], 1);
             mbar_init(&kv_empty[i], 1);
+            mbar_init(&v_full[i], 1);
+            mbar_init(&v_empty[i], 1);
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&s_full[i], 1);
             mbar_init(&s_empty[i], 4);
         }
-        mbar_init(p_full, 4);
-        mbar_init(pv_done, 1);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&p_full[i], 4);
+            mbar_init(&pv_done[i], 1);
+        }
         mbar_init(q_full, 1);
         *abort_f = 0;
         fence_barrier_init();
@@ -200,23 +212,35 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
                     record_error(p.err, PKV_DEV_BAD_BLOCK);
                 row[t] = valid ? phys * kBlock : p.num_blocks * kBlock;  // zero fill
             }
-            if (lane == 0)
-                mbar_arrive_expect_tx(&kv_full[buf], KVB);
-            __syncwarp();
-            // lanes (which, t, c): which = K or V, block t, 64-dim chunk c
-            const int nbox = (alias ? 1 : 2) * 4 * NCH;
-            for (int k = lane; k < nbox; k += 32) {
-                const int which = k / (4 * NCH), t = (k / NCH) & 3, c = k % NCH;
-                const int rt = t == 0 ? row[0] : t == 1 ? row[1] : t == 2 ? row[2] : row[3];
-                uint8_t *dst = kvs + buf * KVB + which * KV_TILE + c * PF_KCHUNK + t * 2048;
-                tma_load_3d(dst, which ? &tmv : &tmk, c * 64, kvh, rt, &kv_full[buf], pol);
+            // lanes (t, c): block t, 64-dim chunk c of the K (or K == V) tile,
+            // then of the V tile once its slot is free
+            const int nbox = 4 * NCH;
+            for (int which = 0; which < (alias ? 1 : 2); ++which) {
+                if (which == 1) {
+                    const bool vroom = i < NB || waitb(&v_empty[buf], ((i / NB) - 1) & 1);
+                    if (!__all_sync(FULL_MASK, vroom))
+                        break;
+                }
+                uint64_t *fullb = which ? &v_full[buf] : &kv_full[buf];
+                if (lane == 0)
+                    mbar_arrive_expect_tx(fullb, KV_TILE);
+                __syncwarp();
+                for (int k = lane; k < nbox; k += 32) {
+                    const int t = k / NCH, c = k % NCH;
+                    const int rt = t == 0 ? row[0] : t == 1 ? row[1] : t == 2 ? row[2] : row[3];
+                    uint8_t *dst = kvs + buf * KVB + which * KV_TILE + c * PF_KCHUNK + t * 2048;
+                    tma_load_3d(dst, which ? &tmv : &tmk, c * 64, kvh, rt, fullb, pol);
+                }
+                __syncwarp();
             }
             last_use = i;
-            __syncwarp();
         }
         if (lane == 0) {
-            if (last_use >= 0)
+            if (last_use >= 0) {
                 mbar_wait(&kv_full[last_use % NB], (last_use / NB) & 1, p.err, 100000000ull);
+                if (!alias)
+                    mbar_wait(&v_full[last_use % NB], (last_use / NB) & 1, p.err, 100000000ull);
+            }
             mbar_wait(q_full, 0, p.err, 100000000ull);
         }
     } else if (warp == PF_MMA_WARP) {
@@ -231,7 +255,10 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
             const int key0 = (ct.blk0 + j * 4) * kBlock;
             const int za = max(0, min(PF_KEYS, ct.lo - key0));
             const int zb = max(0, min(PF_KEYS, ct.last + 1 - key0));
-            bool go = waitb(p_full, j & 1);
+            const int pbuf = j % NPB;
+            bool go = waitb(&p_full[pbuf], (j / NPB) & 1);
+            if (!alias)
+                go = go && waitb(&v_full[j % NB], (j / NB) & 1);
             if (!__all_sync(FULL_MASK, go))
                 return false;
             uint8_t *vt = kvs + (j % NB) * KVB + (alias ? 0 : KV_TILE);
@@ -251,19 +278,33 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
                 for (int pass = 0; pass < (p.out_f32 ? 2 : 1); ++pass) {
 #pragma unroll
                     for (int kk = 0; kk < PF_KEYS / 16; ++kk) {
-                        const uint64_t a = umma_smem_desc(p_base + pass * PF_PROW + kk * 32, 16, 1024);
+                        const uint64_t a = umma_smem_desc(
+                            p_base + (pbuf + pass) * PF_PROW + kk * 32, 16, 1024);
                         const uint64_t bv = umma_smem_desc(v_base + kk * 2048, PF_KCHUNK, 1024);
                         umma_bf16(tmem + O_COL, a, bv, IDESC_PV, j > 0 || pass > 0 || kk > 0);
                     }
                 }
-                umma_commit(pv_done);
-                umma_commit(&kv_empty[j % NB]);
+                umma_commit(&pv_done[pbuf]);
+                umma_commit(alias ? &kv_empty[j % NB] : &v_empty[j % NB]);
             }
             __syncwarp();
             return true;
         };
         for (int i = 0; i < ct.T && ok; ++i) {
             const int buf = i % NB, sb = i & 1;
+            // The previous tile's P.V goes first when this tile's data has not
+            // landed yet: the softmax waits for that P.V, not for these loads.
+            bool prev_done = i == 0;
+            if (!prev_done) {
+                const bool landed = __shfl_sync(
+                    FULL_MASK, lane == 0 ? mbar_test(&kv_full[buf], (i / NB) & 1) : false, 0);
+                if (!landed) {
+                    ok = pv(i - 1);
+                    prev_done = true;
+                    if (!ok)
+                        break;
+                }
+            }
             ok = waitb(&kv_full[buf], (i / NB) & 1);
             ok = ok && (i < 2 || waitb(&s_empty[sb], ((i >> 1) - 1) & 1));
             ok = __all_sync(FULL_MASK, ok);
@@ -281,9 +322,11 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
                     umma_bf16(tmem + sb * PF_KEYS, a, bk, IDESC_QK, kk > 0);
                 }
                 umma_commit(&s_full[sb]);
+                if (!alias)
+                    umma_commit(&kv_empty[buf]);  // the K slot is free once read
             }
             __syncwarp();
-            if (i >= 1)
+            if (!prev_done)
                 ok = pv(i - 1);
         }
         if (ok && ct.T > 0)
@@ -329,9 +372,9 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
                 s[k] = ok ? s[k] * qk : -INFINITY;
                 mt = fmaxf(mt, s[k]);
             }
-            // the previous tile's P.V has read the P buffer (and O is current)
-            if (i >= 1)
-                live = live && waitb(pv_done, (i - 1) & 1);
+            // this tile's P buffer was last read by the P.V of tile i - NPB
+            if (i >= NPB)
+                live = live && waitb(&pv_done[(i - NPB) % NPB], ((i - NPB) / NPB) & 1);
             live = __all_sync(FULL_MASK, live);
             // a new reference max for this row when a score exceeds the old by
             // more than 2^8; O's row (through the previous tile) is scaled in
@@ -340,6 +383,11 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
             // and the other rows scale by 1
             const bool grow = mt > m + 8.f;
             const float alpha = !grow ? 1.f : (m == -INFINITY ? 0.f : fast_exp2(m - mt));
+            if (__any_sync(FULL_MASK, grow && m != -INFINITY) && i >= 1 && live) {
+                // O through the previous tile must be complete before scaling
+                live = waitb(&pv_done[(i - 1) % NPB], ((i - 1) / NPB) & 1);
+                live = __all_sync(FULL_MASK, live);
+            }
             if (__any_sync(FULL_MASK, grow && m != -INFINITY) && i >= 1 && live) {
                 tc_fence_after();
 #pragma unroll
@@ -376,7 +424,8 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
                     __nv_bfloat162 l2 = __floats2bfloat162_rn(p0 - back.x, p1 - back.y);
                     wl[e] = *reinterpret_cast<uint32_t *>(&l2);
                 }
-                *reinterpret_cast<uint4 *>(ps + pf_swz(r, c16)) = make_uint4(w[0], w[1], w[2], w[3]);
+                uint8_t *pbuf = ps + (i % NPB) * PF_PROW;
+                *reinterpret_cast<uint4 *>(pbuf + pf_swz(r, c16)) = make_uint4(w[0], w[1], w[2], w[3]);
                 if (p.out_f32)
                     *reinterpret_cast<uint4 *>(ps + PF_PROW + pf_swz(r, c16)) =
                         make_uint4(wl[0], wl[1], wl[2], wl[3]);
@@ -384,11 +433,11 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0)
-                mbar_arrive(p_full);
+                mbar_arrive(&p_full[i % NPB]);
         }
         // ---- the row's output: O / l after the last P.V
         if (ct.T > 0)
-            live = live && waitb(pv_done, (ct.T - 1) & 1);
+            live = live && waitb(&pv_done[(ct.T - 1) % NPB], ((ct.T - 1) / NPB) & 1);
         tc_fence_after();
         const float inv = l > 0.f ? 1.f / l : 0.f;
         const size_t orow = (static_cast<size_t>(ct.q0 + ct.t0 + t) * p.num_q_heads +
