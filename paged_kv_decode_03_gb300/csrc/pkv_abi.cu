@@ -641,6 +641,7 @@ PKV_API int paged_prefill_attention(const void *q, const int32_t *q_start, int32
     if (int rc = encode_chunk_q_map(&tmq, q, total_q, num_q_heads, pool->head_dim, group))
         return rc;
     PrefillParams p{};
+    p.q = static_cast<const uint16_t *>(q);
     p.q_start = q_start;
     p.block_table = block_table;
     p.seq_lens = seq_lens;

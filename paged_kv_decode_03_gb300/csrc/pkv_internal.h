@@ -55,6 +55,7 @@ struct DecodeParams {
 
 // Parameters of the chunk (q_len > 1) attention kernel.
 struct PrefillParams {
+    const uint16_t *q;        // [total][H_q][D] bf16
     const int32_t *q_start;   // [B + 1] first query row of each sequence's chunk
     const int32_t *block_table;
     const int32_t *seq_lens;

@@ -16,12 +16,16 @@
 // is 128 rows, row r = (token r / G, query head kvh * G + r % G) of the
 // chunk: the rows of one kv head's group share every K/V byte the CTA
 // reads.  The CTA walks the 64-key tiles of [lo(first token), last token]:
-//   warp 5 (one thread): TMA loads of the tile's Q (once) and of each key
-//     tile's K and V blocks (boxes of 16 rows x 64 dims, 128-byte swizzle)
-//     into a ring of buffers;
+//   warps 0-3 first copy their rows of Q into TMEM (thread r = row r = TMEM
+//     lane r; zeros for rows past the chunk): the score MMAs take their A
+//     operand from there, which leaves shared memory to the K/V slots;
+//   warp 5: TMA loads of each key tile's K and V blocks (boxes of 16 rows x
+//     64 dims, 128-byte swizzle) into separate K and V slots, a K slot being
+//     free once the scores have read it and a V slot once the P.V has;
 //   warp 4 (one thread): S = Q K^T (M = 128 rows, N = 64 keys, K = 16) into
 //     one of two TMEM score buffers, then O += P V (M = 128, N = head_dim,
-//     K = 16 keys) into TMEM, accumulating over the key tiles; the whole
+//     K = 16 keys) into TMEM, accumulating over the key tiles; the previous
+//     tile's P.V goes first when this tile's K has not landed yet; the whole
 //     warp first zeroes V rows of keys no row may see inside loaded blocks,
 //     so that no stale value (not even a NaN) meets a zero probability;
 //   warps 0-3 (thread r = row r = TMEM lane r): load the row's 64 scores,
@@ -29,12 +33,13 @@
 //     sum in fp32 (the max changes only when a score exceeds it by more
 //     than 2^8; O's row is then scaled in TMEM by the thread that owns it,
 //     after the previous tile's P.V), write the row's probabilities as bf16
-//     (K-major, swizzled) for the P.V MMA, and finally read O's row, divide
-//     by the sum and store it.
+//     (K-major, swizzled; two P buffers for bf16 outputs) for the P.V MMA,
+//     and finally read O's row, divide by the sum and store it.
 #include <cuda_bf16.h>
 #include <math.h>
 
 #include <atomic>
+#include <type_traits>
 
 #include "pkv_device.cuh"
 #include "pkv_internal.h"
@@ -49,7 +54,6 @@ constexpr int PF_THREADS = 192;    // warps 0-3 softmax, 4 MMA, 5 TMA
 constexpr int PF_MMA_WARP = 4;
 constexpr int PF_TMA_WARP = 5;
 constexpr int PF_CTRL = 1024;
-constexpr int PF_QCHUNK = PF_ROWS * 128;   // 128 rows x 64 dims bf16
 constexpr int PF_KCHUNK = PF_KEYS * 128;   // 64 keys x 64 dims bf16
 constexpr int PF_PROW = PF_ROWS * 128;     // 128 rows x 64 keys bf16
 // P: two bf16 buffers (bf16 output), or one P and its bf16 residual (fp32 output)
@@ -101,8 +105,12 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
     static_assert(D == 64 || D == 128 || D == 256, "head_dim");
     constexpr int NCH = D / 64;                 // 64-dim chunks
     constexpr int KV_TILE = NCH * PF_KCHUNK;    // one K (or V) tile
-    constexpr uint32_t TMEM_COLS = D + 2 * PF_KEYS <= 256 ? 256 : 512;
-    constexpr uint32_t O_COL = 2 * PF_KEYS;     // S buffers at 0 and 64, O after them
+    // TMEM: S buffers at 0 and 64, O (D fp32 columns), then Q (D / 2 columns
+    // of bf16 pairs: the A operand of the score MMAs, read from TMEM so that
+    // shared memory holds a third K/V tile instead of Q)
+    constexpr uint32_t TMEM_COLS = 2 * PF_KEYS + D + D / 2 <= 256 ? 256 : 512;
+    constexpr uint32_t O_COL = 2 * PF_KEYS;
+    constexpr uint32_t Q_COL = O_COL + D;
 
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
@@ -120,8 +128,7 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
     uint64_t *v_empty = v_full + PF_MAX_BUF;                 // [PF_MAX_BUF]
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + 256);
     volatile int *abort_f = reinterpret_cast<volatile int *>(sm + 260);
-    uint8_t *qs = sm + PF_CTRL;
-    uint8_t *ps = qs + NCH * PF_QCHUNK;
+    uint8_t *ps = sm + PF_CTRL;
     uint8_t *kvs = ps + PF_PBYTES;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -162,7 +169,7 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
             mbar_init(&p_full[i], 4);
             mbar_init(&pv_done[i], 1);
         }
-        mbar_init(q_full, 1);
+        mbar_init(q_full, 4);  // the softmax warps, once Q is in TMEM
         *abort_f = 0;
         fence_barrier_init();
     }
@@ -186,13 +193,9 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
         const uint64_t pol = policy_evict_first();
         int last_use = -1;
         if (lane == 0) {
-            prefetch_tensormap(&tmq);
             prefetch_tensormap(&tmk);
-            mbar_arrive_expect_tx(q_full, NCH * PF_QCHUNK);
-#pragma unroll
-            for (int c = 0; c < NCH; ++c)
-                tma_load_3d(qs + c * PF_QCHUNK, &tmq, c * 64, kvh * G, ct.q0 + ct.t0, q_full,
-                            policy_evict_last());
+            if (!alias)
+                prefetch_tensormap(&tmv);
         }
         TableCursor tcur;
         tcur.init(p.block_table + static_cast<size_t>(b) * p.max_blocks, ct.blk0, ct.nblk,
@@ -241,14 +244,14 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
                 if (!alias)
                     mbar_wait(&v_full[last_use % NB], (last_use / NB) & 1, p.err, 100000000ull);
             }
-            mbar_wait(q_full, 0, p.err, 100000000ull);
         }
     } else if (warp == PF_MMA_WARP) {
         // ---------------------------------------------------------- MMAs
         constexpr uint32_t IDESC_QK = umma_idesc_bf16(PF_ROWS, PF_KEYS, false, false);
         constexpr uint32_t IDESC_PV = umma_idesc_bf16(PF_ROWS, D, false, true);
-        const uint32_t q_base = smem_u32(qs), p_base = smem_u32(ps), kv_base = smem_u32(kvs);
+        const uint32_t p_base = smem_u32(ps), kv_base = smem_u32(kvs);
         bool ok = waitb(q_full, 0);
+        tc_fence_after();
         auto pv = [&](int j) {
             // V rows of keys no row may see (before lo, after the last token)
             // inside this tile's loaded blocks: zero them, so 0 * stale = 0
@@ -315,11 +318,9 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
                 const uint32_t k_base = kv_base + buf * KVB;
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint64_t a = umma_smem_desc(
-                        q_base + (kk >> 2) * PF_QCHUNK + (kk & 3) * 32, 16, 1024);
                     const uint64_t bk = umma_smem_desc(
                         k_base + (kk >> 2) * PF_KCHUNK + (kk & 3) * 32, 16, 1024);
-                    umma_bf16(tmem + sb * PF_KEYS, a, bk, IDESC_QK, kk > 0);
+                    umma_bf16_ts(tmem + sb * PF_KEYS, tmem + Q_COL + kk * 8, bk, IDESC_QK, kk > 0);
                 }
                 umma_commit(&s_full[sb]);
                 if (!alias)
@@ -340,6 +341,29 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
         const int pos = ct.len - ct.n + ct.t0 + t;
         const int lo_r = p.window > 0 ? max(0, pos - p.window) : 0;
         const float qk = p.qk_scale_log2;
+        // ---- this row of Q into TMEM (zeros for rows past the chunk): the
+        // score MMAs read their A operand there
+        {
+            const uint4 *qrow = reinterpret_cast<const uint4 *>(
+                p.q + (static_cast<size_t>(ct.q0 + ct.t0 + t) * p.num_q_heads + kvh * G + r % G) * D);
+#pragma unroll
+            for (int c0 = 0; c0 < D / 2; c0 += 16) {  // 16 columns = 32 dims = four 16-byte loads
+                float v[16];
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const uint4 u = valid ? __ldg(qrow + c0 / 4 + k) : make_uint4(0u, 0u, 0u, 0u);
+                    v[4 * k] = __uint_as_float(u.x);
+                    v[4 * k + 1] = __uint_as_float(u.y);
+                    v[4 * k + 2] = __uint_as_float(u.z);
+                    v[4 * k + 3] = __uint_as_float(u.w);
+                }
+                tmem_st<16>(lane_base + Q_COL + c0, v);
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(q_full);
+        }
         float m = -INFINITY, l = 0.f;
         bool live = true;
         for (int i = 0; i < ct.T; ++i) {
@@ -364,13 +388,24 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
                 mbar_arrive(&s_empty[sb]);
             const int key0 = (ct.blk0 + i * 4) * kBlock;
             float mt = -INFINITY;
+            // every key of the tile visible to this row: no per-key tests
+            const bool all_in = live && valid && key0 >= lo_r && key0 + PF_KEYS - 1 <= pos &&
+                                (i + 1) * 4 <= ct.nblk;
+            if (all_in) {
 #pragma unroll
-            for (int k = 0; k < PF_KEYS; ++k) {
-                const int j = key0 + k;
-                const bool ok = live && valid && j >= lo_r && j <= pos &&
-                                (j - ct.blk0 * kBlock) < ct.nblk * kBlock;
-                s[k] = ok ? s[k] * qk : -INFINITY;
-                mt = fmaxf(mt, s[k]);
+                for (int k = 0; k < PF_KEYS; ++k) {
+                    s[k] *= qk;
+                    mt = fmaxf(mt, s[k]);
+                }
+            } else {
+#pragma unroll
+                for (int k = 0; k < PF_KEYS; ++k) {
+                    const int j = key0 + k;
+                    const bool ok = live && valid && j >= lo_r && j <= pos &&
+                                    (j - ct.blk0 * kBlock) < ct.nblk * kBlock;
+                    s[k] = ok ? s[k] * qk : -INFINITY;
+                    mt = fmaxf(mt, s[k]);
+                }
             }
             // this tile's P buffer was last read by the P.V of tile i - NPB
             if (i >= NPB)
@@ -408,28 +443,36 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
             // probabilities of the row, written as one 128-byte swizzled row;
             // for fp32 output also the bf16 residual p - bf16(p), multiplied
             // in a second P.V pass (error near 2^-17 instead of 2^-9)
+            uint8_t *pbuf = ps + (i % NPB) * PF_PROW;
+            auto put_p = [&](auto residual) {
 #pragma unroll
-            for (int c16 = 0; c16 < PF_KEYS / 8; ++c16) {
-                uint32_t w[4], wl[4];
+                for (int c16 = 0; c16 < PF_KEYS / 8; ++c16) {
+                    uint32_t w[4], wl[4];
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const float p0 = s[c16 * 8 + 2 * e] == -INFINITY
-                                         ? 0.f : fast_exp2(s[c16 * 8 + 2 * e] - m);
-                    const float p1 = s[c16 * 8 + 2 * e + 1] == -INFINITY
-                                         ? 0.f : fast_exp2(s[c16 * 8 + 2 * e + 1] - m);
-                    l += p0 + p1;
-                    __nv_bfloat162 h2 = __floats2bfloat162_rn(p0, p1);
-                    w[e] = *reinterpret_cast<uint32_t *>(&h2);
-                    const float2 back = __bfloat1622float2(h2);
-                    __nv_bfloat162 l2 = __floats2bfloat162_rn(p0 - back.x, p1 - back.y);
-                    wl[e] = *reinterpret_cast<uint32_t *>(&l2);
+                    for (int e = 0; e < 4; ++e) {
+                        const float x0 = s[c16 * 8 + 2 * e], x1 = s[c16 * 8 + 2 * e + 1];
+                        const float p0 = x0 == -INFINITY ? 0.f : fast_exp2(x0 - m);
+                        const float p1 = x1 == -INFINITY ? 0.f : fast_exp2(x1 - m);
+                        l += p0 + p1;
+                        __nv_bfloat162 h2 = __floats2bfloat162_rn(p0, p1);
+                        w[e] = *reinterpret_cast<uint32_t *>(&h2);
+                        if constexpr (decltype(residual)::value) {
+                            const float2 back = __bfloat1622float2(h2);
+                            __nv_bfloat162 l2 = __floats2bfloat162_rn(p0 - back.x, p1 - back.y);
+                            wl[e] = *reinterpret_cast<uint32_t *>(&l2);
+                        }
+                    }
+                    *reinterpret_cast<uint4 *>(pbuf + pf_swz(r, c16)) =
+                        make_uint4(w[0], w[1], w[2], w[3]);
+                    if constexpr (decltype(residual)::value)
+                        *reinterpret_cast<uint4 *>(ps + PF_PROW + pf_swz(r, c16)) =
+                            make_uint4(wl[0], wl[1], wl[2], wl[3]);
                 }
-                uint8_t *pbuf = ps + (i % NPB) * PF_PROW;
-                *reinterpret_cast<uint4 *>(pbuf + pf_swz(r, c16)) = make_uint4(w[0], w[1], w[2], w[3]);
-                if (p.out_f32)
-                    *reinterpret_cast<uint4 *>(ps + PF_PROW + pf_swz(r, c16)) =
-                        make_uint4(wl[0], wl[1], wl[2], wl[3]);
-            }
+            };
+            if (p.out_f32)
+                put_p(std::true_type{});
+            else
+                put_p(std::false_type{});
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0)
@@ -478,7 +521,7 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
 // ------------------------------------------------------------ host side
 static size_t prefill_fixed_bytes(int head_dim)
 {
-    return 1024 + PF_CTRL + static_cast<size_t>(head_dim / 64) * PF_QCHUNK + PF_PBYTES;
+    return 1024 + PF_CTRL + PF_PBYTES;  // Q lives in TMEM
 }
 
 int prefill_num_buffers(int head_dim, int alias)
