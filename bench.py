@@ -162,7 +162,7 @@ def record_traffic(args) -> dict:
         "capture_dram_bytes": int(round(dram)),
         "capture_algorithmic_bytes": a_cap,
     }
-    path = os.path.join(ROOT, "profiles", "traffic.json")
+    path = getattr(args, "traffic_path", None) or os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as f:
             d = json.load(f)
