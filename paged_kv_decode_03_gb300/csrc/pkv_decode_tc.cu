@@ -288,6 +288,67 @@ __device__ __forceinline__ int tile_bound(int c, int W, int C)
 
 }  // namespace
 
+// Units of sequence b in the stream-K walk: its tiles (whole splits of F
+// tiles and a remainder, or one range) plus KAPPA per item, for every kv head.
+__device__ __forceinline__ int seq_units(const DecodeParams &p, int b, int F)
+{
+    int len = p.seq_lens[b];
+    const int cap = p.max_blocks * kBlock;
+    if (p.ring_blocks == 0 && len > cap)
+        len = cap;
+    int tiles = 0, ns = 1;
+    if (len > 0) {
+        const int sb = p.split_blocks;
+        const int pos = len - 1;
+        const int lo = p.window > 0 ? max(0, pos - p.window) : 0;
+        const int nblk = pos / kBlock - lo / kBlock + 1;
+        if (sb > 0) {
+            const int whole = nblk / sb, rem = nblk - whole * sb;
+            tiles = whole * F + (rem + 7) / 8;
+            ns = whole + (rem > 0 ? 1 : 0);
+        } else {
+            tiles = (nblk + 7) / 8;
+        }
+    }
+    return (tiles + KAPPA * ns) * p.num_kv_heads;
+}
+
+// The item a CTA whose units start at x processes first: the first item
+// whose real tiles reach into [x, ...), or an empty item starting there.
+// soff = the sequences' first units (prefix sums, soff[batch] = W).
+__device__ __forceinline__ int4 first_item_at(const DecodeParams &p, const int *soff, int x, int F)
+{
+    const int H = p.num_kv_heads, sb = p.split_blocks;
+    // the sequence whose units hold x, then the item whose units hold it
+    int lo_b = 0, hi_b = p.batch;
+    while (lo_b < hi_b) {
+        const int mid = (lo_b + hi_b) >> 1;
+        if (soff[mid + 1] > x)
+            hi_b = mid;
+        else
+            lo_b = mid + 1;
+    }
+    Item it;
+    it.b = lo_b;
+    it.g = 0;
+    it.s = 0;
+    it.start = soff[lo_b];
+    item_geom(p, it);
+    const int Eg = (soff[lo_b + 1] - it.start) / H;  // units per kv head
+    const int rel = x - it.start;
+    if (rel > 0) {
+        it.g = rel / Eg;
+        const int r2 = rel - it.g * Eg;
+        it.s = sb > 0 ? min(r2 / (F + KAPPA), it.nsplit - 1) : 0;
+        it.start += it.g * Eg + it.s * (F + KAPPA);
+        item_geom(p, it);
+        // x in this item's virtual tail: the CTA starts with the next item
+        if (it.start + it.T <= x && !(it.T == 0 && it.start >= x))
+            item_next(p, it);
+    }
+    return make_int4(it.b, it.g, it.s, it.start);
+}
+
 // ------------------------------------------------------------------ plan
 // One CTA: units per sequence (tiles + KAPPA per item, all kv heads and
 // splits), their prefix sums (workspace), and for each of the C CTAs the
@@ -295,6 +356,7 @@ __device__ __forceinline__ int tile_bound(int c, int W, int C)
 // units, or an empty item starting in them.  plan[0] = {W, C}; plan[1 + c] =
 // {b, g, s, first unit of that item}; plan[1 + C] = {batch, 0, 0, W}.
 constexpr int PLAN_SMEM_SEQS = 8192;  // prefix sums kept in shared memory up to this batch
+constexpr int SELF_PLAN_SEQS = 8192;  // batches up to this size: each CTA plans its own walk
 
 __global__ void __launch_bounds__(1024) tc_plan_kernel(const DecodeParams p, int grid)
 {
@@ -316,28 +378,12 @@ __global__ void __launch_bounds__(1024) tc_plan_kernel(const DecodeParams p, int
         const int b = base + tid;
         int v = 0;
         if (b < p.batch) {
-            int len = p.seq_lens[b];
-            const int cap = p.max_blocks * kBlock;
-            if (p.ring_blocks == 0 && len > cap) {
+            const int len = p.seq_lens[b];
+            if (p.ring_blocks == 0 && len > p.max_blocks * kBlock)
                 record_error(p.err, PKV_DEV_LEN_TABLE);
-                len = cap;
-            }
             if (len > p.max_seq_len)
                 record_error(p.err, PKV_DEV_LEN_BOUND);
-            int tiles = 0, ns = 1;
-            if (len > 0) {
-                const int pos = len - 1;
-                const int lo = p.window > 0 ? max(0, pos - p.window) : 0;
-                const int nblk = pos / kBlock - lo / kBlock + 1;
-                if (sb > 0) {
-                    const int whole = nblk / sb, rem = nblk - whole * sb;
-                    tiles = whole * F + (rem + 7) / 8;
-                    ns = whole + (rem > 0 ? 1 : 0);
-                } else {
-                    tiles = (nblk + 7) / 8;
-                }
-            }
-            v = (tiles + KAPPA * ns) * p.num_kv_heads;
+            v = seq_units(p, b, F);
         }
         int x = v;
 #pragma unroll
@@ -376,41 +422,12 @@ __global__ void __launch_bounds__(1024) tc_plan_kernel(const DecodeParams p, int
     const int C = min(grid, W);
     if (tid == 0)
         p.tc_plan[0] = make_int4(W, C, 0, 0);
-    const int H = p.num_kv_heads;
     for (int c = tid; c <= C; c += 1024) {
         int4 e;
         if (c == C) {
             e = make_int4(p.batch, 0, 0, W);
         } else {
-            const int x = tile_bound(c, W, C);
-            // the sequence whose units hold x, then the item whose units hold it
-            int lo_b = 0, hi_b = p.batch;
-            while (lo_b < hi_b) {
-                const int mid = (lo_b + hi_b) >> 1;
-                if (soff[mid + 1] > x)
-                    hi_b = mid;
-                else
-                    lo_b = mid + 1;
-            }
-            Item it;
-            it.b = lo_b;
-            it.g = 0;
-            it.s = 0;
-            it.start = soff[lo_b];
-            item_geom(p, it);
-            const int Eg = (soff[lo_b + 1] - it.start) / H;  // units per kv head
-            const int rel = x - it.start;
-            if (rel > 0) {
-                it.g = rel / Eg;
-                const int r2 = rel - it.g * Eg;
-                it.s = sb > 0 ? min(r2 / (F + KAPPA), it.nsplit - 1) : 0;
-                it.start += it.g * Eg + it.s * (F + KAPPA);
-                item_geom(p, it);
-                // x in this item's virtual tail: CTA c starts with the next item
-                if (it.start + it.T <= x && !(it.T == 0 && it.start >= x))
-                    item_next(p, it);
-            }
-            e = make_int4(it.b, it.g, it.s, it.start);
+            e = first_item_at(p, soff, tile_bound(c, W, C), F);
         }
         p.tc_plan[1 + c] = e;
     }
@@ -594,16 +611,81 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
-    // The set-up above overlaps the plan kernel (programmatic dependent
-    // launch); the plan is read once that kernel has completed.
-    pdl_wait();
-    pdl_launch_dependents();  // a dependent kernel may be scheduled as SMs free up
-    const int4 hdr = p.tc_plan[0];
-    const int W = hdr.x, C = hdr.y;
+    // The walk: up to SELF_PLAN_SEQS sequences each CTA lays out its own
+    // share (the same arithmetic as tc_plan_kernel, the prefix sums in the
+    // ring, which no load uses yet), so it starts streaming without waiting
+    // for the plan kernel, which then only clears the tickets (awaited before
+    // the first ticket is taken).  Larger batches read the plan kernel's.
     const int c = blockIdx.x;
+    int W, C;
+    int4 first;
+    if (p.batch <= SELF_PLAN_SEQS) {
+        int *soff = reinterpret_cast<int *>(units);
+        int *wsum = reinterpret_cast<int *>(sm + 960);                  // [16]
+        volatile int *carry_s = reinterpret_cast<volatile int *>(sm + 300);
+        int4 *res = reinterpret_cast<int4 *>(units + 4 * (SELF_PLAN_SEQS + 4));
+        const int tid = threadIdx.x;
+        const int F = p.split_blocks > 0 ? (p.split_blocks + 7) / 8 : 0;
+        if (tid == 0)
+            *carry_s = 0;
+        __syncthreads();
+        for (int base = 0; base < p.batch; base += TC_THREADS) {
+            const int b = base + tid;
+            const int v = b < p.batch ? seq_units(p, b, F) : 0;
+            int x = v;
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const int y = __shfl_up_sync(FULL_MASK, x, off);
+                if (lane >= off)
+                    x += y;
+            }
+            if (lane == 31)
+                wsum[warp] = x;
+            __syncthreads();
+            if (warp == 0) {
+                int w = lane < TC_WARPS ? wsum[lane] : 0;
+#pragma unroll
+                for (int off = 1; off < 32; off <<= 1) {
+                    const int y = __shfl_up_sync(FULL_MASK, w, off);
+                    if (lane >= off)
+                        w += y;
+                }
+                if (lane < TC_WARPS)
+                    wsum[lane] = w;
+            }
+            __syncthreads();
+            const int incl = x + (warp > 0 ? wsum[warp - 1] : 0);
+            const int carry = *carry_s;
+            if (b < p.batch)
+                soff[b] = carry + incl - v;
+            __syncthreads();
+            if (tid == TC_THREADS - 1)
+                *carry_s = carry + incl;
+            __syncthreads();
+        }
+        if (tid == 0) {
+            const int w = *carry_s;
+            soff[p.batch] = w;
+            const int cc = min(static_cast<int>(gridDim.x), w);
+            res[0] = make_int4(w, cc, 0, 0);
+            res[1] = c < cc ? first_item_at(p, soff, tile_bound(c, w, cc), F)
+                            : make_int4(p.batch, 0, 0, 0);
+        }
+        __syncthreads();
+        W = res[0].x;
+        C = res[0].y;
+        first = res[1];
+        __syncthreads();  // the ring is the producers' from here
+    } else {
+        pdl_wait();  // the plan kernel has completed
+        const int4 hdr = p.tc_plan[0];
+        W = hdr.x;
+        C = hdr.y;
+        first = c < C ? p.tc_plan[1 + c] : make_int4(p.batch, 0, 0, 0);
+    }
+    pdl_launch_dependents();  // a dependent kernel may be scheduled as SMs free up
     const bool active = c < C;  // CTAs past C only release their TMEM
     const int t0 = active ? tile_bound(c, W, C) : 0, t1 = active ? tile_bound(c + 1, W, C) : 0;
-    const int4 first = active ? p.tc_plan[1 + c] : make_int4(p.batch, 0, 0, 0);
 
     constexpr int GL = GP < 16 ? GP : 16;  // TMEM columns per S or O half
     // Unit j (a 128-dim half of a 128-key tile, counted over the CTA's whole
@@ -1152,8 +1234,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             const int nparts = cz - ca + 1;
             __threadfence();
             group_sync<BAR_EPI>();
-            if (t == 0)
+            if (t == 0) {
+                pdl_wait();  // the plan kernel has cleared the tickets
                 *ticket_s = atomicAdd(&p.tc_flags[ca], 1) == nparts - 1;
+            }
             group_sync<BAR_EPI>();
             const bool last = *ticket_s != 0;
             if (last) {
