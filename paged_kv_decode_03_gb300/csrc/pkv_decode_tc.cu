@@ -19,9 +19,13 @@
 // key range (one split when the caller does not split); the 128-key tiles of
 // all items, in (sequence, kv head, split, tile) order, each item followed by
 // KAPPA virtual tiles that stand for its fixed cost, form one sequence of W
-// units.  tc_plan_kernel (one CTA) scans the lengths and gives CTA c the
-// units [c*W/C, (c+1)*W/C), C = min(grid, W): it records the first item with
-// real tiles there (or an empty item starting there).  A CTA walks its items
+// units.  CTA c takes the units [c*W/C, (c+1)*W/C), C = min(grid, W),
+// starting with the first item with real tiles there (or an empty item
+// starting there); up to 8192 sequences each CTA derives that from the
+// lengths itself, for larger batches tc_plan_kernel (one CTA) records it.
+// tc_plan_kernel always clears the cut items' tickets and checks the lengths;
+// the decode kernel, launched behind it with programmatic dependent launch,
+// waits for it only before taking its first ticket.  A CTA walks its items
 // in order with one pipeline that never drains between them; an item it
 // covers entirely is finished in place (the output, or that split's partial
 // state), an item cut at CTA boundaries leaves one partial state per CTA
