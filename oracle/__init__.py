@@ -67,6 +67,14 @@ def _load():
         lib.oracle_prefill.restype = ctypes.c_int
         lib.oracle_slot_mapping.argtypes = [p, p, i32, p, p, i64, p]
         lib.oracle_slot_mapping.restype = None
+        lib.oracle_f32_to_bf16.argtypes = [ctypes.c_float]
+        lib.oracle_f32_to_bf16.restype = ctypes.c_uint16
+        lib.oracle_rope_table.argtypes = [p, i32, i64, p, p]
+        lib.oracle_rope_table.restype = None
+        lib.oracle_rope.argtypes = [p, p, i64, i32, i32, p, p, i64, i32, i32]
+        lib.oracle_rope.restype = ctypes.c_int
+        lib.oracle_rope_exact.argtypes = [p, p, i32, f64, p, i32, i32]
+        lib.oracle_rope_exact.restype = None
         lib.oracle_max_threads.argtypes = []
         lib.oracle_max_threads.restype = ctypes.c_int
         _lib = lib
@@ -237,6 +245,72 @@ def lse_combine(lse: np.ndarray, o: np.ndarray):
     tot = ctypes.c_double()
     _load().oracle_lse_combine(_ptr(lse), _ptr(o), n, D, _ptr(out), ctypes.byref(tot))
     return out, tot.value
+
+
+ROPE_HALVES, ROPE_INTERLEAVED = 0, 1
+E_POS = -4
+
+
+def f32_to_bf16(x: float) -> int:
+    """bf16 bit pattern of an fp32 value, round to nearest, ties to even."""
+    return int(_load().oracle_f32_to_bf16(ctypes.c_float(x)))
+
+
+def rope_table(theta: np.ndarray, num_positions: int):
+    """RoPE cos / sin table: ([num_positions, pairs, 2] fp32, [num_positions,
+    pairs] bool).  Entry (m, i) holds fp32(cos(m theta_i)), fp32(sin(m
+    theta_i)); the flag marks entries so close to an fp32 rounding midpoint
+    that another faithful fp64 cos / sin may round them the other way."""
+    theta = np.ascontiguousarray(theta, dtype=np.float64)
+    pairs = theta.shape[0]
+    table = np.zeros((num_positions, pairs, 2), np.float32)
+    amb = np.zeros((num_positions, pairs), np.uint8)
+    _load().oracle_rope_table(_ptr(theta), pairs, num_positions, _ptr(table), _ptr(amb))
+    return table, amb.astype(bool)
+
+
+def rope(x_bits: np.ndarray, positions: np.ndarray, table: np.ndarray, layout: int = ROPE_HALVES):
+    """Rotate x_bits [T, H, D] (bf16 bits) by the positions [T] with the
+    table [npos, pairs, 2]; returns (rotated bits, status).  Rows at a
+    negative position, or at one past the table (status E_POS), are copied."""
+    x_bits = np.ascontiguousarray(x_bits, dtype=np.uint16)
+    T, H, D = x_bits.shape
+    pos = np.ascontiguousarray(positions, dtype=np.int64)
+    table = np.ascontiguousarray(table, dtype=np.float32)
+    y = np.empty_like(x_bits)
+    rc = _load().oracle_rope(_ptr(x_bits), _ptr(y), T, H, D, _ptr(pos), _ptr(table),
+                             table.shape[0], table.shape[1], layout)
+    if rc not in (0, E_POS):
+        raise ValueError(f"oracle_rope failed ({rc})")
+    return y, rc
+
+
+def rope_exact(x: np.ndarray, position: float, theta: np.ndarray, pairs: int,
+               layout: int = ROPE_HALVES) -> np.ndarray:
+    """fp64 rotation of one vector x [D] at a position, without rounding."""
+    x = np.ascontiguousarray(x, dtype=np.float64)
+    theta = np.ascontiguousarray(theta, dtype=np.float64)
+    assert theta.shape[0] >= pairs
+    y = np.empty_like(x)
+    _load().oracle_rope_exact(_ptr(x), _ptr(y), x.shape[0], float(position), _ptr(theta), pairs,
+                              layout)
+    return y
+
+
+def append_rope(q_bits: Optional[np.ndarray], k_bits: np.ndarray, v_bits: Optional[np.ndarray],
+                positions: np.ndarray, slot_mapping: np.ndarray, pool: OraclePool,
+                table: np.ndarray, layout: int = ROPE_HALVES):
+    """RoPE fused with the append, as the composition of its two steps: q and
+    k rotated by their positions, then the rotated k (and the unrotated v)
+    appended.  A token at a negative position, or past the table, appends
+    nothing and its q row is copied.  Returns (q_out bits or None, status)."""
+    pos = np.ascontiguousarray(positions, dtype=np.int64)
+    q_out, rc_q = (None, 0) if q_bits is None else rope(q_bits, pos, table, layout)
+    k_rot, rc_k = rope(k_bits, pos, table, layout)
+    valid = (pos >= 0) & (pos < table.shape[0])
+    slots = np.where(valid, np.asarray(slot_mapping, dtype=np.int64), -1)
+    append(k_rot, v_bits, slots, pool)
+    return q_out, (rc_q or rc_k)
 
 
 def max_threads() -> int:

@@ -24,13 +24,19 @@
  *                k_cache[block][slot][head][dim], block_table[seq][i]) and
  *                section 5 (KV int8, per_token or per_head scales,
  *                dequantise after the gather).
+ *   RoPE         the pages name p-RoPE on global layers ([Lab5] model
+ *                overview) without a formula; the rotation follows RoFormer
+ *                (Su et al.) and p-RoPE (Barbero et al.), cited at
+ *                oracle_rope below.
  *
  * Arithmetic: attention in fp64 throughout.  The quantiser is fp32 because
  * the stored scale is an fp32 number (one fp32 division for the scale, one
- * fp32 division per element, round-half-to-even).
+ * fp32 division per element, round-half-to-even).  The stored RoPE output is
+ * bf16, so its rounding is taken in the precision the library states (fp32
+ * table and fp32 fused multiply-adds); oracle_rope_exact is the fp64 form.
  *
  * Parity status of each function is stated beside it; all are pinned by the
- * CPU tests in tests/test_oracle_pins.py.
+ * CPU tests in tests/test_oracle_pins.py (RoPE: tests/test_rope_oracle_pins.py).
  */
 #include <math.h>
 #include <stdint.h>
@@ -156,6 +162,147 @@ int oracle_append(const uint16_t *k, const uint16_t *v, const int64_t *slot_mapp
         }
     }
     return OR_OK;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Rotary position embedding, for RoPE fused with the append.  [Lab5] model  */
+/* overview names p-RoPE on Gemma4's global layers but gives no formula;    */
+/* the definition followed is RoFormer's (Su et al., "RoFormer: Enhanced    */
+/* Transformer with Rotary Position Embedding", section 3.2, general form,  */
+/* and its element-wise form in section 3.4.2): the vector at position m is */
+/* cut into two-dimensional pairs and pair i turns by the angle m*theta_i,  */
+/*     a' = a cos(m theta_i) - b sin(m theta_i),                             */
+/*     b' = a sin(m theta_i) + b cos(m theta_i).                             */
+/* p-RoPE (Barbero et al., "Round and Round We Go! What makes Rotary        */
+/* Positional Encodings useful?", its p-RoPE) drops the lowest frequencies;  */
+/* read here as: the first rotary_pairs pairs (the highest frequencies of a */
+/* decreasing theta table) turn and the rest pass unchanged.  theta_i is a  */
+/* table the caller gives.  Pair i is dims (i, i + D/2) (layout 0, halves)  */
+/* or (2i, 2i + 1) (layout 1, RoFormer's own interleaving).                 */
+/*                                                                          */
+/* Precision: the rotated values are stored as bf16 and, in int8 pools,     */
+/* quantised, so a rounding decides stored bits.  Both sides take it in the */
+/* same precision, the one the library states: cos and sin of the fp64      */
+/* angle m * theta_i rounded once to fp32 (the table), then in fp32         */
+/* t = b * s, a' = fma(a, c, -t) and t = b * c, b' = fma(a, s, t), each     */
+/* rounded to bf16 (nearest, ties to even).  oracle_rope_exact is the fp64  */
+/* rotation without any rounding, for the pins.                             */
+/* ------------------------------------------------------------------------ */
+enum { OR_E_POS = -4 };
+
+/* fp32 -> bf16 bit pattern, round to nearest, ties to even (NaN kept quiet). */
+uint16_t oracle_f32_to_bf16(float x)
+{
+    uint32_t u;
+    memcpy(&u, &x, sizeof u);
+    if ((u & 0x7f800000u) == 0x7f800000u && (u & 0x007fffffu))
+        return (uint16_t)((u >> 16) | 0x0040u);
+    return (uint16_t)((u + 0x7fffu + ((u >> 16) & 1u)) >> 16);
+}
+
+/* 1 if the fp64 value v lies so close to the midpoint between two fp32
+ * numbers that another faithful fp64 cos or sin (a few ulps away) could round
+ * to the other one. */
+static int near_f32_midpoint(double v)
+{
+    float f = (float)v;
+    double d = v - (double)f;
+    if (d == 0.0 || v == 0.0)
+        return 0;
+    float g = nextafterf(f, d > 0 ? INFINITY : -INFINITY);
+    double mid = 0.5 * ((double)f + (double)g);
+    double ulp = ldexp(1.0, ilogb(v) - 52);
+    return fabs(v - mid) <= 8.0 * ulp;
+}
+
+/* table[m][i] = (fp32(cos(m theta_i)), fp32(sin(m theta_i))), m < npos,
+ * i < pairs; the angle is one fp64 product.  ambiguous[m][i] (may be NULL)
+ * flags entries whose rounding another faithful cos / sin could change. */
+void oracle_rope_table(const double *theta, int32_t pairs, int64_t npos, float *table,
+                       uint8_t *ambiguous)
+{
+    for (int64_t m = 0; m < npos; ++m)
+        for (int32_t i = 0; i < pairs; ++i) {
+            double ang = (double)m * theta[i];
+            double c = cos(ang), s = sin(ang);
+            int64_t e = m * pairs + i;
+            table[2 * e] = (float)c;
+            table[2 * e + 1] = (float)s;
+            if (ambiguous)
+                ambiguous[e] = (uint8_t)(near_f32_midpoint(c) || near_f32_midpoint(s));
+        }
+}
+
+static void pair_dims(int32_t i, int32_t head_dim, int32_t layout, int32_t *ia, int32_t *ib)
+{
+    if (layout == 0) {
+        *ia = i;
+        *ib = i + head_dim / 2;
+    } else {
+        *ia = 2 * i;
+        *ib = 2 * i + 1;
+    }
+}
+
+/* x, y: [num_tokens][heads][head_dim] bf16 bits; token t sits at position
+ * pos[t].  A negative position (padding) or one past the table copies the
+ * row unchanged; the latter also makes the call return OR_E_POS.  y may be
+ * x. */
+int oracle_rope(const uint16_t *x, uint16_t *y, int64_t num_tokens, int32_t heads,
+                int32_t head_dim, const int64_t *pos, const float *table, int64_t npos,
+                int32_t pairs, int32_t layout)
+{
+    if (pairs < 0 || 2 * pairs > head_dim || (head_dim & 1))
+        return OR_E_ARG;
+    int rc = OR_OK;
+    const int64_t row = (int64_t)heads * head_dim;
+    for (int64_t t = 0; t < num_tokens; ++t) {
+        const uint16_t *xr = x + t * row;
+        uint16_t *yr = y + t * row;
+        int64_t m = pos[t];
+        if (yr != xr)
+            memcpy(yr, xr, (size_t)row * sizeof(uint16_t));
+        if (m < 0)
+            continue;
+        if (m >= npos) {
+            rc = OR_E_POS;
+            continue;
+        }
+        for (int32_t h = 0; h < heads; ++h) {
+            const uint16_t *xh = xr + (int64_t)h * head_dim;
+            uint16_t *yh = yr + (int64_t)h * head_dim;
+            for (int32_t i = 0; i < pairs; ++i) {
+                int32_t ia, ib;
+                pair_dims(i, head_dim, layout, &ia, &ib);
+                const float a = bf16_bits_to_float(xh[ia]), b = bf16_bits_to_float(xh[ib]);
+                const float c = table[2 * (m * pairs + i)], s = table[2 * (m * pairs + i) + 1];
+                /* plain float products are single IEEE fp32 roundings here
+                 * (no contraction: built with -ffp-contract=off) */
+                const float t1 = b * s;
+                const float ap = fmaf(a, c, -t1);
+                const float t2 = b * c;
+                const float bp = fmaf(a, s, t2);
+                yh[ia] = oracle_f32_to_bf16(ap);
+                yh[ib] = oracle_f32_to_bf16(bp);
+            }
+        }
+    }
+    return rc;
+}
+
+/* The same rotation in fp64 with no rounding: x, y [head_dim], position m. */
+void oracle_rope_exact(const double *x, double *y, int32_t head_dim, double m,
+                       const double *theta, int32_t pairs, int32_t layout)
+{
+    for (int32_t d = 0; d < head_dim; ++d)
+        y[d] = x[d];
+    for (int32_t i = 0; i < pairs; ++i) {
+        int32_t ia, ib;
+        pair_dims(i, head_dim, layout, &ia, &ib);
+        double c = cos(m * theta[i]), s = sin(m * theta[i]);
+        y[ia] = x[ia] * c - x[ib] * s;
+        y[ib] = x[ia] * s + x[ib] * c;
+    }
 }
 
 /* ------------------------------------------------------------------------ */
