@@ -907,6 +907,94 @@ def measure_prefill(spec, q_len, dev, steps, warmup, with_oracle):
     return entry
 
 
+def measure_rope_append(spec, base, pairs, dev, steps, warmup, with_oracle):
+    """RoPE fused with the append for one decode step's new tokens (one per
+    sequence, at position seq_len - 1): paged_kv_append_rope in a CUDA graph,
+    beside the plain paged_kv_append of the same tokens.  theta_i =
+    base^(-2i/D) for the first ``pairs`` pairs (p-RoPE keeps the highest
+    frequencies), halves pairing."""
+    import torch
+    import paged_kv_decode_03_gb300 as pkv
+    w = synth.make_workload(spec)
+    B, D = spec.batch, spec.head_dim
+    pool = device_pool(spec, w, dev, hist=False)
+    npos = int(w.seq_lens.max())
+    theta = (base ** (-2.0 * np.arange(D // 2) / D))[:pairs].astype(np.float64)
+    table = pkv.paged_rope_cos_sin_table(_dnum(theta, dev), npos)
+    q = _dbits(w.q, dev)
+    q_out = torch.empty_like(q)
+    k = _dbits(w.new_k, dev)
+    v = None if w.new_v is None else _dbits(w.new_v, dev)
+    pos = _dnum(w.seq_lens.astype(np.int64) - 1, dev)
+    slots = _dnum(w.new_slots, dev)
+    calls = {
+        "fused": lambda: pkv.paged_kv_append_rope(q, q_out, k, v, pos, slots, pool, table),
+        "append_only": lambda: pkv.paged_kv_append(k, v, slots, pool),
+    }
+    us = {}
+    for name, call in calls.items():
+        for _ in range(max(3, warmup)):
+            call()
+        torch.cuda.synchronize()
+        cap = torch.cuda.Stream()
+        cap.wait_stream(torch.cuda.current_stream())
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(cap):
+            with torch.cuda.graph(graph, stream=cap):
+                call()
+        torch.cuda.current_stream().wait_stream(cap)
+        for _ in range(3):
+            graph.replay()
+        torch.cuda.synchronize()
+        evs = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
+        evs[0].record()
+        for i in range(steps):
+            graph.replay()
+            evs[i + 1].record()
+        torch.cuda.synchronize()
+        us[name] = evs[0].elapsed_time(evs[-1]) / steps * 1e3
+        del graph
+    # bytes: q in and out, the new k (and v) rows in, the pool rows out (bf16
+    # or int8 codes), one table row per token, positions and slots
+    row = spec.num_kv_heads * D
+    kv_in = B * row * 2 * (1 if spec.alias else 2)
+    elem = 2 if spec.kv == "bf16" else 1
+    kv_out = B * row * elem * (1 if spec.alias else 2)
+    moved = 2 * B * spec.num_q_heads * D * 2 + kv_in + kv_out + B * pairs * 8 + B * 16
+    hbm_peak, _ = peaks()
+    entry = {
+        "workload": f"{workload_desc(spec)}; one new token per sequence at position seq_len - 1, "
+                    f"RoPE theta = {base:g}^(-2i/{D}) on the first {pairs} of {D // 2} pairs",
+        "call": "paged_kv_append_rope, one CUDA graph (beside paged_kv_append of the same tokens)",
+        "kernel_us": round(us["fused"], 3),
+        "append_only_us": round(us["append_only"], 3),
+        "bytes_moved": moved,
+        "hbm_gbs": round(moved / (us["fused"] * 1e-6) / 1e9, 1),
+        "frac_of_measured_hbm": round(moved / (us["fused"] * 1e-6) / 1e9 / hbm_peak, 4),
+        "device_error_word": pkv.device_status(clear=True),
+    }
+    if with_oracle:
+        import oracle
+        k_, v_, ks_, vs_ = synth.empty_pool_arrays(spec, w.layout)
+        mode = {"bf16": oracle.SCALE_NONE, "int8_token": oracle.SCALE_PER_TOKEN,
+                "int8_head": oracle.SCALE_PER_HEAD}[spec.kv]
+        if spec.kv == "int8_head":
+            ks_, vs_ = w.k_head_scale.copy(), None if spec.alias else w.v_head_scale.copy()
+        opool = oracle.OraclePool(k=k_, v=v_, k_scale=ks_, v_scale=vs_, scale_mode=mode)
+        otable, _ = oracle.rope_table(theta, npos)
+        t0 = time.perf_counter()
+        oracle.append_rope(w.q, w.new_k, w.new_v, w.seq_lens.astype(np.int64) - 1, w.new_slots,
+                           opool, otable)
+        t = time.perf_counter() - t0
+        entry["oracle"] = {"kind": "oracle", "threads": 1, "all_threads_s": round(t, 5),
+                           "sample": f"the whole step ({B} tokens), fp32-rounded C oracle "
+                                     "(table built outside the timing)"}
+    del pool, table, q, q_out
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return entry
+
+
 def per_config(args, dev, main_entry, main_spec, main_w):
     """Every workload at its full size: the decode kernel's time and roofline
     fraction (CUDA events over CUDA-graph replays), the six-layer step, and
@@ -940,6 +1028,13 @@ def per_config(args, dev, main_entry, main_spec, main_w):
         out["c5"]["oracle"] = oracle_full_run(layers[0].spec, layers[0], layers)
     del layers
     out["c2_chunk128"] = measure_prefill(synth.C2, 128, dev, steps, warm, cpu)
+    # RoPE fused with the append: the global layer with p-RoPE on a quarter
+    # of the pairs, the int8 sliding layer with every pair turning
+    out["c5g_rope_append"] = measure_rope_append(synth.C5_GLOBAL, 1e6, synth.C5_GLOBAL.head_dim // 8,
+                                                 dev, steps, warm, cpu)
+    out["c5s_rope_append"] = measure_rope_append(synth.C5_SLIDING, 1e4,
+                                                 synth.C5_SLIDING.head_dim // 2, dev, steps, warm,
+                                                 cpu)
     return out
 
 

@@ -86,6 +86,11 @@ extern "C" {
 #define PKV_DEV_BAD_SLOT 4u     /* slot_mapping entry >= num_blocks * block_size */
 #define PKV_DEV_TIMEOUT 8u      /* a pipeline wait ran past its limit */
 #define PKV_DEV_LEN_BOUND 16u   /* seq_len > max_seq_len given on the host */
+#define PKV_DEV_BAD_POSITION 32u /* a RoPE position >= num_positions of its table */
+
+/* Pairing of dims in a rotary embedding (paged_kv_append_rope). */
+#define PKV_ROPE_HALVES 0      /* pair i = dims (i, i + head_dim / 2) */
+#define PKV_ROPE_INTERLEAVED 1 /* pair i = dims (2i, 2i + 1) */
 
 /*
  * One layer's KV pool (tiniestgpt notes, section 2; one pool per layer).
@@ -166,6 +171,57 @@ PKV_API int paged_kv_slot_mapping(const pkv_pool *pool, const int32_t *block_tab
                                   int32_t max_blocks_per_seq, const int32_t *seq_ids,
                                   const int64_t *positions, int32_t num_tokens,
                                   int64_t *slot_mapping, void *stream);
+
+/*
+ * Rotary position embedding fused with the append.  The Lab5-Gemma4 model
+ * overview names p-RoPE on the global layers but gives no formula; the
+ * rotation is RoFormer's (Su et al., "RoFormer: Enhanced Transformer with
+ * Rotary Position Embedding", section 3.2 and the element-wise form of
+ * section 3.4.2): pair i of a vector at position m turns by m * theta_i,
+ *     a' = a cos(m theta_i) - b sin(m theta_i),
+ *     b' = a sin(m theta_i) + b cos(m theta_i),
+ * and p-RoPE (Barbero et al., "Round and Round We Go! What makes Rotary
+ * Positional Encodings useful?") keeps only the highest frequencies: the
+ * first rotary_pairs pairs of a decreasing theta table turn, the others pass
+ * unchanged.  theta is the caller's (RoFormer: theta_i = base^(-2i/D)).
+ *
+ * paged_rope_cos_sin_table -- the (cos, sin) table of every position.
+ *   theta:  [rotary_pairs] fp64, radians per position, 8-byte aligned.
+ *   table (output): [num_positions][rotary_pairs] pairs of fp32,
+ *          table[m][i] = (fp32(cos(m theta_i)), fp32(sin(m theta_i))), the
+ *          angle one fp64 product and its cosine and sine fp64 values
+ *          rounded once to fp32; 8-byte aligned.  Computed once per model.
+ */
+PKV_API int paged_rope_cos_sin_table(const double *theta, int32_t rotary_pairs,
+                                     int64_t num_positions, float *table, void *stream);
+
+/*
+ * paged_kv_append_rope -- rotate each new token's q and k by its position,
+ * write the rotated q to q_out and append the rotated k (and the unrotated
+ * v) as paged_kv_append does (bf16 copy or int8 quantisation of the rotated
+ * values).  With K and V one tensor the stored (rotated) row serves as both.
+ *   q:         [num_tokens][num_q_heads][head_dim] bf16, 16-byte aligned, or
+ *              NULL (k only); q_out: same shape, may be q (in place).
+ *   k, v, slot_mapping, pool: as paged_kv_append.
+ *   positions: [num_tokens] int64, 8-byte aligned.  A negative position is
+ *              padding: q_out gets the q row unchanged and nothing is
+ *              appended.  A position >= num_positions is treated the same
+ *              and sets PKV_DEV_BAD_POSITION.  A token with a valid position
+ *              and a negative slot has its q rotated and appends nothing.
+ *   table:     from paged_rope_cos_sin_table (num_positions rows of
+ *              rotary_pairs entries); rotary_pairs in [0, head_dim / 2].
+ *   layout:    PKV_ROPE_HALVES or PKV_ROPE_INTERLEAVED.
+ * Arithmetic: with (c, s) from the table, t = b * s, a' = fma(a, c, -t),
+ * t = b * c, b' = fma(a, s, t) in fp32, each rounded once to bf16 (nearest,
+ * ties to even); the stored bits are fixed by it.  Dims that do not turn are
+ * copied bit for bit; a non-finite input gives a non-finite output.
+ */
+PKV_API int paged_kv_append_rope(const void *q, void *q_out, int32_t num_q_heads, const void *k,
+                                 const void *v, const int64_t *positions,
+                                 const int64_t *slot_mapping, int32_t num_tokens,
+                                 const float *table, int64_t num_positions,
+                                 int32_t rotary_pairs, int32_t layout, const pkv_pool *pool,
+                                 void *stream);
 
 /*
  * paged_decode_split_tokens -- the split length paged_decode_attention uses

@@ -4,7 +4,9 @@ Python face of the C-ABI library ``libpagedkv.so`` (declared in
 ``include/pagedkv.h``): ``paged_kv_append`` and ``paged_decode_attention``,
 plus the two steps of the split-KV path (``paged_decode_split_partial``,
 ``paged_decode_lse_combine``) and a whole model step over one layout
-(``paged_decode_step``).  The binding only marshals arguments; every
+(``paged_decode_step``), chunk attention (``paged_prefill_attention``) and
+RoPE fused with the append (``paged_rope_cos_sin_table``,
+``paged_kv_append_rope``).  The binding only marshals arguments; every
 step of the computation runs in the library's sm_103a kernels.  There is no
 CPU fallback: if the library is missing, the first call raises.
 """
@@ -16,4 +18,5 @@ from .binding import (  # noqa: F401
     paged_decode_partial_workspace_bytes, uses_tensor_cores, last_launch_count,
     STATIC_SCRATCH_BYTES, DecodeLayer, paged_prefill_attention, check_bounded_wait, paged_decode_step, paged_decode_step_workspace_bytes,
     library_path, load_library, device_status, exported_symbols,
+    ROPE_HALVES, ROPE_INTERLEAVED, paged_rope_cos_sin_table, paged_kv_append_rope,
 )

@@ -21,6 +21,7 @@ HEADER = os.path.join(os.path.dirname(HERE), "include", "pagedkv.h")
 PKV_BF16, PKV_INT8 = 0, 1
 SCALE_NONE, SCALE_PER_TOKEN, SCALE_PER_HEAD = 0, 1, 2
 OUT_BF16, OUT_F32 = 0, 1
+ROPE_HALVES, ROPE_INTERLEAVED = 0, 1
 SPLIT_AUTO = -1
 
 _lib = None
@@ -97,6 +98,11 @@ def load_library():
     lib.paged_prefill_attention.argtypes = [p, p, i32, i32, p, p, i32, p, i32, i32, i32, i32, f32,
                                             p, i32, p]
     lib.paged_prefill_attention.restype = ctypes.c_int
+    i64 = ctypes.c_int64
+    lib.paged_rope_cos_sin_table.argtypes = [p, i32, i64, p, p]
+    lib.paged_rope_cos_sin_table.restype = ctypes.c_int
+    lib.paged_kv_append_rope.argtypes = [p, p, i32, p, p, p, p, i32, p, i64, i32, i32, p, p]
+    lib.paged_kv_append_rope.restype = ctypes.c_int
     lib.paged_kv_slot_mapping.argtypes = [p, p, i32, p, p, i32, p, p]
     lib.paged_kv_slot_mapping.restype = ctypes.c_int
     lib.paged_decode_step_workspace_bytes.argtypes = [p, i32, i32, i32, i32, i32]
@@ -216,6 +222,44 @@ def paged_kv_append(k, v, slot_mapping, pool: PagedKVPool, stream=None) -> None:
     n = int(slot_mapping.shape[0])
     _check(lib.paged_kv_append(_dev_ptr(k, "k"), _dev_ptr(v, "v"), _dev_ptr(slot_mapping, "slot_mapping"),
                                n, ctypes.byref(pc), _stream(stream)), "paged_kv_append")
+
+
+def paged_rope_cos_sin_table(theta, num_positions: int, table=None, stream=None):
+    """(cos, sin) of every position's angles: ``theta`` [pairs] float64 on the
+    device (radians per position); returns ``table`` [num_positions, pairs, 2]
+    float32 (allocated if None)."""
+    import torch
+    pairs = int(theta.shape[0])
+    if theta.dtype != torch.float64:
+        raise PagedKVError("theta must be float64")
+    if table is None:
+        table = torch.empty((num_positions, pairs, 2), dtype=torch.float32, device=theta.device)
+    if tuple(table.shape) != (num_positions, pairs, 2) or table.dtype != torch.float32:
+        raise PagedKVError("table must be [num_positions, pairs, 2] float32")
+    _check(load_library().paged_rope_cos_sin_table(_dev_ptr(theta, "theta"), pairs, num_positions,
+                                                   _dev_ptr(table, "table"), _stream(stream)),
+           "paged_rope_cos_sin_table")
+    return table
+
+
+def paged_kv_append_rope(q, q_out, k, v, positions, slot_mapping, pool: PagedKVPool, table,
+                         layout: int = ROPE_HALVES, stream=None) -> None:
+    """RoPE fused with the append: q ([T, H_q, D] bf16, or None) rotated into
+    ``q_out`` (may be q), k ([T, H_kv, D]) rotated and appended with v at
+    ``slot_mapping``, every token at its ``positions`` entry ([T] int64),
+    with the (cos, sin) ``table`` of paged_rope_cos_sin_table ([npos, pairs,
+    2]; its pairs are the rotated ones)."""
+    lib = load_library()
+    pc = pool.c_struct()
+    n = int(slot_mapping.shape[0])
+    hq = int(q.shape[1]) if q is not None else 0
+    npos, pairs = int(table.shape[0]), int(table.shape[1])
+    _check(lib.paged_kv_append_rope(_dev_ptr(q, "q"), _dev_ptr(q_out, "q_out"), hq,
+                                    _dev_ptr(k, "k"), _dev_ptr(v, "v"),
+                                    _dev_ptr(positions, "positions"),
+                                    _dev_ptr(slot_mapping, "slot_mapping"), n,
+                                    _dev_ptr(table, "table"), npos, pairs, int(layout),
+                                    ctypes.byref(pc), _stream(stream)), "paged_kv_append_rope")
 
 
 def paged_kv_slot_mapping(pool: PagedKVPool, block_table, positions, slot_mapping,

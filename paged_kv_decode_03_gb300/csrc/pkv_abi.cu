@@ -354,6 +354,93 @@ PKV_API int paged_kv_append(const void *k, const void *v, const int64_t *slot_ma
     return PKV_OK;
 }
 
+PKV_API int paged_rope_cos_sin_table(const double *theta, int32_t rotary_pairs,
+                                     int64_t num_positions, float *table, void *stream)
+{
+    t_last_error.clear();
+    t_launches = 0;
+    if (rotary_pairs < 0 || num_positions < 0)
+        return fail(PKV_E_ARG, "rotary_pairs or num_positions < 0");
+    if (rotary_pairs == 0 || num_positions == 0)
+        return PKV_OK;
+    if (!theta || !table)
+        return fail(PKV_E_NULL, "theta or table is NULL");
+    if (!aligned(theta, 8) || !aligned(table, 8))
+        return fail(PKV_E_ALIGN, "theta and table must be 8-byte aligned");
+    cudaError_t e = launch_rope_table(theta, rotary_pairs, num_positions, table,
+                                      static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess)
+        return cuda_fail(e, "RoPE table launch");
+    return PKV_OK;
+}
+
+PKV_API int paged_kv_append_rope(const void *q, void *q_out, int32_t num_q_heads, const void *k,
+                                 const void *v, const int64_t *positions,
+                                 const int64_t *slot_mapping, int32_t num_tokens,
+                                 const float *table, int64_t num_positions,
+                                 int32_t rotary_pairs, int32_t layout, const pkv_pool *pool,
+                                 void *stream)
+{
+    t_last_error.clear();
+    t_launches = 0;
+    if (int rc = check_pool(pool))
+        return rc;
+    if (num_tokens < 0)
+        return fail(PKV_E_ARG, "num_tokens < 0");
+    if (rotary_pairs < 0 || 2 * rotary_pairs > pool->head_dim)
+        return fail(PKV_E_ARG, "rotary_pairs %d outside [0, head_dim / 2]", rotary_pairs);
+    if (layout != PKV_ROPE_HALVES && layout != PKV_ROPE_INTERLEAVED)
+        return fail(PKV_E_ARG, "unknown RoPE layout %d", layout);
+    if (num_positions < 0)
+        return fail(PKV_E_ARG, "num_positions < 0");
+    if (q && num_q_heads <= 0)
+        return fail(PKV_E_ARG, "num_q_heads <= 0");
+    if (num_tokens == 0)
+        return PKV_OK;
+    const bool alias = pool->v == nullptr || pool->v == pool->k;
+    if (!k || !slot_mapping || !positions || (!alias && !v) || (q && !q_out) ||
+        (rotary_pairs > 0 && num_positions > 0 && !table))
+        return fail(PKV_E_NULL, "k, v, q_out, positions, slot_mapping or table is NULL");
+    if (!aligned(k, 16) || (!alias && !aligned(v, 16)) || !aligned(slot_mapping, 8) ||
+        !aligned(positions, 8) || (q && (!aligned(q, 16) || !aligned(q_out, 16))) ||
+        (table && !aligned(table, 8)))
+        return fail(PKV_E_ALIGN, "q/q_out/k/v must be 16-byte, positions/slot_mapping/table "
+                                 "8-byte aligned");
+    AppendParams p{};
+    p.k = static_cast<const uint16_t *>(k);
+    p.v = static_cast<const uint16_t *>(alias ? k : v);
+    p.slot_mapping = slot_mapping;
+    p.pool_k = pool->k;
+    p.pool_v = alias ? pool->k : pool->v;
+    p.k_scale = pool->k_scale;
+    p.v_scale = alias ? pool->k_scale : pool->v_scale;
+    p.num_tokens = num_tokens;
+    p.row = pool->num_kv_heads * pool->head_dim;
+    p.head_dim = pool->head_dim;
+    p.num_slots = (int64_t)pool->num_blocks * pool->block_size;
+    p.scale_mode = pool->scale_mode;
+    p.alias = alias;
+    p.err = error_word_ptr();
+    if (!p.err)
+        return fail(PKV_E_DRIVER, "cannot resolve the device error word");
+    if (append_rope_smem_bytes(p.row, rotary_pairs) > 227 * 1024)
+        return fail(PKV_E_SHAPE, "a token's K row (%d elements) is too large", p.row);
+    RopeParams r{};
+    r.q = static_cast<const uint16_t *>(q);
+    r.q_out = static_cast<uint16_t *>(q_out);
+    r.positions = positions;
+    r.table = reinterpret_cast<const float2 *>(table);
+    r.num_positions = num_positions;
+    r.num_q_heads = q ? num_q_heads : 0;
+    r.pairs = rotary_pairs;
+    r.layout = layout;
+    cudaError_t e = launch_append_rope(p, r, pool->dtype == PKV_INT8,
+                                       static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess)
+        return cuda_fail(e, "append (RoPE) launch");
+    return PKV_OK;
+}
+
 PKV_API int paged_kv_slot_mapping(const pkv_pool *pool, const int32_t *block_table,
                                   int32_t max_blocks_per_seq, const int32_t *seq_ids,
                                   const int64_t *positions, int32_t num_tokens,

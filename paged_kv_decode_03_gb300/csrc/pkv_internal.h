@@ -94,6 +94,19 @@ struct AppendParams {
     unsigned int *err;
 };
 
+// RoPE fused with the append (with AppendParams): q rotated into q_out, k
+// rotated before it is stored.
+struct RopeParams {
+    const uint16_t *q;        // [T][H_q][D] bf16 or NULL (no q)
+    uint16_t *q_out;          // same shape; may be q
+    const int64_t *positions; // [T]
+    const float2 *table;      // [num_positions][pairs] (cos, sin)
+    int64_t num_positions;
+    int32_t num_q_heads;
+    int32_t pairs;            // rotated pairs, <= D / 2
+    int32_t layout;           // PKV_ROPE_HALVES or PKV_ROPE_INTERLEAVED
+};
+
 struct CombineParams {
     const float *part_lse;    // [B][num_splits][H_q]
     const float *part_o;      // [B][num_splits][H_q][D]
@@ -133,6 +146,11 @@ cudaError_t launch_decode_tc(const DecodeParams &p, const CUtensorMap &tmk,
                              const CUtensorMap &tmv, const CUtensorMap &tmq, int head_dim,
                              cudaStream_t s);
 cudaError_t launch_append(const AppendParams &p, int int8, cudaStream_t s);
+size_t append_rope_smem_bytes(int row, int pairs);
+cudaError_t launch_append_rope(const AppendParams &p, const RopeParams &r, int int8,
+                               cudaStream_t s);
+cudaError_t launch_rope_table(const double *theta, int pairs, int64_t num_positions,
+                              float *table, cudaStream_t s);
 cudaError_t launch_bounded_wait(uint64_t limit_ns, int spin, int *out, int threads,
                                 unsigned int *err, cudaStream_t s);
 // Chunk attention (tensor cores, bf16 pools): K/V tile buffers that fit, the

@@ -193,3 +193,32 @@ def test_oracle_is_not_reachable_from_the_product():
         text = f.read_text(errors="ignore")
         assert "import oracle" not in text and "from oracle" not in text, f
         assert "pkv_oracle" not in text and "_liboracle" not in text, f
+
+
+def test_rope_validation(lib):
+    """RoPE fused with the append: arguments rejected on the host."""
+    pool = _pool()  # head_dim 128: at most 64 rotated pairs
+    f = lib.paged_kv_append_rope
+
+    def call(q=FAKE, q_out=FAKE, hq=4, k=FAKE, v=FAKE, pos=FAKE, slots=FAKE, n=4, table=FAKE,
+             npos=100, pairs=16, layout=0):
+        return f(q, q_out, hq, k, v, pos, slots, n, table, npos, pairs, layout,
+                 ctypes.byref(pool), None)
+    assert call(pairs=65) == E_ARG
+    assert call(pairs=-1) == E_ARG
+    assert call(layout=2) == E_ARG
+    assert call(hq=0) == E_ARG
+    assert call(n=-1) == E_ARG
+    assert call(npos=-1) == E_ARG
+    assert call(pos=None) == E_NULL
+    assert call(q_out=None) == E_NULL
+    assert call(table=None) == E_NULL
+    assert call(q=FAKE + 8) == E_ALIGN
+    assert call(pos=FAKE + 4) == E_ALIGN
+    assert call(table=FAKE + 4) == E_ALIGN
+    assert call(n=0) == 0
+    t = lib.paged_rope_cos_sin_table
+    assert t(FAKE, -1, 10, FAKE, None) == E_ARG
+    assert t(None, 4, 10, FAKE, None) == E_NULL
+    assert t(FAKE + 4, 4, 10, FAKE, None) == E_ALIGN
+    assert t(FAKE, 0, 10, None, None) == 0
