@@ -66,6 +66,9 @@ def parse_args():
     ap.add_argument("--chunk-only", type=int, default=0,
                     help="time only the chunk attention (q_len > 1) with chunks of this many "
                          "tokens on --config's shapes (prints that measurement, not a bench line)")
+    ap.add_argument("--rope-only", action="store_true",
+                    help="time only RoPE fused with the append on the continuous-batching global "
+                         "and sliding layers' new tokens (prints that measurement)")
     return ap.parse_args()
 
 
@@ -713,11 +716,21 @@ def measure_layer(spec, w, dev, req, steps, warmup, split_api_allowed=True):
     return entry
 
 
-def measure_step(dev, steps, warmup):
+def rope_theta(spec):
+    """(base, theta) of a layer's RoPE in the benchmark: every pair with base
+    10^4 on sliding layers, p-RoPE on the first quarter of the pairs with
+    base 10^6 on global layers; theta_i = base^(-2i/D) (RoFormer)."""
+    D = spec.head_dim
+    base, pairs = (1e4, D // 2) if spec.window else (1e6, D // 8)
+    return base, (base ** (-2.0 * np.arange(D // 2) / D))[:pairs].astype(np.float64)
+
+
+def measure_step(dev, steps, warmup, rope=False):
     """The six-layer continuous-batching step (five int8 per-head sliding
     layers, one bf16 global layer, one ragged layout with shared prefix
     blocks): one paged_decode_step call captured as one CUDA graph and
-    replayed; events around each replay."""
+    replayed; events around each replay.  With ``rope`` every layer's append
+    is RoPE fused with the append (q rotated into its own buffer)."""
     import torch
     import paged_kv_decode_03_gb300 as pkv
     layers = synth.make_step(share_history=True)
@@ -736,11 +749,20 @@ def measure_step(dev, steps, warmup):
     del base
     slots, bt, sl = _dnum(w0.new_slots, dev), _dnum(w0.block_table, dev), _dnum(w0.seq_lens, dev)
     max_len = int(w0.seq_lens.max())
+    extra, rope_bytes = [{} for _ in layers], 0
+    if rope:
+        for i, lw in enumerate(layers):
+            _, theta = rope_theta(lw.spec)
+            table = pkv.paged_rope_cos_sin_table(_dnum(theta, dev), max_len)
+            extra[i] = dict(rope_table=table, q_rotated=torch.empty(lw.q.shape, dtype=torch.bfloat16,
+                                                                   device=dev))
+            rope_bytes += 2 * lw.q.size * 2 + len(lw.seq_lens) * len(theta) * 8
     dl = [pkv.DecodeLayer(pool=gp, q=_dbits(lw.q, dev), k_new=_dbits(lw.new_k, dev),
                           v_new=None if lw.new_v is None else _dbits(lw.new_v, dev),
                           out=torch.empty(lw.q.shape, dtype=torch.bfloat16, device=dev),
-                          window=lw.spec.window, softmax_scale=float(np.float32(lw.spec.softmax_scale)))
-          for lw, gp in zip(layers, pools)]
+                          window=lw.spec.window, softmax_scale=float(np.float32(lw.spec.softmax_scale)),
+                          **extra[i])
+          for i, (lw, gp) in enumerate(zip(layers, pools))]
     ws = torch.empty(max(256, pkv.paged_decode_step_workspace_bytes(dl, max_len)),
                      dtype=torch.uint8, device=dev)
 
@@ -775,6 +797,7 @@ def measure_step(dev, steps, warmup):
         d = bytes_model.decode_bytes(lw.spec, lw.seq_lens, lw.block_table)
         step_bytes += d["kv"] + d["q"] + d["out"]
         step_bytes += bytes_model.append_bytes(lw.spec, int((lw.new_slots >= 0).sum()))
+    step_bytes += rope_bytes  # rotated q written and read again, table rows
     peak, _ = peaks()
     gbs = step_bytes / (ms * 1e-3) / 1e9
     B = w0.spec.batch
@@ -783,7 +806,10 @@ def measure_step(dev, steps, warmup):
                      f"({''.join(synth.C5_LAYERS)}) over one layout; sliding: "
                      f"{workload_desc(layers[0].spec)}; global: {workload_desc(layers[-1].spec)}; "
                      "history values shared by the sliding layers, each its own pool"),
-        "call": "paged_decode_step (every layer's append + decode), one CUDA graph",
+        "call": ("paged_decode_step (every layer's RoPE + append, then decode), one CUDA graph; "
+                 "RoPE: every pair, theta base 1e4, on sliding layers; the first quarter of the "
+                 "pairs, base 1e6, on the global layer" if rope else
+                 "paged_decode_step (every layer's append + decode), one CUDA graph"),
         "ms_per_step": round(ms, 6), "ms_per_step_median": round(statistics.median(per), 6),
         "bytes_per_step": int(step_bytes),
         "step_gbs": round(gbs, 1), "frac_of_measured": round(gbs / peak, 4),
@@ -792,7 +818,7 @@ def measure_step(dev, steps, warmup):
         "gpu_launches_per_step": launches,
         "device_error_word": pkv.device_status(clear=True),
     }
-    del dl, pools, ws, graph
+    del dl, pools, ws, graph, extra
     torch.cuda.synchronize()
     torch.cuda.empty_cache()
     return entry, layers
@@ -919,7 +945,7 @@ def measure_rope_append(spec, base, pairs, dev, steps, warmup, with_oracle):
     B, D = spec.batch, spec.head_dim
     pool = device_pool(spec, w, dev, hist=False)
     npos = int(w.seq_lens.max())
-    theta = (base ** (-2.0 * np.arange(D // 2) / D))[:pairs].astype(np.float64)
+    theta = (base ** (-2.0 * np.arange(D // 2) / D))[:pairs].astype(np.float64)  # RoFormer
     table = pkv.paged_rope_cos_sin_table(_dnum(theta, dev), npos)
     q = _dbits(w.q, dev)
     q_out = torch.empty_like(q)
@@ -1027,6 +1053,7 @@ def per_config(args, dev, main_entry, main_spec, main_w):
     if cpu:
         out["c5"]["oracle"] = oracle_full_run(layers[0].spec, layers[0], layers)
     del layers
+    out["c5_rope"], _ = measure_step(dev, max(20, steps // 2), warm, rope=True)
     out["c2_chunk128"] = measure_prefill(synth.C2, 128, dev, steps, warm, cpu)
     # RoPE fused with the append: the global layer with p-RoPE on a quarter
     # of the pairs, the int8 sliding layer with every pair turning
@@ -1181,6 +1208,21 @@ def main():
         pkv.load_library()
         entry = measure_prefill(workload_spec(args), args.chunk_only, torch.device("cuda", local_rank),
                                 args.steps, args.warmup, not args.no_cpu_baseline)
+        print(json.dumps(entry), flush=True)
+        return 0
+    if args.rope_only:
+        import torch
+        import paged_kv_decode_03_gb300 as pkv
+        torch.cuda.set_device(local_rank)
+        pkv.load_library()
+        dev = torch.device("cuda", local_rank)
+        cpu = not args.no_cpu_baseline
+        entry = {
+            "c5g_rope_append": measure_rope_append(synth.C5_GLOBAL, 1e6, synth.C5_GLOBAL.head_dim // 8,
+                                                   dev, args.steps, args.warmup, cpu),
+            "c5s_rope_append": measure_rope_append(synth.C5_SLIDING, 1e4,
+                                                   synth.C5_SLIDING.head_dim // 2, dev, args.steps,
+                                                   args.warmup, cpu)}
         print(json.dumps(entry), flush=True)
         return 0
     if world > 1:

@@ -437,6 +437,15 @@ typedef struct pkv_layer {
     void *out;           /* [batch][num_q_heads][head_dim], bf16 or fp32 (out_dtype) */
     int32_t window;      /* 0 = global causal layer; > 0 = sliding window (keys [pos-w, pos]) */
     float softmax_scale;
+    /* Optional RoPE fused with the append (paged_kv_append_rope).  With
+     * rope_table not NULL, q is rotated into q_rotated and k_new is rotated
+     * before it is stored, each sequence's new token at position
+     * seq_lens[b] - 1, and the decode reads q_rotated.  All zero: no RoPE. */
+    const float *rope_table;   /* [rope_num_positions][rope_pairs] (cos, sin) pairs */
+    int64_t rope_num_positions;
+    int32_t rope_pairs;        /* rotated pairs, <= head_dim / 2 */
+    int32_t rope_layout;       /* PKV_ROPE_HALVES or PKV_ROPE_INTERLEAVED */
+    void *q_rotated;           /* [batch][num_q_heads][head_dim] bf16, 16-byte aligned; may be q */
 } pkv_layer;
 
 /*
@@ -452,8 +461,9 @@ PKV_API size_t paged_decode_step_workspace_bytes(const pkv_layer *layers, int32_
 /*
  * paged_decode_step -- one decode step of a whole model's attention: for
  * each layer in order, paged_kv_append of the layer's new tokens at
- * slot_mapping, then paged_decode_attention over the layer's pool, all
- * enqueued on `stream` by one call.  (tiniestgpt notes, section 8: a decode
+ * slot_mapping (paged_kv_append_rope at positions seq_lens[b] - 1 for a
+ * layer with a RoPE table), then paged_decode_attention over the layer's
+ * pool, all enqueued on `stream` by one call.  (tiniestgpt notes, section 8: a decode
  * step over static block_table / seq_lens / slot_ids buffers with a host-side
  * length bound, captured once as a CUDA graph and replayed; CS336 lecture 10,
  * local/global section: sliding-window layers interleaved with global ones.)

@@ -54,6 +54,11 @@ class PkvLayerC(ctypes.Structure):
         ("out", ctypes.c_void_p),
         ("window", ctypes.c_int32),
         ("softmax_scale", ctypes.c_float),
+        ("rope_table", ctypes.c_void_p),
+        ("rope_num_positions", ctypes.c_int64),
+        ("rope_pairs", ctypes.c_int32),
+        ("rope_layout", ctypes.c_int32),
+        ("q_rotated", ctypes.c_void_p),
     ]
 
 
@@ -426,7 +431,11 @@ def device_status(clear: bool = True) -> int:
 class DecodeLayer:
     """One layer of a decode step: its pool, query [B, H_q, D] bf16, new
     token K/V [B, H_kv, D] bf16 (v_new None when K and V are one tensor),
-    output [B, H_q, D] (bf16 or fp32), window (0 = global) and softmax scale."""
+    output [B, H_q, D] (bf16 or fp32), window (0 = global) and softmax scale.
+    Optional RoPE fused with the append: ``rope_table`` from
+    paged_rope_cos_sin_table ([npos, pairs, 2]), pairing ``rope_layout``, and
+    ``q_rotated`` ([B, H_q, D] bf16, may be q) that receives the rotated q the
+    decode reads; the new tokens sit at positions seq_lens - 1."""
     pool: PagedKVPool
     q: "object"
     k_new: "object"
@@ -434,11 +443,18 @@ class DecodeLayer:
     out: "object"
     window: int
     softmax_scale: float
+    rope_table: Optional[object] = None
+    rope_layout: int = ROPE_HALVES
+    q_rotated: Optional[object] = None
 
     def c_struct(self) -> PkvLayerC:
+        npos = pairs = 0
+        if self.rope_table is not None:
+            npos, pairs = int(self.rope_table.shape[0]), int(self.rope_table.shape[1])
         return PkvLayerC(self.pool.c_struct(), _dev_ptr(self.q, "q"), _dev_ptr(self.k_new, "k_new"),
                          _dev_ptr(self.v_new, "v_new"), _dev_ptr(self.out, "out"), int(self.window),
-                         float(self.softmax_scale))
+                         float(self.softmax_scale), _dev_ptr(self.rope_table, "rope_table"), npos,
+                         pairs, int(self.rope_layout), _dev_ptr(self.q_rotated, "q_rotated"))
 
 
 def _layers_c(layers):

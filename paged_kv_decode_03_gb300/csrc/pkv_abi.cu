@@ -14,6 +14,7 @@
 
 #include "pkv_device.cuh"
 #include "pkv_internal.h"
+#include "pkv_write.h"
 
 namespace pkv {
 
@@ -374,15 +375,16 @@ PKV_API int paged_rope_cos_sin_table(const double *theta, int32_t rotary_pairs,
     return PKV_OK;
 }
 
-PKV_API int paged_kv_append_rope(const void *q, void *q_out, int32_t num_q_heads, const void *k,
-                                 const void *v, const int64_t *positions,
-                                 const int64_t *slot_mapping, int32_t num_tokens,
-                                 const float *table, int64_t num_positions,
-                                 int32_t rotary_pairs, int32_t layout, const pkv_pool *pool,
-                                 void *stream)
+}  // extern "C"
+
+// RoPE fused with the append at positions[t], or (positions NULL, the decode
+// step) at seq_lens[t] - 1.  Host checks, then one launch.
+static int append_rope_impl(const void *q, void *q_out, int32_t num_q_heads, const void *k,
+                            const void *v, const int64_t *positions, const int32_t *seq_lens,
+                            const int64_t *slot_mapping, int32_t num_tokens, const float *table,
+                            int64_t num_positions, int32_t rotary_pairs, int32_t layout,
+                            const pkv_pool *pool, void *stream)
 {
-    t_last_error.clear();
-    t_launches = 0;
     if (int rc = check_pool(pool))
         return rc;
     if (num_tokens < 0)
@@ -398,11 +400,11 @@ PKV_API int paged_kv_append_rope(const void *q, void *q_out, int32_t num_q_heads
     if (num_tokens == 0)
         return PKV_OK;
     const bool alias = pool->v == nullptr || pool->v == pool->k;
-    if (!k || !slot_mapping || !positions || (!alias && !v) || (q && !q_out) ||
+    if (!k || !slot_mapping || !(positions || seq_lens) || (!alias && !v) || (q && !q_out) ||
         (rotary_pairs > 0 && num_positions > 0 && !table))
         return fail(PKV_E_NULL, "k, v, q_out, positions, slot_mapping or table is NULL");
     if (!aligned(k, 16) || (!alias && !aligned(v, 16)) || !aligned(slot_mapping, 8) ||
-        !aligned(positions, 8) || (q && (!aligned(q, 16) || !aligned(q_out, 16))) ||
+        (positions && !aligned(positions, 8)) || (q && (!aligned(q, 16) || !aligned(q_out, 16))) ||
         (table && !aligned(table, 8)))
         return fail(PKV_E_ALIGN, "q/q_out/k/v must be 16-byte, positions/slot_mapping/table "
                                  "8-byte aligned");
@@ -429,6 +431,7 @@ PKV_API int paged_kv_append_rope(const void *q, void *q_out, int32_t num_q_heads
     r.q = static_cast<const uint16_t *>(q);
     r.q_out = static_cast<uint16_t *>(q_out);
     r.positions = positions;
+    r.seq_lens = seq_lens;
     r.table = reinterpret_cast<const float2 *>(table);
     r.num_positions = num_positions;
     r.num_q_heads = q ? num_q_heads : 0;
@@ -439,6 +442,23 @@ PKV_API int paged_kv_append_rope(const void *q, void *q_out, int32_t num_q_heads
     if (e != cudaSuccess)
         return cuda_fail(e, "append (RoPE) launch");
     return PKV_OK;
+}
+
+extern "C" {
+
+PKV_API int paged_kv_append_rope(const void *q, void *q_out, int32_t num_q_heads, const void *k,
+                                 const void *v, const int64_t *positions,
+                                 const int64_t *slot_mapping, int32_t num_tokens,
+                                 const float *table, int64_t num_positions,
+                                 int32_t rotary_pairs, int32_t layout, const pkv_pool *pool,
+                                 void *stream)
+{
+    t_last_error.clear();
+    t_launches = 0;
+    if (!positions && num_tokens > 0)
+        return fail(PKV_E_NULL, "positions is NULL");
+    return append_rope_impl(q, q_out, num_q_heads, k, v, positions, nullptr, slot_mapping,
+                            num_tokens, table, num_positions, rotary_pairs, layout, pool, stream);
 }
 
 PKV_API int paged_kv_slot_mapping(const pkv_pool *pool, const int32_t *block_table,
@@ -936,6 +956,16 @@ PKV_API int paged_decode_step(const pkv_layer *layers, int32_t num_layers,
             return fail(PKV_E_NULL, "layer %d: k_new or v_new is NULL", l);
         if (!aligned(L.k_new, 16) || (!alias && !aligned(L.v_new, 16)))
             return fail(PKV_E_ALIGN, "layer %d: k_new/v_new must be 16-byte aligned", l);
+        if (L.rope_table) {
+            if (L.rope_pairs < 0 || 2 * L.rope_pairs > L.pool.head_dim || L.rope_num_positions < 0 ||
+                (L.rope_layout != PKV_ROPE_HALVES && L.rope_layout != PKV_ROPE_INTERLEAVED))
+                return fail(PKV_E_ARG, "layer %d: RoPE pairs, positions or layout out of range", l);
+            if (!L.q_rotated)
+                return fail(PKV_E_NULL, "layer %d: q_rotated is NULL", l);
+            if (!aligned(L.q_rotated, 16) || !aligned(L.rope_table, 8))
+                return fail(PKV_E_ALIGN, "layer %d: q_rotated (16 B) or rope_table (8 B) misaligned",
+                            l);
+        }
         const int32_t st = paged_decode_split_tokens(batch, num_q_heads, L.pool.num_kv_heads,
                                                      L.pool.block_size, max_seq_len, L.window,
                                                      split_tokens);
@@ -954,10 +984,20 @@ PKV_API int paged_decode_step(const pkv_layer *layers, int32_t num_layers,
     int launches = 0;
     for (int32_t l = 0; l < num_layers; ++l) {
         const pkv_layer &L = layers[l];
-        int rc = paged_kv_append(L.k_new, L.v_new, slot_mapping, batch, &L.pool, stream);
+        int rc;
+        if (L.rope_table) {
+            t_launches = 0;
+            rc = append_rope_impl(L.q, L.q_rotated, num_q_heads, L.k_new, L.v_new, nullptr,
+                                  seq_lens, slot_mapping, batch, L.rope_table,
+                                  L.rope_num_positions, L.rope_pairs, L.rope_layout, &L.pool,
+                                  stream);
+        } else {
+            rc = paged_kv_append(L.k_new, L.v_new, slot_mapping, batch, &L.pool, stream);
+        }
         launches += t_launches;
         if (rc == PKV_OK) {
-            rc = paged_decode_attention(L.q, &L.pool, block_table, max_blocks_per_seq, seq_lens,
+            rc = paged_decode_attention(L.rope_table ? L.q_rotated : L.q, &L.pool, block_table,
+                                        max_blocks_per_seq, seq_lens,
                                         batch, num_q_heads, max_seq_len, L.window,
                                         L.softmax_scale, split_tokens, workspace, workspace_bytes,
                                         L.out, out_dtype, stream);

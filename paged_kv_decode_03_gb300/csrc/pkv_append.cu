@@ -17,6 +17,7 @@
 
 #include "pkv_device.cuh"
 #include "pkv_internal.h"
+#include "pkv_write.h"
 
 namespace pkv {
 
@@ -246,8 +247,9 @@ __device__ __forceinline__ void rotate_rows(const uint16_t *src, uint16_t *dst, 
     }
 }
 
-// One CTA per token: its q rows rotated into q_out, its k row rotated into
-// shared memory and stored into the pool from there, its v row stored as is.
+// One CTA per token: its v row stored as is (while the table row loads), its
+// q rows rotated into q_out, its k row rotated into shared memory and stored
+// into the pool from there.
 // A negative position is padding (q copied, nothing appended); a position
 // past the table is reported (PKV_DEV_BAD_POSITION) and treated the same.
 template <bool INT8>
@@ -259,11 +261,28 @@ __global__ void __launch_bounds__(APPEND_THREADS) append_rope_kernel(const Appen
     float2 *cs = reinterpret_cast<float2 *>(rope_sm);                        // [pairs]
     uint16_t *krow = reinterpret_cast<uint16_t *>(rope_sm + ((r.pairs * 8 + 15) & ~15));  // [row]
     const int t = blockIdx.x;
-    const int64_t m = r.positions[t];
+    const int64_t qrow = static_cast<int64_t>(r.num_q_heads) * p.head_dim;
+    {
+        // the token's q, k and v rows do not depend on its position: start
+        // bringing them into L2 while the position and the table row load
+        const char *rows[3] = {r.q ? reinterpret_cast<const char *>(r.q + t * qrow) : nullptr,
+                               reinterpret_cast<const char *>(p.k + static_cast<int64_t>(t) * p.row),
+                               p.alias ? nullptr
+                                       : reinterpret_cast<const char *>(p.v + static_cast<int64_t>(t) * p.row)};
+        const int64_t bytes[3] = {qrow * 2, static_cast<int64_t>(p.row) * 2,
+                                  static_cast<int64_t>(p.row) * 2};
+#pragma unroll
+        for (int j = 0; j < 3; ++j)
+            if (rows[j])
+                for (int64_t o = static_cast<int64_t>(threadIdx.x) * 128; o < bytes[j];
+                     o += static_cast<int64_t>(blockDim.x) * 128)
+                    asm volatile("prefetch.global.L2 [%0];" ::"l"(rows[j] + o));
+    }
+    const int64_t m = r.positions ? r.positions[t] : static_cast<int64_t>(r.seq_lens[t]) - 1;
+    const int64_t slot = p.slot_mapping[t];  // loaded beside the position
     const bool valid = m >= 0 && m < r.num_positions;
     if (m >= r.num_positions && threadIdx.x == 0)
         record_error(p.err, PKV_DEV_BAD_POSITION);
-    const int64_t qrow = static_cast<int64_t>(r.num_q_heads) * p.head_dim;
     const uint16_t *qs = r.q ? r.q + t * qrow : nullptr;
     uint16_t *qd = r.q ? r.q_out + t * qrow : nullptr;
     if (!valid) {
@@ -274,24 +293,22 @@ __global__ void __launch_bounds__(APPEND_THREADS) append_rope_kernel(const Appen
     }
     for (int i = threadIdx.x; i < r.pairs; i += blockDim.x)
         cs[i] = r.table[m * r.pairs + i];
+    const bool store = slot >= 0 && slot < p.num_slots;  // uniform over the block
+    if (slot >= p.num_slots && threadIdx.x == 0)
+        record_error(p.err, PKV_DEV_BAD_SLOT);
+    // v needs no rotation: its row goes first, while the table row lands
+    if (store && !p.alias)
+        store_row<INT8>(p, reinterpret_cast<const uint4 *>(p.v + static_cast<int64_t>(t) * p.row),
+                        1, slot, red);
     __syncthreads();
     if (qs)
         rotate_rows(qs, qd, r.num_q_heads, p.head_dim, cs, r.pairs, r.layout);
-    const int64_t slot = p.slot_mapping[t];
-    if (slot < 0)
+    if (!store)
         return;
-    if (slot >= p.num_slots) {
-        if (threadIdx.x == 0)
-            record_error(p.err, PKV_DEV_BAD_SLOT);
-        return;
-    }
     rotate_rows(p.k + static_cast<int64_t>(t) * p.row, krow, p.row / p.head_dim, p.head_dim, cs,
                 r.pairs, r.layout);
     __syncthreads();
     store_row<INT8>(p, reinterpret_cast<const uint4 *>(krow), 0, slot, red);
-    if (!p.alias)
-        store_row<INT8>(p, reinterpret_cast<const uint4 *>(p.v + static_cast<int64_t>(t) * p.row),
-                        1, slot, red);
 }
 
 cudaError_t launch_append(const AppendParams &p, int int8, cudaStream_t s)

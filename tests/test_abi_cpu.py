@@ -222,3 +222,28 @@ def test_rope_validation(lib):
     assert t(None, 4, 10, FAKE, None) == E_NULL
     assert t(FAKE + 4, 4, 10, FAKE, None) == E_ALIGN
     assert t(FAKE, 0, 10, None, None) == 0
+
+
+def test_step_validation(lib):
+    """paged_decode_step checks every layer (and its optional RoPE fields)
+    before anything is launched."""
+    def layer(**kw):
+        d = dict(pool=_pool(), q=FAKE, k_new=FAKE, v_new=FAKE, out=FAKE, window=0,
+                 softmax_scale=0.1, rope_table=None, rope_num_positions=0, rope_pairs=0,
+                 rope_layout=0, q_rotated=None)
+        d.update(kw)
+        return binding.PkvLayerC(**d)
+
+    def step(*layers, slots=FAKE):
+        arr = (binding.PkvLayerC * len(layers))(*layers)
+        return lib.paged_decode_step(arr, len(layers), slots, FAKE, 8, FAKE, 2, 4, 100, 0, None, 0,
+                                     0, None)
+    assert step(layer(), slots=None) == E_NULL
+    assert step(layer(), layer(k_new=None)) == E_NULL
+    assert step(layer(), layer(k_new=FAKE + 8)) == E_ALIGN
+    rope = dict(rope_table=FAKE, rope_num_positions=100, rope_pairs=16, q_rotated=FAKE)
+    assert step(layer(**{**rope, "rope_pairs": 65})) == E_ARG
+    assert step(layer(**{**rope, "rope_layout": 3})) == E_ARG
+    assert step(layer(**{**rope, "q_rotated": None})) == E_NULL
+    assert step(layer(**{**rope, "q_rotated": FAKE + 8})) == E_ALIGN
+    assert step(layer(**{**rope, "rope_table": FAKE + 4})) == E_ALIGN
