@@ -423,9 +423,10 @@ class LayerRun:
         return n
 
     def capture(self):
-        """The step's parts as CUDA graphs, replayed so that the timed region
-        measures the GPU and not the Python loop that enqueues the calls;
-        events between the replays give the per-part device times."""
+        """The whole step as one CUDA graph (what the step time is taken on,
+        as an engine replays a captured step), and its parts as graphs of
+        their own, replayed with events between them for the per-part device
+        times; replays measure the GPU and not the Python loop."""
         import torch
         parts = [None, None, None]
         cap = torch.cuda.Stream()
@@ -435,26 +436,34 @@ class LayerRun:
                 parts[i] = torch.cuda.CUDAGraph()
                 with torch.cuda.graph(parts[i], stream=cap):
                     fn()
+            self.step_graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(self.step_graph, stream=cap):
+                self.step()
         torch.cuda.current_stream().wait_stream(cap)
         torch.cuda.synchronize()
         self.graphs = parts
 
-    def replay(self, ev):
-        ev[0].record()
-        self.graphs[0].replay()
-        ev[1].record()
-        self.graphs[1].replay()
-        ev[2].record()
-        if self.graphs[2] is not None:
-            self.graphs[2].replay()
-        ev[3].record()
-
-
-def part_times(evs):
-    app = statistics.mean(e[0].elapsed_time(e[1]) for e in evs) * 1e3
-    dec = statistics.mean(e[1].elapsed_time(e[2]) for e in evs) * 1e3
-    cmb = statistics.mean(e[2].elapsed_time(e[3]) for e in evs) * 1e3
-    return app, dec, cmb
+    def part_times(self, steps):
+        """Per-part device times (us): append, decode, combine -- each part's
+        graph replayed back to back between two events (every replay redoes
+        the same work: the same tokens into the same slots, the same
+        outputs)."""
+        import torch
+        times = []
+        for g in self.graphs:
+            if g is None:
+                times.append(0.0)
+                continue
+            start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            torch.cuda.synchronize()
+            start.record()
+            for _ in range(steps):
+                g.replay()
+            end.record()
+            torch.cuda.synchronize()
+            times.append(start.elapsed_time(end) / steps * 1e3)
+        app, dec, cmb = times
+        return app, dec, (cmb if self.split_api else 0.0)
 
 
 def run_ours(args, rank, world, local_rank):
@@ -486,9 +495,8 @@ def run_ours(args, rank, world, local_rank):
     run.capture()
 
     for _ in range(3):
-        run.replay([torch.cuda.Event(enable_timing=True) for _ in range(4)])
+        run.step_graph.replay()
     torch.cuda.synchronize()
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
@@ -499,7 +507,7 @@ def run_ours(args, rank, world, local_rank):
     t0 = time.time()
     start.record()
     for i in range(args.steps):
-        run.replay(evs[i])
+        run.step_graph.replay()
     end.record()
     torch.cuda.synchronize()
     t1 = time.time()
@@ -508,9 +516,8 @@ def run_ours(args, rank, world, local_rank):
     clocks = sampler.stop(t0, t1) if sampler else None
     elapsed_ms = max_over_ranks(start.elapsed_time(end), world, dev)
     status = pkv.device_status(clear=True)
-    app_us, dec_us, cmb_us = part_times(evs)
-    if not split_api:
-        cmb_us = 0.0
+    # per-kernel times for the roofline: the parts' graphs with events between
+    app_us, dec_us, cmb_us = run.part_times(args.steps)
     ms_per_step = elapsed_ms / args.steps
     value = whole_job_gbs(step_bytes, ms_per_step, world)
 
@@ -602,7 +609,9 @@ def run_ours(args, rank, world, local_rank):
         "data": "synthetic (seeded N(0,1) bf16 K/V/q; shuffled physical blocks)",
         "config": config_dict(spec, w, st, ns, split_api, world),
         "method": {
-            "timing": "CUDA-graph replays of the step's parts, CUDA events between them",
+            "timing": ("one CUDA graph per step (append + decode), CUDA events around the "
+                       "timed replays; per-kernel times from each part's graph replayed back "
+                       "to back between two events"),
             "decode_kernel": ("tensor cores (tcgen05), persistent stream-K" if tc
                               else "CUDA cores"),
         },
@@ -689,17 +698,16 @@ def measure_layer(spec, w, dev, req, steps, warmup, split_api_allowed=True):
     torch.cuda.synchronize()
     run.capture()
     for _ in range(3):
-        run.replay([torch.cuda.Event(enable_timing=True) for _ in range(4)])
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(steps)]
+        run.step_graph.replay()
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize()
     start.record()
     for i in range(steps):
-        run.replay(evs[i])
+        run.step_graph.replay()
     end.record()
     torch.cuda.synchronize()
     ms = start.elapsed_time(end) / steps
-    app, dec, cmb = part_times(evs)
+    app, dec, cmb = run.part_times(steps)
     peak, _ = peaks()
     achieved = run.decode_kernel_bytes / (dec * 1e-6) / 1e9
     B = spec.batch
