@@ -1,8 +1,8 @@
 """Parity at the full workload sizes, in the launch configuration the
-benchmark times (automatic split length, bf16 output): append/quantise is
-compared bit for bit over the whole pool; attention on a sample of output
-rows that the oracle computes one by one (plus the longest and shortest
-sequences)."""
+benchmark times (automatic split length, bf16 output) and with fp32 outputs:
+append/quantise is compared bit for bit over the whole pool; attention on a
+sample of output rows that the oracle computes one by one (plus the longest
+and shortest sequences)."""
 from __future__ import annotations
 
 import numpy as np
@@ -17,6 +17,7 @@ from tests import _util  # noqa: E402
 pytestmark = pytest.mark.gpu
 
 BF16_TOL = 2e-2
+F32_REL_TOL = 1e-4  # normwise per (b, h) row, fp32 outputs
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -63,6 +64,13 @@ def _full_case(spec, check_pool_bits=True):
     err = _gpu.max_abs_err(got[rows[:, 0], rows[:, 1]], ref)
     assert err <= BF16_TOL, (spec.name, err)
     assert np.all(np.isfinite(got))
+    # fp32 outputs (the parity mode) at full size, on the same sampled rows
+    got32 = _gpu.out_to_f64(step.decode(gp, split_tokens=spec.split_tokens or pkv.SPLIT_AUTO,
+                                        out_f32=True))
+    torch.cuda.synchronize()
+    assert pkv.device_status(clear=True) == 0
+    rel = _gpu.max_row_rel_err(got32[rows[:, 0], rows[:, 1]], ref)
+    assert rel <= F32_REL_TOL, (spec.name, rel)
 
 
 def test_c2_gemma4_sliding_full():
