@@ -1083,13 +1083,6 @@ def per_config(args, dev, main_entry, main_spec, main_w):
 
 
 # --------------------------------------------------------- CPU baseline
-def cores_used():
-    try:
-        return len(os.sched_getaffinity(0))
-    except Exception:
-        return os.cpu_count()
-
-
 def oracle_setup(spec, w):
     import oracle
     k, v, ks, vs = synth.empty_pool_arrays(spec, w.layout)
